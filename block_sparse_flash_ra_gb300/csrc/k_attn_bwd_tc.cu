@@ -1,0 +1,786 @@
+// k_attn_bwd_tc.cu -- block-sparse flash attention backward on tcgen05 tensor
+// cores ("ejKernel ring_attention._ring_splash" module source,
+// _ring_attention_backward: per chunk the gradient is taken with the FINAL
+// out and lse, dq accumulates locally, dk/dv accumulate with their chunk,
+// everything in fp32 and cast back at the end).  Summing over every
+// non-empty tile of every chunk gives, with P = exp(s - lse) on visible
+// pairs and Delta = <dO, O> (from the preprocessing kernel):
+//   dV_j = sum_i P_ij dO_i                      dP_ij = <dO_i, V_j>
+//   dS_ij = P_ij (dP_ij - Delta_i) (1 - tanh^2)  (tanh term only with a cap)
+//   dK_j = scale sum_i dS_ij Q_i                dQ_i = scale sum_j dS_ij K_j
+// dK / dV are summed over the query heads of a kv head (GQA / MQA).
+//
+// Two persistent kernels, both without atomics (deterministic):
+//   dkdv: one work unit per (b, kv head, 128-row kv tile); it walks the G
+//         query heads and the non-empty query tiles of its block-map column.
+//         Thread t owns kv row t = TMEM lane t.  TMEM: S^T [0,128),
+//         dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  P^T and dS^T
+//         (bf16) overwrite the first halves of S^T and dP^T and feed the
+//         dV += P^T dO and dK += dS^T Q products straight from TMEM.
+//   dq:   one work unit per (b, q head, 128-row query tile); it walks the
+//         non-empty kv tiles of its block-map row.  Thread t owns query row
+//         t.  TMEM: S [0,128), dP [128,256), dQ [256,256+D); dS (bf16)
+//         overwrites S and feeds dQ += dS K from TMEM.
+// The dkdv kernel recomputes S and dP per tile and the dq kernel recomputes
+// them again: 7 tile products instead of 5, in exchange for no fp32 atomics.
+#include <math.h>
+
+#include "ra_sched.cuh"
+
+namespace ra {
+namespace {
+
+constexpr uint32_t kIdescT = idesc_bf16(128, 128, false, false); // S^T / dP^T / S / dP
+
+// ====================================================================== dkdv
+template <int D>
+struct DkdvCfg {
+    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kStageBytes = 2 * kTileBytes + 1024; // Q, dO, lse[128], delta[128]
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kTileBytes;
+    static constexpr int kStageOff = 2 * kTileBytes;
+    static constexpr int kStages = 2;
+    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kNumBars = 2 + 2 * kStages + 5;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    // at least 120 KB so that one CTA (which takes all 512 TMEM columns)
+    // occupies an SM on its own
+    static constexpr int kSmem = (kMiscOff + 16 + 1024) > 122880 ? (kMiscOff + 16 + 1024) : 122880;
+    static constexpr uint32_t kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);
+};
+
+struct DkdvBars {
+    uint64_t *kv_full, *kv_empty, *st_full, *st_empty, *s_full, *p_ready, *ds_ready, *acc_ready,
+        *drain;
+};
+
+template <int D>
+__device__ __forceinline__ DkdvBars dkdv_bars(uint8_t *smem)
+{
+    using C = DkdvCfg<D>;
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    DkdvBars r;
+    r.kv_full = b;
+    r.kv_empty = b + 1;
+    r.st_full = b + 2;
+    r.st_empty = r.st_full + C::kStages;
+    r.s_full = r.st_empty + C::kStages;
+    r.p_ready = r.s_full + 1;
+    r.ds_ready = r.p_ready + 1;
+    r.acc_ready = r.ds_ready + 1;
+    r.drain = r.acc_ready + 1;
+    return r;
+}
+
+struct ColUnit {
+    int b, kt, hkv, col, cnt;
+    const int32_t *list; // q tiles of the column
+};
+
+__device__ __forceinline__ ColUnit col_unit(const Problem &p, int u)
+{
+    ColUnit x;
+    x.col = p.bwd_order[u / p.Hkv];
+    x.hkv = u % p.Hkv;
+    x.b = x.col / p.nk;
+    x.kt = x.col - x.b * p.nk;
+    x.cnt = p.bwd_cnt[x.col];
+    x.list = p.bwd_idx + (size_t)x.col * p.nq;
+    return x;
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    Problem p, const float *__restrict__ lse, const float *__restrict__ delta,
+                    __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv)
+{
+    using C = DkdvCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const DkdvBars bars = dkdv_bars<D>(smem);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+    const WaitCtx ctx{abort_flag, p.status, p.timeout_ns};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int U = p.B * p.nk * p.Hkv;
+    const int Gd = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars.kv_full, 1);
+        mbar_init(bars.kv_empty, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bars.st_full + s, 1);
+            mbar_init(bars.st_empty + s, 1);
+        }
+        mbar_init(bars.s_full, 1);
+        mbar_init(bars.p_ready, 128);
+        mbar_init(bars.ds_ready, 128);
+        mbar_init(bars.acc_ready, 1);
+        mbar_init(bars.drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 4) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t n = 0, uk = 0;
+            uint32_t st_issued[C::kStages] = {};
+            bool ok = true;
+            for (int r = 0; ok && r * Gd < U; ++r) {
+                const int u = unit_index(r, blockIdx.x, Gd);
+                if (u >= U) continue;
+                const ColUnit x = col_unit(p, u);
+                if (x.cnt == 0) continue;
+                if (!(ok = mbar_wait(bars.kv_empty, (uk & 1) ^ 1, ctx))) break;
+                mbar_expect_tx(bars.kv_full, 2 * C::kTileBytes);
+                for (int hb = 0; hb < D / 64; ++hb) {
+                    tma_load_4d(smem + C::kKOff + hb * 16384, &tm_k, bars.kv_full, hb * 64, x.hkv,
+                                x.kt * kTile, x.b);
+                    tma_load_4d(smem + C::kVOff + hb * 16384, &tm_v, bars.kv_full, hb * 64, x.hkv,
+                                x.kt * kTile, x.b);
+                }
+                ++uk;
+                for (int gi = 0; ok && gi < p.G; ++gi) {
+                    const int h = x.hkv * p.G + gi;
+                    for (int e = 0; e < x.cnt; ++e) {
+                        const int qt = x.list[e];
+                        const int st = n % C::kStages;
+                        if (!(ok = mbar_wait(bars.st_empty + st, ((n / C::kStages) & 1) ^ 1, ctx))) break;
+                        uint8_t *sb = smem + C::kStageOff + st * C::kStageBytes;
+                        mbar_expect_tx(bars.st_full + st, 2 * C::kTileBytes + 1024);
+                        for (int hb = 0; hb < D / 64; ++hb) {
+                            tma_load_4d(sb + hb * 16384, &tm_q, bars.st_full + st, hb * 64, h,
+                                        qt * kTile, x.b);
+                            tma_load_4d(sb + C::kTileBytes + hb * 16384, &tm_do, bars.st_full + st,
+                                        hb * 64, h, qt * kTile, x.b);
+                        }
+                        const size_t li = ((size_t)x.b * p.Hq + h) * p.Lq + (size_t)qt * kTile;
+                        bulk_load(sb + 2 * C::kTileBytes, lse + li, 512, bars.st_full + st);
+                        bulk_load(sb + 2 * C::kTileBytes + 512, delta + li, 512, bars.st_full + st);
+                        ++st_issued[st];
+                        ++n;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::kStages; ++s)
+                    if (st_issued[s]) wait_drain(bars.st_full + s, (st_issued[s] - 1) & 1, kDrainNs);
+                if (uk) wait_drain(bars.kv_full, (uk - 1) & 1, kDrainNs);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t k_base = smem_u32(smem + C::kKOff);
+            const uint32_t v_base = smem_u32(smem + C::kVOff);
+            uint32_t n = 0, uk = 0;
+            bool ok = true;
+            for (int r = 0; ok && r * Gd < U; ++r) {
+                const int u = unit_index(r, blockIdx.x, Gd);
+                if (u >= U) continue;
+                const ColUnit x = col_unit(p, u);
+                if (x.cnt == 0) continue;
+                if (!(ok = mbar_wait(bars.kv_full, uk & 1, ctx))) break;
+                tc_fence_after();
+                ++uk;
+                const int steps = p.G * x.cnt;
+                for (int i = 0; i < steps; ++i, ++n) {
+                    const int st = n % C::kStages;
+                    if (!(ok = mbar_wait(bars.st_full + st, (n / C::kStages) & 1, ctx))) break;
+                    tc_fence_after();
+                    const uint32_t q_base = smem_u32(smem + C::kStageOff + st * C::kStageBytes);
+                    const uint32_t do_base = q_base + C::kTileBytes;
+                    // S^T = K Q^T and dP^T = V dO^T
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem, sdesc_sw128(k_base + off, 16, 1024),
+                               sdesc_sw128(q_base + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
+                               sdesc_sw128(do_base + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bars.s_full);
+                    // dV += P^T dO   (A = P^T from TMEM, B = dO as a K=q x N=D MN-major tile)
+                    if (!(ok = mbar_wait(bars.p_ready, n & 1, ctx))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts(tmem + C::kColDV, tmem + kk * 8,
+                               sdesc_sw128(do_base + kk * 2048, 16384, 1024), C::kIdescAcc,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+                    // dK += dS^T Q
+                    if (!(ok = mbar_wait(bars.ds_ready, n & 1, ctx))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                               sdesc_sw128(q_base + kk * 2048, 16384, 1024), C::kIdescAcc,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bars.st_empty + st);
+                }
+                if (!ok) break;
+                tc_commit(bars.kv_empty);
+                tc_commit(bars.acc_ready);
+            }
+            tc_commit(bars.drain);
+            wait_drain(bars.drain, 0, kDrainNs);
+        }
+    } else {
+        // ---------------------------------------------------------- softmax-grad
+        const int row = threadIdx.x; // kv row within the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float scale2 = p.scale * kLog2e;
+        const float cap = p.soft_cap;
+        const float cap2 = cap * kLog2e;
+        const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
+        uint32_t n = 0, ua = 0;
+        bool ok = true;
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+        };
+        for (int r = 0; ok && r * Gd < U; ++r) {
+            const int u = unit_index(r, blockIdx.x, Gd);
+            if (u >= U) continue;
+            const ColUnit x = col_unit(p, u);
+            const int kj = x.kt * kTile + row;
+            const size_t orow = (((size_t)x.b * p.Lkv + kj) * p.Hkv + x.hkv) * D;
+            if (x.cnt > 0) {
+                const int my_pos = p.kv_pos ? p.kv_pos[(size_t)x.b * p.Lkv + kj] : kj;
+                const int my_seg = p.kv_seg ? p.kv_seg[(size_t)x.b * p.Lkv + kj] : 0;
+                const int steps = p.G * x.cnt;
+                for (int i = 0; i < steps; ++i, ++n) {
+                    const int qt = x.list[i % x.cnt];
+                    const int st = n % C::kStages;
+                    const float *lse_s = reinterpret_cast<const float *>(
+                        smem + C::kStageOff + st * C::kStageBytes + 2 * C::kTileBytes);
+                    const float *dl_s = lse_s + 128;
+                    const bool partial =
+                        p.tile_class[((size_t)x.b * p.nq + qt) * p.nk + x.kt] == RA_TILE_PARTIAL;
+                    if (!(ok = wait_all(bars.s_full, n & 1))) break;
+                    tc_fence_after();
+                    // ---- P^T (bf16 -> TMEM) and Pc = P * (1 - tanh^2) kept packed
+                    uint32_t pc[64];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float s[64];
+                        tmem_ld32(lane_base + hh * 64, s);
+                        tmem_ld32(lane_base + hh * 64 + 32, s + 32);
+                        tmem_ld_wait();
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int j = 0; j < 64; j += 2) {
+                            float pv[2], cv[2];
+#pragma unroll
+                            for (int z = 0; z < 2; ++z) {
+                                const int ci = hh * 64 + j + z; // q column in the tile
+                                float x2, cg = 1.f;
+                                if (cap > 0.f) {
+                                    const float t = tanh_fast(s[j + z] * scale_over_cap);
+                                    x2 = cap2 * t;
+                                    cg = 1.f - t * t;
+                                } else {
+                                    x2 = s[j + z] * scale2;
+                                }
+                                const float l2 = lse_s[ci] * kLog2e;
+                                float pr = (l2 == -INFINITY) ? 0.f : ex2_approx(x2 - l2);
+                                if (partial) {
+                                    const int qi = qt * kTile + ci;
+                                    const int qs = p.q_seg ? p.q_seg[(size_t)x.b * p.Lq + qi] : 0;
+                                    bool vis = (qs == my_seg) && !(p.q_seg && qs == p.pad_id);
+                                    if (p.causal) {
+                                        const int qp = p.q_pos ? p.q_pos[(size_t)x.b * p.Lq + qi] : qi;
+                                        vis = vis && (qp >= my_pos);
+                                    }
+                                    if (!vis) pr = 0.f;
+                                }
+                                pv[z] = pr;
+                                cv[z] = pr * cg;
+                            }
+                            pk[j >> 1] = pack_bf16x2(pv[0], pv[1]);
+                            pc[hh * 32 + (j >> 1)] = pack_bf16x2(cv[0], cv[1]);
+                        }
+                        tmem_st32(lane_base + hh * 32, pk);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bars.p_ready);
+                    // ---- dS^T = Pc (dP^T - Delta)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float dpv[64];
+                        tmem_ld32(lane_base + C::kColDP + hh * 64, dpv);
+                        tmem_ld32(lane_base + C::kColDP + hh * 64 + 32, dpv + 32);
+                        tmem_ld_wait();
+                        uint32_t dk2[32];
+#pragma unroll
+                        for (int j = 0; j < 64; j += 2) {
+                            const uint32_t w = pc[hh * 32 + (j >> 1)];
+                            const float c0 = __uint_as_float(w << 16);
+                            const float c1 = __uint_as_float(w & 0xffff0000u);
+                            const float d0 = c0 * (dpv[j] - dl_s[hh * 64 + j]);
+                            const float d1 = c1 * (dpv[j + 1] - dl_s[hh * 64 + j + 1]);
+                            dk2[j >> 1] = pack_bf16x2(d0, d1);
+                        }
+                        tmem_st32(lane_base + C::kColDP + hh * 32, dk2);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bars.ds_ready);
+                }
+                if (!ok) break;
+                // ---- epilogue: dV, scale * dK -> bf16
+                if (!(ok = wait_all(bars.acc_ready, ua & 1))) break;
+                ++ua;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float a[32], bk[32];
+                    tmem_ld32(lane_base + C::kColDV + c * 32, a);
+                    tmem_ld32(lane_base + C::kColDK + c * 32, bk);
+                    tmem_ld_wait();
+                    uint4 *dvp = reinterpret_cast<uint4 *>(dv + orow + c * 32);
+                    uint4 *dkp = reinterpret_cast<uint4 *>(dk + orow + c * 32);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        uint4 v, w;
+                        v.x = pack_bf16x2(a[8 * k4 + 0], a[8 * k4 + 1]);
+                        v.y = pack_bf16x2(a[8 * k4 + 2], a[8 * k4 + 3]);
+                        v.z = pack_bf16x2(a[8 * k4 + 4], a[8 * k4 + 5]);
+                        v.w = pack_bf16x2(a[8 * k4 + 6], a[8 * k4 + 7]);
+                        w.x = pack_bf16x2(p.scale * bk[8 * k4 + 0], p.scale * bk[8 * k4 + 1]);
+                        w.y = pack_bf16x2(p.scale * bk[8 * k4 + 2], p.scale * bk[8 * k4 + 3]);
+                        w.z = pack_bf16x2(p.scale * bk[8 * k4 + 4], p.scale * bk[8 * k4 + 5]);
+                        w.w = pack_bf16x2(p.scale * bk[8 * k4 + 6], p.scale * bk[8 * k4 + 7]);
+                        dvp[k4] = v;
+                        dkp[k4] = w;
+                    }
+                }
+            } else {
+                uint4 *dvp = reinterpret_cast<uint4 *>(dv + orow);
+                uint4 *dkp = reinterpret_cast<uint4 *>(dk + orow);
+                for (int k4 = 0; k4 < D / 8; ++k4) {
+                    dvp[k4] = make_uint4(0, 0, 0, 0);
+                    dkp[k4] = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ====================================================================== dq
+template <int D>
+struct DqCfg {
+    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kQOff = 0;
+    static constexpr int kDoOff = kTileBytes;
+    static constexpr int kKOff = 2 * kTileBytes;
+    static constexpr int kStages = 2;
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    static constexpr int kNumBars = 2 + 4 * kStages + 4;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmem = (kMiscOff + 16 + 1024) > 122880 ? (kMiscOff + 16 + 1024) : 122880;
+    static constexpr uint32_t kColDP = 128, kColDQ = 256;
+    static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);
+};
+
+struct DqBars {
+    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *ds_ready,
+        *acc_ready, *drain;
+};
+
+template <int D>
+__device__ __forceinline__ DqBars dq_bars(uint8_t *smem)
+{
+    using C = DqCfg<D>;
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    DqBars r;
+    r.q_full = b;
+    r.q_empty = b + 1;
+    r.k_full = b + 2;
+    r.k_empty = r.k_full + C::kStages;
+    r.v_full = r.k_empty + C::kStages;
+    r.v_empty = r.v_full + C::kStages;
+    r.s_full = r.v_empty + C::kStages;
+    r.ds_ready = r.s_full + 1;
+    r.acc_ready = r.ds_ready + 1;
+    r.drain = r.acc_ready + 1;
+    return r;
+}
+
+struct RowUnit {
+    int b, qt, h, row, cnt;
+    const int32_t *list;
+};
+
+__device__ __forceinline__ RowUnit row_unit(const Problem &p, int u)
+{
+    RowUnit x;
+    x.row = p.fwd_order[u / p.Hq];
+    x.h = u % p.Hq;
+    x.b = x.row / p.nq;
+    x.qt = x.row - x.b * p.nq;
+    x.cnt = p.fwd_cnt[x.row];
+    x.list = p.fwd_idx + (size_t)x.row * p.nk;
+    return x;
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  Problem p, const float *__restrict__ lse, const float *__restrict__ delta,
+                  __nv_bfloat16 *__restrict__ dq)
+{
+    using C = DqCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const DqBars bars = dq_bars<D>(smem);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+    const WaitCtx ctx{abort_flag, p.status, p.timeout_ns};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int U = p.B * p.nq * p.Hq;
+    const int Gd = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bars.k_full + s, 1);
+            mbar_init(bars.k_empty + s, 1);
+            mbar_init(bars.v_full + s, 1);
+            mbar_init(bars.v_empty + s, 1);
+        }
+        mbar_init(bars.s_full, 1);
+        mbar_init(bars.ds_ready, 128);
+        mbar_init(bars.acc_ready, 1);
+        mbar_init(bars.drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 4) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t g = 0, uq = 0;
+            uint32_t k_issued[C::kStages] = {}, v_issued[C::kStages] = {};
+            bool ok = true;
+            for (int r = 0; ok && r * Gd < U; ++r) {
+                const int u = unit_index(r, blockIdx.x, Gd);
+                if (u >= U) continue;
+                const RowUnit x = row_unit(p, u);
+                if (x.cnt == 0) continue;
+                if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
+                mbar_expect_tx(bars.q_full, 2 * C::kTileBytes);
+                for (int hb = 0; hb < D / 64; ++hb) {
+                    tma_load_4d(smem + C::kQOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h,
+                                x.qt * kTile, x.b);
+                    tma_load_4d(smem + C::kDoOff + hb * 16384, &tm_do, bars.q_full, hb * 64, x.h,
+                                x.qt * kTile, x.b);
+                }
+                ++uq;
+                const int g_kv = x.h / p.G;
+                for (int e = 0; e < x.cnt; ++e) {
+                    const int kt = x.list[e];
+                    const int st = g % C::kStages;
+                    const uint32_t ph = (g / C::kStages) & 1;
+                    if (!(ok = mbar_wait(bars.k_empty + st, ph ^ 1, ctx))) break;
+                    mbar_expect_tx(bars.k_full + st, C::kTileBytes);
+                    for (int hb = 0; hb < D / 64; ++hb)
+                        tma_load_4d(smem + C::kKOff + st * C::kTileBytes + hb * 16384, &tm_k,
+                                    bars.k_full + st, hb * 64, g_kv, kt * kTile, x.b);
+                    ++k_issued[st];
+                    if (!(ok = mbar_wait(bars.v_empty + st, ph ^ 1, ctx))) break;
+                    mbar_expect_tx(bars.v_full + st, C::kTileBytes);
+                    for (int hb = 0; hb < D / 64; ++hb)
+                        tma_load_4d(smem + C::kVOff + st * C::kTileBytes + hb * 16384, &tm_v,
+                                    bars.v_full + st, hb * 64, g_kv, kt * kTile, x.b);
+                    ++v_issued[st];
+                    ++g;
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::kStages; ++s) {
+                    if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
+                    if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
+                }
+                if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t q_base = smem_u32(smem + C::kQOff);
+            const uint32_t do_base = smem_u32(smem + C::kDoOff);
+            const uint32_t k_base = smem_u32(smem + C::kKOff);
+            const uint32_t v_base = smem_u32(smem + C::kVOff);
+            uint32_t g = 0, uq = 0;
+            bool ok = true;
+            for (int r = 0; ok && r * Gd < U; ++r) {
+                const int u = unit_index(r, blockIdx.x, Gd);
+                if (u >= U) continue;
+                const RowUnit x = row_unit(p, u);
+                if (x.cnt == 0) continue;
+                if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                tc_fence_after();
+                ++uq;
+                for (int e = 0; e < x.cnt; ++e, ++g) {
+                    const int st = g % C::kStages;
+                    const uint32_t ph = (g / C::kStages) & 1;
+                    if (!(ok = mbar_wait(bars.k_full + st, ph, ctx))) break;
+                    if (!(ok = mbar_wait(bars.v_full + st, ph, ctx))) break;
+                    tc_fence_after();
+                    const uint32_t kb = k_base + st * C::kTileBytes;
+                    const uint32_t vb = v_base + st * C::kTileBytes;
+                    // S = Q K^T, dP = dO V^T
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem, sdesc_sw128(q_base + off, 16, 1024),
+                               sdesc_sw128(kb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem + C::kColDP, sdesc_sw128(do_base + off, 16, 1024),
+                               sdesc_sw128(vb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bars.v_empty + st);
+                    tc_commit(bars.s_full);
+                    if (e == x.cnt - 1) tc_commit(bars.q_empty);
+                    // dQ += dS K   (A = dS from TMEM, B = K as a K=kv x N=D MN-major tile)
+                    if (!(ok = mbar_wait(bars.ds_ready, g & 1, ctx))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts(tmem + C::kColDQ, tmem + kk * 8,
+                               sdesc_sw128(kb + kk * 2048, 16384, 1024), C::kIdescAcc,
+                               (e > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bars.k_empty + st);
+                }
+                if (!ok) break;
+                tc_commit(bars.acc_ready);
+            }
+            tc_commit(bars.drain);
+            wait_drain(bars.drain, 0, kDrainNs);
+        }
+    } else {
+        // ---------------------------------------------------------- softmax-grad
+        const int row = threadIdx.x;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float scale2 = p.scale * kLog2e;
+        const float cap = p.soft_cap;
+        const float cap2 = cap * kLog2e;
+        const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
+        uint32_t g = 0, ua = 0;
+        bool ok = true;
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+        };
+        for (int r = 0; ok && r * Gd < U; ++r) {
+            const int u = unit_index(r, blockIdx.x, Gd);
+            if (u >= U) continue;
+            const RowUnit x = row_unit(p, u);
+            const int qi = x.qt * kTile + row;
+            __nv_bfloat16 *qrow = dq + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D;
+            if (x.cnt > 0) {
+                const size_t li = ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
+                const float l2 = lse[li] * kLog2e;
+                const float dl = delta[li];
+                const int my_pos = p.q_pos ? p.q_pos[(size_t)x.b * p.Lq + qi] : qi;
+                const int my_seg = p.q_seg ? p.q_seg[(size_t)x.b * p.Lq + qi] : 0;
+                const bool my_pad = p.q_seg && my_seg == p.pad_id;
+                const uint8_t *crow = p.tile_class + (size_t)x.row * p.nk;
+                for (int e = 0; e < x.cnt; ++e, ++g) {
+                    const int kt = x.list[e];
+                    const bool partial = crow[kt] == RA_TILE_PARTIAL;
+                    if (!(ok = wait_all(bars.s_full, g & 1))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float s[64], dpv[64];
+                        tmem_ld32(lane_base + hh * 64, s);
+                        tmem_ld32(lane_base + hh * 64 + 32, s + 32);
+                        tmem_ld32(lane_base + C::kColDP + hh * 64, dpv);
+                        tmem_ld32(lane_base + C::kColDP + hh * 64 + 32, dpv + 32);
+                        tmem_ld_wait();
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int j = 0; j < 64; j += 2) {
+                            float dsv[2];
+#pragma unroll
+                            for (int z = 0; z < 2; ++z) {
+                                const int cj = hh * 64 + j + z;
+                                float x2, cg = 1.f;
+                                if (cap > 0.f) {
+                                    const float t = tanh_fast(s[j + z] * scale_over_cap);
+                                    x2 = cap2 * t;
+                                    cg = 1.f - t * t;
+                                } else {
+                                    x2 = s[j + z] * scale2;
+                                }
+                                float pr = (l2 == -INFINITY) ? 0.f : ex2_approx(x2 - l2);
+                                if (partial) {
+                                    const int kj = kt * kTile + cj;
+                                    const int ks = p.kv_seg ? p.kv_seg[(size_t)x.b * p.Lkv + kj] : 0;
+                                    bool vis = (ks == my_seg) && !my_pad;
+                                    if (p.causal) {
+                                        const int kp = p.kv_pos ? p.kv_pos[(size_t)x.b * p.Lkv + kj] : kj;
+                                        vis = vis && (my_pos >= kp);
+                                    }
+                                    if (!vis) pr = 0.f;
+                                }
+                                dsv[z] = pr * cg * (dpv[j + z] - dl);
+                            }
+                            pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                        }
+                        tmem_st32(lane_base + hh * 32, pk);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bars.ds_ready);
+                }
+                if (!ok) break;
+                if (!(ok = wait_all(bars.acc_ready, ua & 1))) break;
+                ++ua;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float a[32];
+                    tmem_ld32(lane_base + C::kColDQ + c * 32, a);
+                    tmem_ld_wait();
+                    uint4 *dst = reinterpret_cast<uint4 *>(qrow + c * 32);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        uint4 v;
+                        v.x = pack_bf16x2(p.scale * a[8 * k4 + 0], p.scale * a[8 * k4 + 1]);
+                        v.y = pack_bf16x2(p.scale * a[8 * k4 + 2], p.scale * a[8 * k4 + 3]);
+                        v.z = pack_bf16x2(p.scale * a[8 * k4 + 4], p.scale * a[8 * k4 + 5]);
+                        v.w = pack_bf16x2(p.scale * a[8 * k4 + 6], p.scale * a[8 * k4 + 7]);
+                        dst[k4] = v;
+                    }
+                }
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(qrow);
+                for (int k4 = 0; k4 < D / 8; ++k4) dst[k4] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+} // namespace
+
+int bwd_dkdv_smem_bytes(int D) { return D == 64 ? DkdvCfg<64>::kSmem : DkdvCfg<128>::kSmem; }
+int bwd_dq_smem_bytes(int D) { return D == 64 ? DqCfg<64>::kSmem : DqCfg<128>::kSmem; }
+
+cudaError_t bwd_tc_set_attributes(int D)
+{
+    cudaError_t e;
+    if (D == 64) {
+        e = cudaFuncSetAttribute(bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 DkdvCfg<64>::kSmem);
+        if (e != cudaSuccess) return e;
+        return cudaFuncSetAttribute(bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    DqCfg<64>::kSmem);
+    }
+    e = cudaFuncSetAttribute(bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkdvCfg<128>::kSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                DqCfg<128>::kSmem);
+}
+
+cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *tm_k,
+                               const void *tm_v, const void *tm_do, const float *lse,
+                               const float *delta, void *dk, void *dv, int num_sms,
+                               cudaStream_t s)
+{
+    const int U = p.B * p.nk * p.Hkv;
+    const int grid = U < num_sms ? U : num_sms;
+    const CUtensorMap &q = *static_cast<const CUtensorMap *>(tm_q);
+    const CUtensorMap &k = *static_cast<const CUtensorMap *>(tm_k);
+    const CUtensorMap &v = *static_cast<const CUtensorMap *>(tm_v);
+    const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
+    __nv_bfloat16 *gk = static_cast<__nv_bfloat16 *>(dk), *gv = static_cast<__nv_bfloat16 *>(dv);
+    if (p.D == 64)
+        bwd_dkdv_kernel<64><<<grid, 192, DkdvCfg<64>::kSmem, s>>>(q, k, v, d, p, lse, delta, gk, gv);
+    else
+        bwd_dkdv_kernel<128><<<grid, 192, DkdvCfg<128>::kSmem, s>>>(q, k, v, d, p, lse, delta, gk, gv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
+                             const void *tm_v, const void *tm_do, const float *lse,
+                             const float *delta, void *dq, int num_sms, cudaStream_t s)
+{
+    const int U = p.B * p.nq * p.Hq;
+    const int grid = U < num_sms ? U : num_sms;
+    const CUtensorMap &q = *static_cast<const CUtensorMap *>(tm_q);
+    const CUtensorMap &k = *static_cast<const CUtensorMap *>(tm_k);
+    const CUtensorMap &v = *static_cast<const CUtensorMap *>(tm_v);
+    const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
+    __nv_bfloat16 *gq = static_cast<__nv_bfloat16 *>(dq);
+    if (p.D == 64)
+        bwd_dq_kernel<64><<<grid, 192, DqCfg<64>::kSmem, s>>>(q, k, v, d, p, lse, delta, gq);
+    else
+        bwd_dq_kernel<128><<<grid, 192, DqCfg<128>::kSmem, s>>>(q, k, v, d, p, lse, delta, gq);
+    return cudaGetLastError();
+}
+
+} // namespace ra

@@ -1,0 +1,533 @@
+// k_attn_fwd_tc.cu -- block-sparse flash attention forward on the 5th-gen
+// tensor cores (tcgen05 + TMEM, TMA-fed), with the ring (out, lse) merge
+// fused into the epilogue of every virtual shard.
+//
+// What it computes ("ejKernel ring_attention._ring_splash" module source,
+// _ring_attention_forward and _update_out_and_lse; Kvax "Flash Attention for
+// JAX", flash_attention): for each (b, h, 128-row query tile) on virtual
+// device d, the KV shards are visited in ring order s = (d - t) mod N; inside
+// a shard the non-empty 128-row KV tiles of the block map are processed with
+// an online softmax (S = Q K^T on tensor cores, scale, soft cap, mask of
+// partial tiles, P = exp2(S - m) in bf16, O_acc += P V on tensor cores); at
+// the shard's end the partial (O_s = O_acc / l, lse_s) -- with the sink in
+// the denominator at t = 0 -- is merged into the running (O_run, lse_run) by
+// the sigmoid/softplus update.  Output is bf16, lse fp32.
+//
+// Design (one CTA per SM, persistent, longest-row-first static schedule):
+//   warps 0-3  softmax / merge / epilogue; thread t owns query row t, which
+//              is TMEM lane t (warp w may only touch lanes 32w..32w+31)
+//   warp 4     TMA producer: Q once per work unit, K and V tiles into a
+//              kStages-deep ring of shared-memory stages
+//   warp 5     TMEM allocator and single-thread MMA issuer
+// TMEM (512 columns x 128 lanes, fp32):
+//   [0,128)   S buffer 0   (P of that tile overwrites its first 64 columns)
+//   [128,256) S buffer 1
+//   [256,256+D)      O_acc  shard accumulator
+//   [256+D,256+2D)   O_run  running merged output of the ring
+// MMA issue order per tile g: S(g) = Q K(g)^T, then O_acc += P(g-1) V(g-1),
+// so the softmax of tile g overlaps the PV product of tile g-1.  The O_acc
+// rescale after a row-max increase is lazy (only when the max grows by more
+// than 2^8) and waits for the previous PV product.
+#include <math.h>
+
+#include "ra_sched.cuh"
+
+namespace ra {
+namespace {
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kTileBytes = kTile * D * 2; // one 128-row bf16 tile
+    static constexpr int kStages = (D == 128) ? 3 : 4;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kTileBytes;
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    static constexpr int kNumBars = 2 + 4 * kStages + 5 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemUsed = kMiscOff + 16;
+    static constexpr int kSmem = kSmemUsed + 1024; // slack for 1024-byte alignment
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColO = 256;
+    static constexpr uint32_t kColRun = 256 + D;
+    static constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
+};
+
+struct Bars {
+    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full, *pv_done,
+        *drain;
+};
+
+template <int D>
+__device__ __forceinline__ Bars carve_bars(uint8_t *smem)
+{
+    using C = FwdCfg<D>;
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    Bars r;
+    r.q_full = b;
+    r.q_empty = b + 1;
+    r.k_full = b + 2;
+    r.k_empty = r.k_full + C::kStages;
+    r.v_full = r.k_empty + C::kStages;
+    r.v_empty = r.v_full + C::kStages;
+    r.s_full = r.v_empty + C::kStages;
+    r.p_full = r.s_full + 2;
+    r.pv_done = r.p_full + 2;
+    r.drain = r.pv_done + 1;
+    return r;
+}
+
+// Work unit u -> (row id b*nq+qt from the longest-first order, head h).
+struct Unit {
+    int b, qt, h, row, cnt, dev;
+    const int32_t *list;
+};
+
+__device__ __forceinline__ Unit unit_of(const Problem &p, int u)
+{
+    Unit x;
+    x.row = p.fwd_order[u / p.Hq];
+    x.h = u % p.Hq;
+    x.b = x.row / p.nq;
+    x.qt = x.row - x.b * p.nq;
+    x.cnt = p.fwd_cnt[x.row];
+    x.dev = x.qt / p.tq;
+    x.list = p.fwd_idx + (size_t)x.row * p.nk;
+    return x;
+}
+
+// Range [lo, hi) of the unit's tile list that lies in KV shard `src`.
+__device__ __forceinline__ void shard_range(const Problem &p, const Unit &x, int src, int &lo,
+                                            int &hi)
+{
+    lo = lower_bound_i32(x.list, x.cnt, src * p.tk);
+    hi = lower_bound_i32(x.list, x.cnt, (src + 1) * p.tk);
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, Problem p,
+                  __nv_bfloat16 *__restrict__ out, float *__restrict__ lse)
+{
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const Bars bars = carve_bars<D>(smem);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+    const WaitCtx ctx{abort_flag, p.status, p.timeout_ns};
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int U = p.B * p.nq * p.Hq;
+    const int G = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bars.k_full + s, 1);
+            mbar_init(bars.k_empty + s, 1);
+            mbar_init(bars.v_full + s, 1);
+            mbar_init(bars.v_empty + s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bars.s_full + s, 1);
+            mbar_init(bars.p_full + s, 128);
+        }
+        mbar_init(bars.pv_done, 1);
+        mbar_init(bars.drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_holder, C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t g = 0, uq = 0;
+            uint32_t k_issued[C::kStages] = {}, v_issued[C::kStages] = {};
+            bool ok = true;
+            for (int r = 0; ok && r * G < U; ++r) {
+                const int u = unit_index(r, blockIdx.x, G);
+                if (u >= U) continue;
+                const Unit x = unit_of(p, u);
+                if (x.cnt == 0) continue;
+                if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
+                mbar_expect_tx(bars.q_full, C::kTileBytes);
+                for (int hb = 0; hb < D / 64; ++hb)
+                    tma_load_4d(smem + C::kQOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h,
+                                x.qt * kTile, x.b);
+                ++uq;
+                const int g_kv = x.h / p.G;
+                for (int t = 0; ok && t < p.N; ++t) {
+                    int lo, hi;
+                    shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
+                    for (int e = lo; e < hi; ++e) {
+                        const int kt = x.list[e];
+                        const int st = g % C::kStages;
+                        const uint32_t ph = (g / C::kStages) & 1;
+                        if (!(ok = mbar_wait(bars.k_empty + st, ph ^ 1, ctx))) break;
+                        mbar_expect_tx(bars.k_full + st, C::kTileBytes);
+                        for (int hb = 0; hb < D / 64; ++hb)
+                            tma_load_4d(smem + C::kKOff + st * C::kTileBytes + hb * 16384, &tm_k,
+                                        bars.k_full + st, hb * 64, g_kv, kt * kTile, x.b);
+                        ++k_issued[st];
+                        if (!(ok = mbar_wait(bars.v_empty + st, ph ^ 1, ctx))) break;
+                        mbar_expect_tx(bars.v_full + st, C::kTileBytes);
+                        for (int hb = 0; hb < D / 64; ++hb)
+                            tma_load_4d(smem + C::kVOff + st * C::kTileBytes + hb * 16384, &tm_v,
+                                        bars.v_full + st, hb * 64, g_kv, kt * kTile, x.b);
+                        ++v_issued[st];
+                        ++g;
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                for (int s = 0; s < C::kStages; ++s) {
+                    if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
+                    if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
+                }
+                if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t q_base = smem_u32(smem + C::kQOff);
+            const uint32_t k_base = smem_u32(smem + C::kKOff);
+            const uint32_t v_base = smem_u32(smem + C::kVOff);
+            uint32_t g = 0, uq = 0;
+            bool have_prev = false, prev_first = false;
+            uint32_t prev_g = 0;
+            bool ok = true;
+            auto issue_pv = [&](uint32_t pg, bool first) -> bool {
+                const int sb = pg & 1;
+                if (!mbar_wait(bars.p_full + sb, (pg >> 1) & 1, ctx)) return false;
+                const int st = pg % C::kStages;
+                if (!mbar_wait(bars.v_full + st, (pg / C::kStages) & 1, ctx)) return false;
+                tc_fence_after();
+                const uint32_t vb = v_base + st * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, 16384, 1024);
+                    mma_ts(tmem + C::kColO, tmem + sb * 128 + kk * 8, bdesc, C::kIdescPV,
+                           (kk > 0 || !first) ? 1u : 0u);
+                }
+                tc_commit(bars.v_empty + st);
+                tc_commit(bars.pv_done);
+                return true;
+            };
+            for (int r = 0; ok && r * G < U; ++r) {
+                const int u = unit_index(r, blockIdx.x, G);
+                if (u >= U) continue;
+                const Unit x = unit_of(p, u);
+                if (x.cnt == 0) continue;
+                if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                tc_fence_after();
+                ++uq;
+                int done = 0;
+                for (int t = 0; ok && t < p.N; ++t) {
+                    int lo, hi;
+                    shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
+                    for (int e = lo; e < hi; ++e) {
+                        const int st = g % C::kStages;
+                        if (!(ok = mbar_wait(bars.k_full + st, (g / C::kStages) & 1, ctx))) break;
+                        tc_fence_after();
+                        const int sb = g & 1;
+                        const uint32_t kb = k_base + st * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_ss(tmem + sb * 128, sdesc_sw128(q_base + off, 16, 1024),
+                                   sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bars.k_empty + st);
+                        tc_commit(bars.s_full + sb);
+                        if (++done == x.cnt) tc_commit(bars.q_empty);
+                        if (have_prev && !(ok = issue_pv(prev_g, prev_first))) break;
+                        have_prev = true;
+                        prev_g = g;
+                        prev_first = (e == lo);
+                        ++g;
+                    }
+                }
+            }
+            if (ok && have_prev) ok = issue_pv(prev_g, prev_first);
+            // all issued MMAs must finish before TMEM is released
+            tc_commit(bars.drain);
+            wait_drain(bars.drain, 0, kDrainNs);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int row = threadIdx.x; // 0..127 == TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float scale2 = p.scale * kLog2e;
+        const float cap = p.soft_cap;
+        const float cap2 = cap * kLog2e;
+        const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
+        uint32_t g = 0, pv_seen = 0;
+        bool ok = true;
+        // waits of the softmax warps are made warp-uniform, so that no warp
+        // reaches a .sync.aligned tcgen05 instruction with some lanes gone
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+        };
+        auto wait_pv_upto = [&](uint32_t n) -> bool {
+            while (pv_seen < n) {
+                if (!wait_all(bars.pv_done, pv_seen & 1)) return false;
+                ++pv_seen;
+            }
+            return true;
+        };
+        for (int r = 0; ok && r * G < U; ++r) {
+            const int u = unit_index(r, blockIdx.x, G);
+            if (u >= U) continue;
+            const Unit x = unit_of(p, u);
+            const int qi = x.qt * kTile + row;
+            __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D;
+            float *lrow = lse + ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
+            const bool has_sink = p.sinks != nullptr;
+            const float sink2 = has_sink ? p.sinks[x.h] * kLog2e : 0.f;
+            float lse_run = -INFINITY;
+            bool orun_set = false; // uniform: O_run columns hold this unit's data
+            if (x.cnt > 0) {
+                const int my_pos = p.q_pos ? p.q_pos[(size_t)x.b * p.Lq + qi] : qi;
+                const int my_seg = p.q_seg ? p.q_seg[(size_t)x.b * p.Lq + qi] : 0;
+                const bool my_pad = p.q_seg && my_seg == p.pad_id;
+                const uint8_t *crow = p.tile_class + (size_t)x.row * p.nk;
+                for (int t = 0; ok && t < p.N; ++t) {
+                    int lo, hi;
+                    shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
+                    const bool sink_here = has_sink && t == 0;
+                    if (lo == hi) {
+                        // empty shard: partial is (0, -inf), or (0, sink) at t = 0
+                        if (sink_here) {
+                            const float ls = sink2 * kLn2;
+                            if (lse_run == -INFINITY) lse_run = ls;
+                            else lse_run = lse_run + softplus_f(ls - lse_run);
+                            // O_run = O_run * (1 - w): only possible when t == 0, so O_run == 0
+                        }
+                        continue;
+                    }
+                    float m_ref = -INFINITY, l = 0.f;
+                    for (int e = lo; ok && e < hi; ++e) {
+                        const int kt = x.list[e];
+                        const bool partial = crow[kt] == RA_TILE_PARTIAL;
+                        const int sb = g & 1;
+                        if (!(ok = wait_all(bars.s_full + sb, (g >> 1) & 1))) break;
+                        tc_fence_after();
+                        float s[128];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + sb * 128 + c * 32, s + c * 32);
+                        tmem_ld_wait();
+                        if (cap > 0.f) {
+#pragma unroll
+                            for (int j = 0; j < 128; ++j) s[j] = cap2 * tanh_fast(s[j] * scale_over_cap);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 128; ++j) s[j] *= scale2;
+                        }
+                        if (partial) {
+                            const int j0 = kt * kTile;
+                            const int4 *kp4 = p.kv_pos
+                                ? reinterpret_cast<const int4 *>(p.kv_pos + (size_t)x.b * p.Lkv + j0)
+                                : nullptr;
+                            const int4 *ks4 = p.kv_seg
+                                ? reinterpret_cast<const int4 *>(p.kv_seg + (size_t)x.b * p.Lkv + j0)
+                                : nullptr;
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) {
+                                int4 pv = kp4 ? __ldg(kp4 + jj)
+                                              : make_int4(j0 + 4 * jj, j0 + 4 * jj + 1,
+                                                          j0 + 4 * jj + 2, j0 + 4 * jj + 3);
+                                int4 sv = ks4 ? __ldg(ks4 + jj) : make_int4(0, 0, 0, 0);
+                                const int pj[4] = {pv.x, pv.y, pv.z, pv.w};
+                                const int sj[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    bool vis = (sj[q4] == my_seg) && !my_pad;
+                                    if (p.causal) vis = vis && (my_pos >= pj[q4]);
+                                    if (!vis) s[4 * jj + q4] = -INFINITY;
+                                }
+                            }
+                        }
+                        float mx[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) mx[k] = s[k];
+#pragma unroll
+                        for (int j = 8; j < 128; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+                        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                        const float m_new = fmaxf(m_ref, tmax);
+                        const bool need = (m_ref != -INFINITY) && (m_new > m_ref + 8.f);
+                        if (m_ref == -INFINITY) m_ref = m_new;
+                        if (__any_sync(0xffffffffu, need)) {
+                            // rescale O_acc: the previous PV product must be complete
+                            if (!(ok = wait_pv_upto(g))) break;
+                            tc_fence_after();
+                            const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
+                            if (need) {
+                                l *= f;
+                                m_ref = m_new;
+                            }
+#pragma unroll
+                            for (int c = 0; c < D / 32; ++c) {
+                                float o[32];
+                                tmem_ld32(lane_base + C::kColO + c * 32, o);
+                                tmem_ld_wait();
+                                uint32_t w32[32];
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) w32[j] = __float_as_uint(o[j] * f);
+                                tmem_st32(lane_base + C::kColO + c * 32, w32);
+                            }
+                            tmem_st_wait();
+                        }
+                        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        uint32_t pk[64];
+#pragma unroll
+                        for (int j = 0; j < 128; j += 2) {
+                            const float a = ex2_approx(s[j] - m_use);
+                            const float b2 = ex2_approx(s[j + 1] - m_use);
+                            ls[(j >> 1) & 7] += a + b2;
+                            pk[j >> 1] = pack_bf16x2(a, b2);
+                        }
+                        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                        tmem_st32(lane_base + sb * 128, pk);
+                        tmem_st32(lane_base + sb * 128 + 32, pk + 32);
+                        tmem_st_wait();
+                        // PV(g-1) must be complete before P(g) is published
+                        if (!(ok = wait_pv_upto(g))) break;
+                        tc_fence_before();
+                        mbar_arrive(bars.p_full + sb);
+                        ++g;
+                    }
+                    if (!ok) break;
+                    // ---- shard end: normalise, add the sink (t == 0), merge
+                    if (!(ok = wait_pv_upto(g))) break;
+                    tc_fence_after();
+                    float m_fin = m_ref, fac = 1.f;
+                    if (sink_here) {
+                        m_fin = fmaxf(m_ref, sink2);
+                        fac = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_fin);
+                        l = l * fac + ex2_approx(sink2 - m_fin);
+                    }
+                    float lse_s, inv;
+                    if (l > 0.f) {
+                        lse_s = (m_fin + log2f(l)) * kLn2;
+                        inv = fac / l;
+                    } else {
+                        lse_s = -INFINITY;
+                        inv = 0.f;
+                    }
+                    const bool first = (lse_run == -INFINITY);
+                    const float w = first ? 1.f : sigmoid_f(lse_s - lse_run);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float a[32], cur[32];
+                        tmem_ld32(lane_base + C::kColO + c * 32, a);
+                        if (orun_set) tmem_ld32(lane_base + C::kColRun + c * 32, cur);
+                        tmem_ld_wait();
+                        uint32_t nv[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float os = a[j] * inv;
+                            const float cv = orun_set ? cur[j] : 0.f;
+                            nv[j] = __float_as_uint(first ? os : cv - w * (cv - os));
+                        }
+                        tmem_st32(lane_base + C::kColRun + c * 32, nv);
+                    }
+                    tmem_st_wait();
+                    lse_run = first ? lse_s : lse_run + softplus_f(lse_s - lse_run);
+                    orun_set = true;
+                }
+                if (!ok) break;
+            } else if (has_sink) {
+                lse_run = sink2 * kLn2;
+            }
+            // ---- epilogue: O_run -> bf16, lse
+            if (orun_set) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float a[32];
+                    tmem_ld32(lane_base + C::kColRun + c * 32, a);
+                    tmem_ld_wait();
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint4 v;
+                        v.x = pack_bf16x2(a[8 * k + 0], a[8 * k + 1]);
+                        v.y = pack_bf16x2(a[8 * k + 2], a[8 * k + 3]);
+                        v.z = pack_bf16x2(a[8 * k + 4], a[8 * k + 5]);
+                        v.w = pack_bf16x2(a[8 * k + 6], a[8 * k + 7]);
+                        dst[k] = v;
+                    }
+                }
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+                for (int k = 0; k < D / 8; ++k) dst[k] = make_uint4(0, 0, 0, 0);
+            }
+            *lrow = lse_run;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+} // namespace
+
+int fwd_tc_smem_bytes(int D)
+{
+    return D == 64 ? FwdCfg<64>::kSmem : FwdCfg<128>::kSmem;
+}
+
+cudaError_t fwd_tc_set_attributes(int D)
+{
+    if (D == 64)
+        return cudaFuncSetAttribute(fwd_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    FwdCfg<64>::kSmem);
+    return cudaFuncSetAttribute(fwd_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<128>::kSmem);
+}
+
+cudaError_t launch_fwd_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,
+                          void *out, float *lse, int num_sms, cudaStream_t s)
+{
+    const int U = p.B * p.nq * p.Hq;
+    const int grid = U < num_sms ? U : num_sms;
+    const CUtensorMap &q = *static_cast<const CUtensorMap *>(tm_q);
+    const CUtensorMap &k = *static_cast<const CUtensorMap *>(tm_k);
+    const CUtensorMap &v = *static_cast<const CUtensorMap *>(tm_v);
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
+    if (p.D == 64)
+        fwd_tc_kernel<64><<<grid, 192, FwdCfg<64>::kSmem, s>>>(q, k, v, p, o, lse);
+    else
+        fwd_tc_kernel<128><<<grid, 192, FwdCfg<128>::kSmem, s>>>(q, k, v, p, o, lse);
+    return cudaGetLastError();
+}
+
+} // namespace ra

@@ -1,0 +1,101 @@
+// k_bwd_pre.cu -- backward preprocessing ("ejKernel ring_attention._ring_splash"
+// module source, _ring_attention_backward: dO widened to fp32, dsinks
+// accumulated and summed over the ring):
+//   Delta[b, h, i] = <dO[b, i, h, :], O[b, i, h, :]>           (fp32)
+//   dsinks[h]      = - sum_{b, i} exp(sink_h - lse[b, h, i]) * Delta[b, h, i]
+// The dsinks sum is taken in two deterministic passes: per-(b, q-tile)
+// partials, then one block per head.  HBM-bound: reads O and dO once.
+#include <cuda_bf16.h>
+
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x)
+{
+    return x;
+}
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x)
+{
+    return __bfloat162float(x);
+}
+
+// grid (nq, Hq, B), 128 threads: warp w handles rows w, w+4, ... of the tile.
+template <typename T>
+__global__ void __launch_bounds__(128) bwd_pre_kernel(Problem p, const T *__restrict__ out,
+                                                      const T *__restrict__ dout,
+                                                      const float *__restrict__ lse,
+                                                      float *__restrict__ delta,
+                                                      float *__restrict__ dsink_part)
+{
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const float sink = p.sinks ? p.sinks[h] : 0.f;
+    float ds = 0.f;
+    for (int r = wid; r < kTile; r += 4) {
+        const int i = qt * kTile + r;
+        const size_t row = (((size_t)b * p.Lq + i) * p.Hq + h) * p.D;
+        float acc = 0.f;
+        for (int d = lane; d < p.D; d += 32) acc += to_f(out[row + d]) * to_f(dout[row + d]);
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        const size_t li = ((size_t)b * p.Hq + h) * p.Lq + i;
+        if (lane == 0) {
+            delta[li] = acc;
+            if (p.sinks) {
+                const float l = lse[li];
+                if (l != -INFINITY) ds += __expf(sink - l) * acc;
+            }
+        }
+    }
+    if (p.sinks) {
+        __shared__ float w[4];
+        if (lane == 0) w[wid] = ds;
+        __syncthreads();
+        if (threadIdx.x == 0)
+            dsink_part[(size_t)h * p.B * p.nq + (size_t)b * p.nq + qt] = w[0] + w[1] + w[2] + w[3];
+    }
+}
+
+// one block per head: dsinks[h] = -sum of its partials (fixed order)
+__global__ void __launch_bounds__(256) dsink_reduce_kernel(const float *part, int n, float *dsinks)
+{
+    const int h = blockIdx.x;
+    float s = 0.f;
+    for (int i = threadIdx.x; i < n; i += 256) s += part[(size_t)h * n + i];
+    __shared__ float w[256];
+    w[threadIdx.x] = s;
+    __syncthreads();
+    for (int k = 128; k > 0; k >>= 1) {
+        if ((int)threadIdx.x < k) w[threadIdx.x] += w[threadIdx.x + k];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) dsinks[h] = -w[0];
+}
+
+} // namespace
+
+cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, int dtype,
+                           const float *lse, float *delta, float *dsink_part, float *dsinks,
+                           cudaStream_t s)
+{
+    const dim3 grid(p.nq, p.Hq, p.B);
+    if (dtype == RA_BF16)
+        bwd_pre_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
+            p, static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout),
+            lse, delta, dsink_part);
+    else
+        bwd_pre_kernel<float><<<grid, 128, 0, s>>>(p, static_cast<const float *>(out),
+                                                   static_cast<const float *>(dout), lse, delta,
+                                                   dsink_part);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !p.sinks) return e;
+    dsink_reduce_kernel<<<p.Hq, 256, 0, s>>>(dsink_part, p.B * p.nq, dsinks);
+    return cudaGetLastError();
+}
+
+} // namespace ra

@@ -1,0 +1,284 @@
+// k_mask.cu -- block map on the 128 x 128 tile grid: the counterpart of the
+// pages' MaskInfo ("ejKernel ring_attention._ring_splash" module source,
+// make_ring_attention: forward and dkv mask infos) and of Kvax
+// create_attention_mask (block-wise mask from positions and segment ids,
+// padding-only blocks skipped).  Integer work, bit-exact:
+//   class(qt, kt) = EMPTY if no pair is visible, FULL if all are, else PARTIAL
+// with visible(i, j) = same non-padding segment && (!causal || q_pos >= kv_pos).
+//
+// 1. tile_summary: per 128-row tile, min / max segment id and position over
+//    the non-padding rows and the padding count.
+// 2. classify_rows: one block per (b, qt).  Tiles whose class follows
+//    exactly from the summaries (disjoint segment ranges; one common segment,
+//    where the causal predicate reduces to comparing position ranges) are
+//    classified from them; the rest are counted pair by pair.  The block then
+//    compacts the non-empty kt of its row into fwd_idx.
+// 3. columns: one block per (b, kt) compacts the non-empty qt into bwd_idx.
+// 4. order: stable counting sort of rows (columns) by descending count.
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+struct TileSum {
+    int seg_min, seg_max, pos_min, pos_max, npad;
+};
+
+__device__ __forceinline__ int seg_at(const int32_t *seg, int b, int L, int i)
+{
+    return seg ? seg[(size_t)b * L + i] : 0;
+}
+__device__ __forceinline__ int pos_at(const int32_t *pos, int b, int L, int i)
+{
+    return pos ? pos[(size_t)b * L + i] : i;
+}
+
+// grid (ntiles, B), 128 threads: thread i looks at row tile*128 + i.
+__global__ void __launch_bounds__(128) tile_summary_kernel(const int32_t *seg, const int32_t *pos,
+                                                           int L, int pad_id, TileSum *out)
+{
+    const int b = blockIdx.y, t = blockIdx.x, i = t * kTile + threadIdx.x;
+    const int s = seg_at(seg, b, L, i);
+    const int p = pos_at(pos, b, L, i);
+    const bool pad = seg && (s == pad_id);
+    int smin = pad ? INT_MAX : s, smax = pad ? INT_MIN : s;
+    int pmin = pad ? INT_MAX : p, pmax = pad ? INT_MIN : p;
+    int npad = pad ? 1 : 0;
+    for (int o = 16; o > 0; o >>= 1) {
+        smin = min(smin, __shfl_xor_sync(0xffffffffu, smin, o));
+        smax = max(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+        pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
+        pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
+        npad += __shfl_xor_sync(0xffffffffu, npad, o);
+    }
+    __shared__ TileSum w[4];
+    if ((threadIdx.x & 31) == 0) w[threadIdx.x >> 5] = TileSum{smin, smax, pmin, pmax, npad};
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        TileSum r = w[0];
+        for (int k = 1; k < 4; ++k) {
+            r.seg_min = min(r.seg_min, w[k].seg_min);
+            r.seg_max = max(r.seg_max, w[k].seg_max);
+            r.pos_min = min(r.pos_min, w[k].pos_min);
+            r.pos_max = max(r.pos_max, w[k].pos_max);
+            r.npad += w[k].npad;
+        }
+        out[(size_t)b * gridDim.x + t] = r;
+    }
+}
+
+// Class from the summaries when it is exact, else -1 (count pairs).
+__device__ __forceinline__ int classify_fast(const TileSum &q, const TileSum &k, int causal)
+{
+    if (q.npad == kTile || k.npad == kTile) return RA_TILE_EMPTY;
+    if (q.seg_max < k.seg_min || k.seg_max < q.seg_min) return RA_TILE_EMPTY;
+    const bool one = q.seg_min == q.seg_max && k.seg_min == k.seg_max && q.seg_min == k.seg_min;
+    if (!one) return -1;
+    const bool nopad = (q.npad == 0 && k.npad == 0);
+    if (!causal) return nopad ? RA_TILE_FULL : RA_TILE_PARTIAL;
+    if (q.pos_max < k.pos_min) return RA_TILE_EMPTY;
+    if (q.pos_min >= k.pos_max) return nopad ? RA_TILE_FULL : RA_TILE_PARTIAL;
+    return RA_TILE_PARTIAL;
+}
+
+constexpr int kCls = 256; // threads of classify / column kernels
+
+// grid (nq, B)
+__global__ void __launch_bounds__(kCls) classify_rows_kernel(Problem p, const TileSum *qsum,
+                                                             const TileSum *ksum, uint8_t *cls,
+                                                             int32_t *fwd_cnt, int32_t *fwd_idx)
+{
+    const int b = blockIdx.y, qt = blockIdx.x, nk = p.nk;
+    __shared__ int q_seg_s[kTile], q_pos_s[kTile], k_seg_s[kTile], k_pos_s[kTile];
+    __shared__ int slow[1024];
+    __shared__ int nslow, red[kCls / 32], base;
+    const TileSum qs = qsum[(size_t)b * p.nq + qt];
+    uint8_t *crow = cls + ((size_t)b * p.nq + qt) * nk;
+    int32_t *irow = fwd_idx + ((size_t)b * p.nq + qt) * nk;
+    if (threadIdx.x < kTile) {
+        const int i = qt * kTile + threadIdx.x;
+        q_seg_s[threadIdx.x] = seg_at(p.q_seg, b, p.Lq, i);
+        q_pos_s[threadIdx.x] = pos_at(p.q_pos, b, p.Lq, i);
+    }
+    if (threadIdx.x == 0) base = 0;
+    for (int k0 = 0; k0 < nk; k0 += 1024) {
+        const int kend = min(nk, k0 + 1024);
+        if (threadIdx.x == 0) nslow = 0;
+        __syncthreads();
+        for (int kt = k0 + threadIdx.x; kt < kend; kt += kCls) {
+            const int c = classify_fast(qs, ksum[(size_t)b * nk + kt], p.causal);
+            if (c < 0) {
+                slow[atomicAdd(&nslow, 1)] = kt;
+            } else {
+                crow[kt] = (uint8_t)c;
+            }
+        }
+        __syncthreads();
+        const int ns = nslow;
+        for (int si = 0; si < ns; ++si) {
+            const int kt = slow[si];
+            if (threadIdx.x < kTile) {
+                const int j = kt * kTile + threadIdx.x;
+                k_seg_s[threadIdx.x] = seg_at(p.kv_seg, b, p.Lkv, j);
+                k_pos_s[threadIdx.x] = pos_at(p.kv_pos, b, p.Lkv, j);
+            }
+            __syncthreads();
+            int cnt = 0;
+            for (int e = threadIdx.x; e < kTile * kTile; e += kCls) {
+                const int i = e >> 7, j = e & (kTile - 1);
+                const int sq = q_seg_s[i];
+                bool vis = (sq == k_seg_s[j]) && !(p.q_seg && sq == p.pad_id);
+                if (p.causal) vis = vis && (q_pos_s[i] >= k_pos_s[j]);
+                cnt += vis ? 1 : 0;
+            }
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cnt;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int t = 0;
+                for (int w = 0; w < kCls / 32; ++w) t += red[w];
+                crow[kt] = (uint8_t)(t == 0 ? RA_TILE_EMPTY
+                                            : (t == kTile * kTile ? RA_TILE_FULL : RA_TILE_PARTIAL));
+            }
+            __syncthreads();
+        }
+        __syncthreads();
+        // compact non-empty kt of this chunk, in ascending order
+        for (int kk = k0; kk < kend; kk += kCls) {
+            const int kt = kk + threadIdx.x;
+            const bool ne = kt < kend && crow[kt] != RA_TILE_EMPTY;
+            const unsigned m = __ballot_sync(0xffffffffu, ne);
+            const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+            if (lane == 0) red[wid] = __popc(m);
+            __syncthreads();
+            int off = base;
+            for (int w = 0; w < wid; ++w) off += red[w];
+            if (ne) irow[off + __popc(m & ((1u << lane) - 1u))] = kt;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int t = 0;
+                for (int w = 0; w < kCls / 32; ++w) t += red[w];
+                base += t;
+            }
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+    const int cnt = base;
+    for (int r = cnt + threadIdx.x; r < nk; r += kCls) irow[r] = -1;
+    if (threadIdx.x == 0) fwd_cnt[(size_t)b * p.nq + qt] = cnt;
+}
+
+// grid (nk, B): column compaction
+__global__ void __launch_bounds__(kCls) columns_kernel(const uint8_t *cls, int nq, int nk,
+                                                       int32_t *bwd_cnt, int32_t *bwd_idx)
+{
+    const int b = blockIdx.y, kt = blockIdx.x;
+    __shared__ int red[kCls / 32], base;
+    if (threadIdx.x == 0) base = 0;
+    __syncthreads();
+    int32_t *col = bwd_idx + ((size_t)b * nk + kt) * nq;
+    for (int q0 = 0; q0 < nq; q0 += kCls) {
+        const int qt = q0 + threadIdx.x;
+        const bool ne = qt < nq && cls[((size_t)b * nq + qt) * nk + kt] != RA_TILE_EMPTY;
+        const unsigned m = __ballot_sync(0xffffffffu, ne);
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        if (lane == 0) red[wid] = __popc(m);
+        __syncthreads();
+        int off = base;
+        for (int w = 0; w < wid; ++w) off += red[w];
+        if (ne) col[off + __popc(m & ((1u << lane) - 1u))] = qt;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int t = 0;
+            for (int w = 0; w < kCls / 32; ++w) t += red[w];
+            base += t;
+        }
+        __syncthreads();
+    }
+    const int cnt = base;
+    for (int r = cnt + threadIdx.x; r < nq; r += kCls) col[r] = -1;
+    if (threadIdx.x == 0) bwd_cnt[(size_t)b * nk + kt] = cnt;
+}
+
+// Stable counting sort of ids 0..R-1 by descending cnt[id] (ties by id).
+// One block of 1024 threads; hist needs (maxc + 1) ints of dynamic smem.
+__global__ void __launch_bounds__(1024) order_kernel(const int32_t *cnt, int R, int maxc,
+                                                     int32_t *order)
+{
+    extern __shared__ int hist[]; // [maxc + 1], then [1024] partials
+    int *part = hist + maxc + 1;
+    const int nb = maxc + 1;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < R; i += blockDim.x) atomicAdd(&hist[maxc - cnt[i]], 1);
+    __syncthreads();
+    // exclusive scan of hist (key = maxc - cnt ascending == cnt descending)
+    const int per = (nb + blockDim.x - 1) / blockDim.x;
+    const int lo = threadIdx.x * per, hi = min(nb, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += hist[i];
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int t = 0; t < (int)blockDim.x; ++t) {
+            const int v = part[t];
+            part[t] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    int run = part[threadIdx.x];
+    for (int i = lo; i < hi; ++i) {
+        const int v = hist[i];
+        hist[i] = run;
+        run += v;
+    }
+    __syncthreads();
+    // stable scatter by warp 0, 32 ids at a time in id order
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        for (int i0 = 0; i0 < R; i0 += 32) {
+            const int id = i0 + lane;
+            const bool act = id < R;
+            const int key = act ? maxc - cnt[id] : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            const int leader = __ffs(peers) - 1;
+            int start = 0;
+            if (act && lane == leader) {
+                start = hist[key];
+                hist[key] = start + __popc(peers);
+            }
+            start = __shfl_sync(0xffffffffu, start, leader);
+            if (act) order[start + __popc(peers & ((1u << lane) - 1u))] = id;
+            __syncwarp();
+        }
+    }
+}
+
+} // namespace
+
+size_t mask_scratch_ints(int B, int nq, int nk)
+{
+    return (size_t)B * (nq + nk) * (sizeof(TileSum) / sizeof(int32_t));
+}
+
+cudaError_t launch_mask_build(const Problem &p, uint8_t *cls, int32_t *fwd_cnt, int32_t *fwd_idx,
+                              int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order,
+                              int32_t *bwd_order, int32_t *scratch, cudaStream_t s)
+{
+    TileSum *qsum = reinterpret_cast<TileSum *>(scratch);
+    TileSum *ksum = qsum + (size_t)p.B * p.nq;
+    tile_summary_kernel<<<dim3(p.nq, p.B), 128, 0, s>>>(p.q_seg, p.q_pos, p.Lq, p.pad_id, qsum);
+    tile_summary_kernel<<<dim3(p.nk, p.B), 128, 0, s>>>(p.kv_seg, p.kv_pos, p.Lkv, p.pad_id, ksum);
+    classify_rows_kernel<<<dim3(p.nq, p.B), kCls, 0, s>>>(p, qsum, ksum, cls, fwd_cnt, fwd_idx);
+    columns_kernel<<<dim3(p.nk, p.B), kCls, 0, s>>>(cls, p.nq, p.nk, bwd_cnt, bwd_idx);
+    const size_t sm_f = sizeof(int) * ((size_t)p.nk + 1 + 1024);
+    const size_t sm_b = sizeof(int) * ((size_t)p.nq + 1 + 1024);
+    order_kernel<<<1, 1024, sm_f, s>>>(fwd_cnt, p.B * p.nq, p.nk, fwd_order);
+    order_kernel<<<1, 1024, sm_b, s>>>(bwd_cnt, p.B * p.nk, p.nq, bwd_order);
+    return cudaGetLastError();
+}
+
+} // namespace ra

@@ -1,0 +1,70 @@
+// ra_internal.h -- declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ra.h"
+
+namespace ra {
+
+constexpr int kTile = RA_TILE;            // canonical tile edge (tokens)
+constexpr int RA_STATUS_TIMEOUT = 1;      // device status word value on a timed-out wait
+
+// Everything a kernel needs to know about the problem, in device-friendly form.
+struct Problem {
+    int B, Lq, Lkv, Hq, Hkv, G, D;
+    int nq, nk;          // tiles along q and kv
+    int N;               // virtual ring shards
+    int tq, tk;          // tiles per shard along q and kv
+    float scale;
+    float soft_cap;      // 0 = none
+    int causal;
+    int pad_id;
+    const int32_t *q_pos, *kv_pos, *q_seg, *kv_seg;
+    const float *sinks;
+    // block map
+    const uint8_t *tile_class;
+    const int32_t *fwd_cnt, *fwd_idx, *bwd_cnt, *bwd_idx, *fwd_order, *bwd_order;
+    // failure reporting
+    int *status;
+    uint64_t timeout_ns;
+};
+
+// ---- launchers (each returns cudaError_t of its launch) -------------------
+cudaError_t launch_permute(const void *in, void *out, int B, int L, size_t row_bytes, int n,
+                           int inverse, cudaStream_t s);
+cudaError_t launch_mask_build(const Problem &p, uint8_t *cls, int32_t *fwd_cnt, int32_t *fwd_idx,
+                              int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order,
+                              int32_t *bwd_order, int32_t *scratch, cudaStream_t s);
+size_t mask_scratch_ints(int B, int nq, int nk);
+cudaError_t launch_merge(float *out, float *lse, const float *bout, const float *blse, int B,
+                         int L, int H, int D, cudaStream_t s);
+cudaError_t launch_fwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,
+                                float *out, float *lse, cudaStream_t s);
+cudaError_t launch_fwd_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,
+                          void *out, float *lse, int num_sms, cudaStream_t s);
+cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, int dtype,
+                           const float *lse, float *delta, float *dsink_part, float *dsinks,
+                           cudaStream_t s);
+cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *tm_k,
+                               const void *tm_v, const void *tm_do, const float *lse,
+                               const float *delta, void *dk, void *dv, int num_sms,
+                               cudaStream_t s);
+cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
+                             const void *tm_v, const void *tm_do, const float *lse,
+                             const float *delta, void *dq, int num_sms, cudaStream_t s);
+cudaError_t launch_bwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,
+                                const float *dout, const float *lse, const float *delta,
+                                float *dq, float *dk, float *dv, cudaStream_t s);
+
+// dynamic shared memory the tensor-core kernels request (for attribute setup)
+int fwd_tc_smem_bytes(int D);
+int bwd_dkdv_smem_bytes(int D);
+int bwd_dq_smem_bytes(int D);
+cudaError_t fwd_tc_set_attributes(int D);
+cudaError_t bwd_tc_set_attributes(int D);
+cudaError_t simt_set_attributes(int D);
+
+} // namespace ra

@@ -1,0 +1,282 @@
+/*
+ * ra.h -- C ABI of block-sparse masked flash attention with the ring
+ * (out, lse) merge, for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (sources are named by page title and section):
+ *   - "ejKernel ring_attention._ring_splash" module source:
+ *       _update_out_and_lse      the sigmoid/softplus merge of a chunk's
+ *                                partial (out, lse) into the running pair;
+ *       _ring_attention_forward  the ring loop: step t of virtual device d
+ *                                attends to the key/value chunk of source
+ *                                (d - t) mod N, sinks only on step 0, soft cap;
+ *       _ring_attention_backward dq accumulated locally, dk/dv travelling with
+ *                                their chunk, dsinks summed over the ring;
+ *       make_ring_attention      MaskInfo block metadata for forward and dkv.
+ *   - "Kvax: Flash Attention for JAX":
+ *       flash_attention          (batch, seq, heads, head_dim) layout,
+ *                                positions, segment ids, PADDING_SEGMENT_ID,
+ *                                scale, GQA via num_kv_heads;
+ *       create_attention_mask    block-wise mask from positions and segments,
+ *                                padding-only blocks skipped;
+ *       context parallelism      permute tokens for load balance, unpermute
+ *                                outputs.
+ *
+ * Semantics, for each batch b, query head h (kv head g = h / (Hq / Hkv)):
+ *   visible(i, j) = q_seg[i] == kv_seg[j] && q_seg[i] != pad_segment_id
+ *                   && (!causal || q_pos[i] >= kv_pos[j])
+ *   s_ij   = scale * <q_i, k_j>;  if soft_cap > 0: s_ij = soft_cap * tanh(s_ij / soft_cap)
+ *   lse_i  = log( sum_{visible j} exp(s_ij) + (sinks ? exp(sinks[h]) : 0) )
+ *   out_i  = sum_{visible j} exp(s_ij - lse_i) v_j
+ *   Invisible pairs are excluded; a row with nothing visible and no sink has
+ *   out = 0, lse = -inf.  The forward walks the KV sequence as N virtual ring
+ *   shards and merges each shard's partial into the running pair with the
+ *   pages' update, which equals the formula above up to rounding.
+ *
+ * Conventions
+ *   - Every pointer argument is a DEVICE pointer on the current CUDA device
+ *     unless stated otherwise; the caller owns every buffer.  The library
+ *     never allocates memory and keeps no state besides a per-device cache of
+ *     device properties and kernel attributes.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous; argument errors are reported synchronously.
+ *   - Layouts are dense, row-major: q, out, dout, dq (B, Lq, Hq, D);
+ *     k, v, dk, dv (B, Lkv, Hkv, D); lse (B, Hq, Lq) fp32;
+ *     positions / segment ids (B, L) int32; sinks (Hq) fp32.
+ *   - Tiles are 128 x 128 tokens: Lq and Lkv must be multiples of
+ *     128 * n_virtual_shards.
+ *   - Device pointers handed to the attention calls must be 16-byte aligned.
+ *   - Return value: RA_OK or a negative RA_ERR_* code; ra_last_error() gives
+ *     a thread-local message for the last failing call of this thread.
+ */
+#ifndef RA_H
+#define RA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RA_API __attribute__((visibility("default")))
+#else
+#define RA_API
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *ra_stream_t;
+
+enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = -1, /* bad shape, pointer, alignment or mask */
+    RA_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. D not in {64,128}) */
+    RA_ERR_CUDA = -3,        /* a CUDA runtime call failed */
+    RA_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
+    RA_ERR_TIMEOUT = -5      /* a kernel's bounded wait ran out (device status) */
+};
+
+enum { RA_BF16 = 0, RA_FP32 = 1 };
+enum { RA_TILE_EMPTY = 0, RA_TILE_PARTIAL = 1, RA_TILE_FULL = 2 };
+#define RA_TILE 128
+
+/*
+ * Problem description shared by every attention call.
+ *   B, Lq, Lkv, Hq, Hkv, D  sizes; D in {64, 128}; Hq % Hkv == 0.
+ *   dtype            RA_BF16 or RA_FP32: element type of q, k, v, out, dout,
+ *                    dq, dk, dv.  Accumulation is always fp32.
+ *   scale            multiplies <q, k> before the cap (Kvax `scale`).
+ *   soft_cap         > 0 applies cap * tanh(s / cap); <= 0 disables it
+ *                    (_ring_splash `logits_soft_cap`).
+ *   causal           1: a pair is visible only if q_pos >= kv_pos.
+ *   is_mqa           1: one kv head shared by all query heads (requires
+ *                    Hkv == 1); _ring_splash `is_mqa`.
+ *   n_virtual_shards N >= 1 ring shards of Lq / N query and Lkv / N key rows.
+ *   pad_segment_id   segment id that marks padding (Kvax PADDING_SEGMENT_ID;
+ *                    this library's reading: -1).  Padding is never visible.
+ *   q_pos, kv_pos    (B, L) int32 positions, or NULL for the token's index in
+ *                    the sequence as passed (after any permutation).
+ *   q_seg, kv_seg    (B, L) int32 segment ids, or NULL for a single segment
+ *                    without padding.  Both or neither.
+ *   sinks            (Hq) fp32 sink logits, counted once per row in the
+ *                    denominator only, or NULL.
+ */
+typedef struct {
+    int B, Lq, Lkv, Hq, Hkv, D;
+    int dtype;
+    float scale;
+    float soft_cap;
+    int causal;
+    int is_mqa;
+    int n_virtual_shards;
+    int pad_segment_id;
+    const int32_t *q_pos;
+    const int32_t *kv_pos;
+    const int32_t *q_seg;
+    const int32_t *kv_seg;
+    const float *sinks;
+} ra_attn_params;
+
+/*
+ * Block map on the 128 x 128 tile grid (nq = Lq / 128, nk = Lkv / 128),
+ * the counterpart of the pages' MaskInfo.  All arrays live in one caller
+ * buffer carved by ra_build_block_mask.
+ *   tile_class  (B, nq, nk) uint8: RA_TILE_EMPTY / PARTIAL / FULL.
+ *   fwd_cnt     (B*nq) non-empty tiles in each query-tile row.
+ *   fwd_idx     (B*nq, nk) their kt, ascending, padded with -1.
+ *   bwd_cnt     (B*nk) non-empty tiles in each key-tile column.
+ *   bwd_idx     (B*nk, nq) their qt, ascending, padded with -1.
+ *   fwd_order   (B*nq) row ids b*nq+qt by descending fwd_cnt, ties by id
+ *               (the longest-first schedule of the forward).
+ *   bwd_order   (B*nk) column ids b*nk+kt, same rule (backward schedule).
+ *   key         fingerprint of the ra_attn_params fields the map depends on;
+ *               attention calls reject a map built for other params.
+ */
+typedef struct {
+    uint8_t *tile_class;
+    int32_t *fwd_cnt;
+    int32_t *fwd_idx;
+    int32_t *bwd_cnt;
+    int32_t *bwd_idx;
+    int32_t *fwd_order;
+    int32_t *bwd_order;
+    int B, nq, nk;
+    uint64_t key;
+} ra_block_mask;
+
+/* Thread-local message of the last failing call on this thread ("" if none). */
+RA_API const char *ra_last_error(void);
+
+/* Library version string. */
+RA_API const char *ra_version(void);
+
+/*
+ * Bytes of the device buffer ra_build_block_mask needs for params `p`
+ * (0 if `p` is invalid; ra_last_error says why).
+ */
+RA_API size_t ra_block_mask_bytes(const ra_attn_params *p);
+
+/*
+ * Classifies every 128 x 128 tile from positions and segment ids and builds
+ * the tile lists and schedules (make_ring_attention's forward and dkv
+ * MaskInfo; Kvax create_attention_mask with padding-only tiles skipped).
+ * Result is bit-exact: a tile is EMPTY iff no pair is visible, FULL iff all
+ * 128*128 pairs are, PARTIAL otherwise.
+ *   buf, buf_bytes  device buffer of at least ra_block_mask_bytes(p) bytes,
+ *                   256-byte aligned; owned by the caller and must outlive
+ *                   every call that uses `out`.
+ *   out             host struct filled with device pointers into `buf`.
+ * Errors: RA_ERR_INVALID_ARG (params, null pointers), RA_ERR_WORKSPACE
+ * (buffer too small or misaligned), RA_ERR_CUDA.
+ */
+RA_API int ra_build_block_mask(const ra_attn_params *p, void *buf, size_t buf_bytes,
+                               ra_block_mask *out, ra_stream_t stream);
+
+/* Workspace bytes of ra_attn_fwd (0: the forward keeps its running state on
+ * chip). */
+RA_API size_t ra_attn_fwd_workspace_size(const ra_attn_params *p);
+
+/*
+ * Forward (_ring_attention_forward on N virtual shards, one launch).
+ *   q (B,Lq,Hq,D), k, v (B,Lkv,Hkv,D) in p->dtype;  mask from
+ *   ra_build_block_mask for the same params;  out (B,Lq,Hq,D) in p->dtype;
+ *   lse (B,Hq,Lq) fp32 natural-log (-inf for rows with nothing visible).
+ *   For each query tile the shards are visited in ring order
+ *   s = (d - t) mod N (d = the tile's own shard, t = 0..N-1), empty tiles are
+ *   skipped, the sink enters at t = 0 only, and each shard's partial is merged
+ *   into the running (out, lse) by the sigmoid/softplus update.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_WORKSPACE, RA_ERR_CUDA.
+ */
+RA_API int ra_attn_fwd(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                       const ra_block_mask *mask, void *out, float *lse, void *ws,
+                       size_t ws_bytes, ra_stream_t stream);
+
+/*
+ * _update_out_and_lse, elementwise and in place:
+ *   out (B,L,H,D) fp32, lse (B,H,L) fp32 running pair;
+ *   block_out, block_lse the chunk's partial, same layouts.
+ *   Where lse == -inf the block is taken as is; otherwise
+ *   w = sigmoid(block_lse - lse), out -= w * (out - block_out),
+ *   lse += softplus(block_lse - lse).
+ *   out / block_out must not overlap; D % 4 == 0.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_CUDA.
+ */
+RA_API int ra_merge_out_lse(float *out, float *lse, const float *block_out,
+                            const float *block_lse, int B, int L, int H, int D,
+                            ra_stream_t stream);
+
+/* Workspace bytes of ra_attn_bwd: per-row Delta = <dO, O> (fp32, B*Hq*Lq)
+ * and per-tile partial sums of dsinks. */
+RA_API size_t ra_attn_bwd_workspace_size(const ra_attn_params *p);
+
+/*
+ * Backward (_ring_attention_backward): the exact gradient of ra_attn_fwd's
+ * output, computed with the final out and lse.
+ *   q, k, v, out, dout in p->dtype; lse from ra_attn_fwd;
+ *   dq (B,Lq,Hq,D), dk, dv (B,Lkv,Hkv,D) in p->dtype, overwritten (dk, dv
+ *   summed over the query heads that share a kv head);
+ *   dsinks (Hq) fp32, overwritten, summed over batch and all rows; may be
+ *   NULL only when p->sinks is NULL.
+ *   ws: at least ra_attn_bwd_workspace_size(p) bytes, 256-byte aligned.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_WORKSPACE, RA_ERR_CUDA.
+ */
+RA_API int ra_attn_bwd(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                       const void *out, const float *lse, const void *dout,
+                       const ra_block_mask *mask, void *dq, void *dk, void *dv, float *dsinks,
+                       void *ws, size_t ws_bytes, ra_stream_t stream);
+
+/*
+ * The three stages ra_attn_bwd runs, for callers that schedule or time them
+ * one by one.  Arguments mean what they mean for ra_attn_bwd and obey the
+ * same rules; the stages communicate through `ws`, so for one problem they
+ * must run in this order on one stream (or be ordered by the caller):
+ *   ra_attn_bwd_prep  Delta = rowsum(dO * O) into ws and dsinks (if sinks);
+ *   ra_attn_bwd_dkdv  dk, dv (one work unit per kv head and 128-row kv tile);
+ *   ra_attn_bwd_dq    dq     (one work unit per query head and query tile).
+ */
+RA_API int ra_attn_bwd_prep(const ra_attn_params *p, const void *out, const float *lse,
+                            const void *dout, float *dsinks, void *ws, size_t ws_bytes,
+                            ra_stream_t stream);
+RA_API int ra_attn_bwd_dkdv(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                            const float *lse, const void *dout, const ra_block_mask *mask,
+                            void *dk, void *dv, void *ws, size_t ws_bytes, ra_stream_t stream);
+RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                          const float *lse, const void *dout, const ra_block_mask *mask,
+                          void *dq, void *ws, size_t ws_bytes, ra_stream_t stream);
+
+/*
+ * Zigzag load-balancing permutation along the sequence (Kvax context
+ * parallelism).  The sequence of L rows is split into 2N chunks of L/(2N);
+ * virtual device d holds chunk d followed by chunk 2N-1-d, so permuted row
+ * p = d*(L/N) + r comes from row d*c + r if r < c, else (2N-1-d)*c + r - c,
+ * with c = L/(2N).
+ *   in, out      (B, L, row_bytes) device buffers, must not overlap.
+ *   row_bytes    bytes per token row (any element type; copied bitwise).
+ * ra_unpermute_tokens applies the inverse.
+ * Errors: RA_ERR_INVALID_ARG (L % (2N) != 0, in == out, null), RA_ERR_CUDA.
+ */
+RA_API int ra_permute_tokens(const void *in, void *out, int B, int L, size_t row_bytes,
+                             int n_shards, ra_stream_t stream);
+RA_API int ra_unpermute_tokens(const void *in, void *out, int B, int L, size_t row_bytes,
+                               int n_shards, ra_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: RA_OK, or RA_ERR_TIMEOUT if a kernel gave up a bounded wait.
+ */
+RA_API int ra_get_device_status(ra_stream_t stream);
+
+/* Number of CUDA kernels this library has launched in this process (all
+ * devices, all threads); lets callers count the library's launches in a
+ * region without a profiler. */
+RA_API uint64_t ra_launch_count(void);
+
+/* Upper bound, in nanoseconds, of any single in-kernel wait (default 2e9).
+ * Applies to launches made after the call, from any thread. */
+RA_API void ra_set_wait_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H */

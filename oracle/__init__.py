@@ -77,9 +77,9 @@ def _load():
             lib = ctypes.CDLL(build())
             P = ctypes.POINTER(_Params)
             vp, ci, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-            lib.ora_attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, ci, ci]
+            lib.ora_attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, ci, ci, ci, ci]
             lib.ora_attn_fwd_ring.argtypes = [P, ci, vp, vp, vp, vp, vp, ci, ci]
-            lib.ora_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.ora_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci]
             lib.ora_merge.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci]
             lib.ora_merge.restype = None
             lib.ora_block_mask.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
@@ -124,19 +124,20 @@ class _Call:
         self.shape = (B, Lq, Lkv, Hq, Hkv, D)
 
 
-def attn_fwd(q, k, v, *, scale, heads=None, **kw):
+def attn_fwd(q, k, v, *, scale, heads=None, rows=None, **kw):
     """Plain definition.  q [B,Lq,Hq,D], k/v [B,Lkv,Hkv,D] -> (out [B,Lq,Hq,D], lse [B,Hq,Lq]).
 
-    ``heads=(lo, hi)`` restricts the computation to query heads [lo, hi); the
-    other heads' outputs are left at zero / -inf.
+    ``heads=(lo, hi)`` / ``rows=(lo, hi)`` restrict the computation to those
+    query heads / query rows; the other outputs are left at zero / -inf.
     """
     c = _Call(q, k, v, scale=scale, **kw)
     B, Lq, Lkv, Hq, Hkv, D = c.shape
     out = np.zeros((B, Lq, Hq, D))
     lse = np.full((B, Hq, Lq), -np.inf)
     lo, hi = heads if heads else (0, 0)
+    rlo, rhi = rows if rows else (0, 0)
     rc = _load().ora_attn_fwd(ctypes.byref(c.p), _ptr(c.q), _ptr(c.k), _ptr(c.v),
-                              _ptr(out), _ptr(lse), lo, hi)
+                              _ptr(out), _ptr(lse), lo, hi, rlo, rhi)
     if rc:
         raise ValueError(f"ora_attn_fwd failed ({rc})")
     return out, lse
@@ -156,8 +157,11 @@ def attn_fwd_ring(q, k, v, *, scale, n_shards, heads=None, **kw):
     return out, lse
 
 
-def attn_bwd(q, k, v, dout, *, scale, **kw):
-    """Exact gradient -> (dq, dk, dv, dsinks or None); also returns (out, lse)."""
+def attn_bwd(q, k, v, dout, *, scale, heads=None, rows=None, **kw):
+    """Exact gradient -> (dq, dk, dv, dsinks or None, out, lse).
+
+    ``heads`` / ``rows`` restrict the sums to the contributions of those
+    query heads / rows (dq of other rows stays 0)."""
     c = _Call(q, k, v, scale=scale, **kw)
     B, Lq, Lkv, Hq, Hkv, D = c.shape
     do = _f64(dout)
@@ -167,8 +171,11 @@ def attn_bwd(q, k, v, dout, *, scale, **kw):
     ds = np.zeros(Hq) if c.sinks is not None else None
     out = np.zeros((B, Lq, Hq, D))
     lse = np.full((B, Hq, Lq), -np.inf)
+    lo, hi = heads if heads else (0, 0)
+    rlo, rhi = rows if rows else (0, 0)
     rc = _load().ora_attn_bwd(ctypes.byref(c.p), _ptr(c.q), _ptr(c.k), _ptr(c.v), _ptr(do),
-                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ds), _ptr(out), _ptr(lse))
+                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ds), _ptr(out), _ptr(lse),
+                              lo, hi, rlo, rhi)
     if rc:
         raise ValueError(f"ora_attn_bwd failed ({rc})")
     return dq, dk, dv, ds, out, lse

@@ -157,12 +157,18 @@ static int ora_check(const ora_params *p)
     return 0;
 }
 
-/* Plain definition: every (b, h, i) over all keys, sink counted once. */
+/* Plain definition: every (b, h, i) over all keys, sink counted once.
+ * Only query heads [heads_lo, heads_hi) and query rows [rows_lo, rows_hi)
+ * are computed (an empty range means all); the rest of out / lse is left
+ * untouched.  Restricting rows or heads changes which rows are computed,
+ * never how a row is computed. */
 int ora_attn_fwd(const ora_params *p, const double *q, const double *k, const double *v,
-                 double *out, double *lse, int heads_lo, int heads_hi)
+                 double *out, double *lse, int heads_lo, int heads_hi, int rows_lo, int rows_hi)
 {
     if (ora_check(p)) return -1;
     if (heads_hi <= heads_lo) { heads_lo = 0; heads_hi = p->Hq; }
+    if (rows_hi <= rows_lo) { rows_lo = 0; rows_hi = p->Lq; }
+    if (heads_lo < 0 || heads_hi > p->Hq || rows_lo < 0 || rows_hi > p->Lq) return -1;
     const int R = ora_row_block(p);
     const int nblk = (p->Lq + R - 1) / R;
     const int D = p->D;
@@ -181,6 +187,9 @@ int ora_attn_fwd(const ora_params *p, const double *q, const double *k, const do
             for (int b = 0; b < p->B; ++b)
                 for (int blk = 0; blk < nblk; ++blk) {
                     int i0 = blk * R, i1 = i0 + R < p->Lq ? i0 + R : p->Lq;
+                    if (i0 < rows_lo) i0 = rows_lo;
+                    if (i1 > rows_hi) i1 = rows_hi;
+                    if (i0 >= i1) continue;
                     ora_fill_mask(p, b, i0, i1, vis);
                     for (int h = heads_lo; h < heads_hi; ++h) {
                         ora_rows(p, q, k, v, b, h, i0, i1, 0, p->Lkv, vis, 1, orow, lrow, sbuf);
@@ -314,7 +323,10 @@ int ora_attn_fwd_ring(const ora_params *p, int n_shards, const double *q, const 
 }
 
 /* Exact gradient of the plain forward (its own forward is recomputed here,
- * so no input comes from elsewhere).  Summing per-chunk contributions as
+ * so no input comes from elsewhere).  With a head range / row range, only
+ * the contributions of those query heads and rows are summed (dq of the
+ * other rows stays 0); the result is the full gradient when the ranges are
+ * empty (= all).  Summing per-chunk contributions as
  * [RS] _ring_attention_backward does gives the same sums.
  *   Delta_i = <dO_i, O_i>,  P_ij = exp(s_ij - lse_i) on visible pairs
  *   dV_j  += P_ij dO_i ;  dP_ij = <dO_i, v_j> ;  dS_ij = P_ij (dP_ij - Delta_i)
@@ -325,10 +337,13 @@ int ora_attn_fwd_ring(const ora_params *p, int n_shards, const double *q, const 
  * (b, kv head) so that no two threads write the same dk / dv row. */
 int ora_attn_bwd(const ora_params *p, const double *q, const double *k, const double *v,
                  const double *dout, double *dq, double *dk, double *dv, double *dsinks,
-                 double *out_ws, double *lse_ws)
+                 double *out_ws, double *lse_ws, int heads_lo, int heads_hi, int rows_lo,
+                 int rows_hi)
 {
     if (ora_check(p)) return -1;
-    int rc = ora_attn_fwd(p, q, k, v, out_ws, lse_ws, 0, 0);
+    if (heads_hi <= heads_lo) { heads_lo = 0; heads_hi = p->Hq; }
+    if (rows_hi <= rows_lo) { rows_lo = 0; rows_hi = p->Lq; }
+    int rc = ora_attn_fwd(p, q, k, v, out_ws, lse_ws, heads_lo, heads_hi, rows_lo, rows_hi);
     if (rc) return rc;
     const int D = p->D, G = p->Hq / p->Hkv;
     memset(dq, 0, sizeof(double) * (size_t)p->B * p->Lq * p->Hq * D);
@@ -349,7 +364,8 @@ int ora_attn_bwd(const ora_params *p, const double *q, const double *k, const do
                 for (int g = 0; g < p->Hkv; ++g)
                     for (int h = g * G; h < (g + 1) * G; ++h) {
                         double ds_acc = 0.0;
-                        for (int i = 0; i < p->Lq; ++i) {
+                        if (h < heads_lo || h >= heads_hi) continue;
+                        for (int i = rows_lo; i < rows_hi; ++i) {
                             double l = lse_ws[((size_t)b * p->Hq + h) * p->Lq + i];
                             const double *o = out_ws + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
                             const double *go = dout + (((size_t)b * p->Lq + i) * p->Hq + h) * D;

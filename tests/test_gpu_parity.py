@@ -1,0 +1,300 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Bars: block map and permutations bit-exact; forward O max-abs <= 2e-2 and
+lse max-abs <= 1e-3 (rows whose lse is -inf must be -inf on both sides);
+gradients dq, dk, dv, dsinks relative L2 <= 1e-2 per tensor.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_flash_ra_gb300 as ra
+import oracle
+from workloads import WORKLOADS, Workload, make_inputs, random_structure
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, LSE_TOL, GRAD_TOL = 2e-2, 1e-3, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_sparse_flash_ra_gb300 import _build
+    _build.build()
+    yield
+    torch.cuda.synchronize()
+    assert ra.ra_get_device_status() == ra.RA_OK
+
+
+def f64(t):
+    return None if t is None else t.detach().to("cpu", torch.float64).numpy()
+
+
+def i32(t):
+    return None if t is None else t.detach().cpu().numpy().astype(np.int32)
+
+
+def check_fwd(out, lse, o_ref, l_ref):
+    o, l = f64(out), f64(lse)
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isfinite(l), fin), "rows with nothing visible differ"
+    assert np.all(l[~fin] == l_ref[~fin])
+    if fin.any():
+        assert np.max(np.abs(l[fin] - l_ref[fin])) <= LSE_TOL
+    assert np.max(np.abs(o - o_ref)) <= O_TOL
+
+
+def rel_l2(a, b):
+    den = np.linalg.norm(b)
+    return np.linalg.norm(a - b) / (den if den > 0 else 1.0)
+
+
+def host_permute(t, n):
+    """The oracle's zigzag permutation of a CPU tensor (bitwise, any dtype)."""
+    if t.dtype == torch.bfloat16:
+        return torch.from_numpy(oracle.permute(t.view(torch.int16).numpy(), n)).view(torch.bfloat16)
+    return torch.from_numpy(oracle.permute(t.numpy(), n))
+
+
+class Case:
+    """One problem, with inputs on both sides in the (possibly permuted) order."""
+
+    def __init__(self, w: Workload, *, structure=None, seed_struct=0, dout=False,
+                 overrides=None):
+        self.w = w
+        inp = make_inputs(w, with_dout=dout)
+        if structure is not None:
+            g = torch.Generator().manual_seed(seed_struct)
+            seg, pos = random_structure(g, w.B, w.L, **structure)
+            inp.update(q_seg=seg, kv_seg=seg.clone(), q_pos=pos, kv_pos=pos.clone())
+        if overrides:
+            inp.update(overrides)
+        self.inp = inp
+        N = w.n_shards
+        dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        host = dict(inp)
+        if w.zigzag:
+            for key in ("q", "k", "v", "dout", "q_pos", "kv_pos", "q_seg", "kv_seg"):
+                if dev[key] is not None:
+                    dev[key] = ra.permute(dev[key], N)
+                    host[key] = host_permute(host[key], N)
+        self.dev, self.host = dev, host
+        self.params = ra.make_params(
+            dev["q"], dev["k"], scale=w.scale, causal=w.causal, soft_cap=w.soft_cap,
+            n_virtual_shards=N, is_mqa=w.is_mqa, q_pos=dev["q_pos"], kv_pos=dev["kv_pos"],
+            q_seg=dev["q_seg"], kv_seg=dev["kv_seg"], sinks=dev["sinks"])
+        self.okw = dict(scale=w.scale, soft_cap=w.soft_cap or None, causal=w.causal,
+                        q_pos=i32(host["q_pos"]), kv_pos=i32(host["kv_pos"]),
+                        q_seg=i32(host["q_seg"]), kv_seg=i32(host["kv_seg"]),
+                        sinks=f64(host["sinks"]))
+
+    def mask(self):
+        return ra.build_mask(self.params)
+
+    def gpu_fwd(self):
+        m = self.mask()
+        d = self.dev
+        return ra.forward(self.params, d["q"], d["k"], d["v"], m) + (m,)
+
+    def oracle_fwd(self, ring=True):
+        h = self.host
+        if ring:
+            return oracle.attn_fwd_ring(f64(h["q"]), f64(h["k"]), f64(h["v"]),
+                                        n_shards=self.w.n_shards, **self.okw)
+        return oracle.attn_fwd(f64(h["q"]), f64(h["k"]), f64(h["v"]), **self.okw)
+
+
+def W(**kw):
+    base = dict(name="t", B=1, L=1024, Hq=4, Hkv=2, D=128, n_shards=2, seed=11)
+    base.update(kw)
+    return Workload(**base)
+
+
+FWD_CASES = {
+    "tiny_fp32": WORKLOADS["tiny"],
+    "causal_n1": W(n_shards=1),
+    "causal_n4": W(n_shards=4, seed=12),
+    "causal_n8_one_tile_per_shard": W(n_shards=8, seed=13),
+    "gqa_noncausal": W(causal=False, Hq=8, Hkv=2, seed=14),
+    "mqa_sinks_cap50_zigzag": W(Hq=4, Hkv=1, is_mqa=True, sinks=True, soft_cap=50.0,
+                                zigzag=True, n_shards=2, seed=15),
+    "sinks_cap5": W(sinks=True, soft_cap=5.0, seed=16),
+    "d64": W(D=64, seed=17),
+    "d64_fp32": W(D=64, dtype="fp32", seed=18, L=512),
+    "zigzag_n4": W(zigzag=True, n_shards=4, seed=19),
+    "b2_gqa": W(B=2, Hq=6, Hkv=3, seed=20, L=768, n_shards=3),
+}
+
+
+@pytest.mark.parametrize("name", list(FWD_CASES))
+def test_forward_matches_oracle(name):
+    c = Case(FWD_CASES[name])
+    out, lse, _ = c.gpu_fwd()
+    torch.cuda.synchronize()
+    o_ref, l_ref = c.oracle_fwd()
+    check_fwd(out, lse, o_ref, l_ref)
+
+
+STRUCT_CASES = {
+    "packed_docs_pad": (W(B=2, seed=21), dict(n_docs_max=5, pad_max=300)),
+    "packed_docs_pad_sinks": (W(B=2, seed=22, sinks=True), dict(n_docs_max=4, pad_max=400)),
+    "shuffled_positions": (W(seed=23, L=512, n_shards=1), dict(n_docs_max=1, shuffle_positions=True)),
+    "noncausal_segments": (W(causal=False, seed=24), dict(n_docs_max=6, pad_max=50)),
+}
+
+
+@pytest.mark.parametrize("name", list(STRUCT_CASES))
+def test_forward_structured_matches_oracle(name):
+    w, st = STRUCT_CASES[name]
+    c = Case(w, structure=st, seed_struct=7)
+    out, lse, _ = c.gpu_fwd()
+    torch.cuda.synchronize()
+    o_ref, l_ref = c.oracle_fwd()
+    check_fwd(out, lse, o_ref, l_ref)
+
+
+def test_forward_all_padding_rows_and_empty_tiles():
+    # the last 256 tokens are padding: two whole query tiles with no visible
+    # key (lse = sink, out = 0), and padding rows inside a partial tile
+    w = W(B=1, L=1024, n_shards=2, sinks=True, seed=25)
+    g = torch.Generator().manual_seed(3)
+    seg, pos = random_structure(g, 1, 1024, n_docs_max=3)
+    seg[:, -300:] = -1
+    c = Case(w, overrides=dict(q_seg=seg, kv_seg=seg.clone(), q_pos=pos, kv_pos=pos.clone()))
+    out, lse, _ = c.gpu_fwd()
+    torch.cuda.synchronize()
+    o_ref, l_ref = c.oracle_fwd()
+    check_fwd(out, lse, o_ref, l_ref)
+    assert torch.all(out[:, -300:] == 0)
+
+
+# ------------------------------------------------------------ block map
+@pytest.mark.parametrize("seed", range(5))
+def test_block_mask_bit_exact(seed):
+    g = torch.Generator().manual_seed(seed)
+    B, L = 2, 1024 + 128 * seed
+    seg, pos = random_structure(g, B, L, n_docs_max=1 + 2 * seed, pad_max=150 * seed,
+                                shuffle_positions=(seed == 4))
+    causal = seed != 3
+    q = torch.zeros(B, L, 1, 64, dtype=torch.bfloat16, device="cuda")
+    dseg, dpos = seg.cuda(), pos.cuda()
+    p = ra.make_params(q, q, scale=1.0, causal=causal, q_pos=dpos, kv_pos=dpos, q_seg=dseg,
+                       kv_seg=dseg)
+    m = ra.build_mask(p)
+    torch.cuda.synchronize()
+    ref = oracle.block_mask(B, L, L, causal=causal, q_pos=pos.numpy(), kv_pos=pos.numpy(),
+                            q_seg=seg.numpy(), kv_seg=seg.numpy())
+    nq = nk = L // 128
+
+    buf = m._buf
+
+    def dev_arr(ptr, n, dtype):
+        off = ptr - buf.data_ptr()
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        return buf[off:off + nbytes].view(dtype).cpu().numpy()
+
+    got = dict(tile_class=dev_arr(m.tile_class, B * nq * nk, torch.uint8),
+               fwd_cnt=dev_arr(m.fwd_cnt, B * nq, torch.int32),
+               fwd_idx=dev_arr(m.fwd_idx, B * nq * nk, torch.int32),
+               bwd_cnt=dev_arr(m.bwd_cnt, B * nk, torch.int32),
+               bwd_idx=dev_arr(m.bwd_idx, B * nk * nq, torch.int32),
+               fwd_order=dev_arr(m.fwd_order, B * nq, torch.int32),
+               bwd_order=dev_arr(m.bwd_order, B * nk, torch.int32))
+    for key, val in got.items():
+        assert np.array_equal(val.reshape(-1), np.asarray(ref[key]).reshape(-1)), key
+
+
+def test_block_mask_sequential_positions_bit_exact():
+    # no position / segment arrays: positions are the token indices
+    B, L = 1, 2048
+    q = torch.zeros(B, L, 1, 64, dtype=torch.bfloat16, device="cuda")
+    for causal in (True, False):
+        p = ra.make_params(q, q, scale=1.0, causal=causal, n_virtual_shards=4)
+        m = ra.build_mask(p)
+        off = m.tile_class - m._buf.data_ptr()
+        cls = m._buf[off:off + B * 16 * 16].cpu().numpy()
+        ref = oracle.block_mask(B, L, L, causal=causal)
+        assert np.array_equal(cls, ref["tile_class"].reshape(-1))
+
+
+# ------------------------------------------------------------ permutation
+@pytest.mark.parametrize("dtype,inner", [(torch.bfloat16, (4, 64)), (torch.int32, ()),
+                                         (torch.float32, (3,)), (torch.uint8, (5,))])
+@pytest.mark.parametrize("n", [1, 2, 8])
+def test_permute_bit_exact(dtype, inner, n):
+    B, L = 2, 256
+    g = torch.Generator().manual_seed(n)
+    x = (torch.randn((B, L) + inner, generator=g) * 50).to(dtype)
+    y = ra.permute(x.cuda(), n)
+    src = x.view(torch.int16) if dtype == torch.bfloat16 else x
+    ref = oracle.permute(src.numpy(), n)
+    got = y.cpu().view(torch.int16) if dtype == torch.bfloat16 else y.cpu()
+    assert np.array_equal(got.numpy(), ref)
+    back = ra.unpermute(y, n)
+    assert torch.equal(back.cpu(), x)
+
+
+# ------------------------------------------------------------ merge
+def test_merge_matches_oracle():
+    g = torch.Generator().manual_seed(5)
+    B, L, H, D = 2, 300, 3, 128
+    o = torch.randn(B, L, H, D, generator=g)
+    bo = torch.randn(B, L, H, D, generator=g)
+    l = torch.randn(B, H, L, generator=g) * 3
+    bl = torch.randn(B, H, L, generator=g) * 3
+    l[0, 0, :7] = -math.inf      # first merge: take the block
+    bl[1, 2, 5:9] = -math.inf    # empty block: no change
+    l[1, 1, 3] = bl[1, 1, 3] = -math.inf
+    ro, rl = oracle.merge(o.double().numpy(), l.double().numpy(), bo.double().numpy(),
+                          bl.double().numpy())
+    do, dl = o.cuda(), l.cuda()
+    ra.ra_merge_out_lse(do, dl, bo.cuda(), bl.cuda(), B, L, H, D)
+    torch.cuda.synchronize()
+    dl = dl.cpu().double().numpy()
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(dl), fin)
+    assert np.max(np.abs(dl[fin] - rl[fin])) < 1e-5
+    assert np.max(np.abs(do.cpu().double().numpy() - ro)) < 1e-5
+
+
+# ------------------------------------------------------------ backward
+BWD_CASES = {
+    "causal_gqa": W(Hq=4, Hkv=2, L=512, seed=31, n_shards=2),
+    "mqa_sinks_cap": W(Hq=4, Hkv=1, is_mqa=True, sinks=True, soft_cap=5.0, L=512, seed=32),
+    "noncausal": W(causal=False, L=512, seed=33),
+    "d64_zigzag": W(D=64, L=512, zigzag=True, n_shards=2, seed=34),
+}
+
+
+def _check_bwd(c, grads):
+    h = c.host
+    dq, dk, dv, ds, _, _ = oracle.attn_bwd(f64(h["q"]), f64(h["k"]), f64(h["v"]), f64(h["dout"]),
+                                           **c.okw)
+    for name, got, ref in (("dq", grads[0], dq), ("dk", grads[1], dk), ("dv", grads[2], dv)):
+        err = rel_l2(f64(got), ref)
+        assert err <= GRAD_TOL, (name, err)
+    if ds is not None:
+        err = rel_l2(f64(grads[3]), ds)
+        assert err <= GRAD_TOL, ("dsinks", err)
+
+
+@pytest.mark.parametrize("name", list(BWD_CASES))
+def test_backward_matches_oracle(name):
+    c = Case(BWD_CASES[name], dout=True)
+    out, lse, m = c.gpu_fwd()
+    d = c.dev
+    grads = ra.backward(c.params, d["q"], d["k"], d["v"], out, lse, d["dout"], m)
+    torch.cuda.synchronize()
+    _check_bwd(c, grads)
+
+
+def test_backward_packed_docs_with_padding():
+    c = Case(W(B=2, L=768, Hq=2, Hkv=2, seed=35, n_shards=3, sinks=True), dout=True,
+             structure=dict(n_docs_max=4, pad_max=200), seed_struct=9)
+    out, lse, m = c.gpu_fwd()
+    d = c.dev
+    grads = ra.backward(c.params, d["q"], d["k"], d["v"], out, lse, d["dout"], m)
+    torch.cuda.synchronize()
+    _check_bwd(c, grads)

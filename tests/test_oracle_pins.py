@@ -383,3 +383,20 @@ def test_golden_ring_order(ex):
     n = ex["n_shards"]
     got = [[oracle.ring_source(d, t, n) for t in range(n)] for d in range(n)]
     assert got == ex["source"]
+
+
+def test_row_and_head_restriction_equals_full():
+    """Restricted runs (used to sample large workloads) agree with the full oracle on
+    the rows / heads they compute, and the row contributions add up to the full gradient."""
+    q, k, v, kw = _case(41, B=1, L=96, Hq=4, Hkv=2, D=8, segs=True, sinks=True, cap=2.0)
+    o, l = oracle.attn_fwd(q, k, v, **kw)
+    o2, l2 = oracle.attn_fwd(q, k, v, heads=(1, 3), rows=(17, 60), **kw)
+    np.testing.assert_array_equal(o2[:, 17:60, 1:3], o[:, 17:60, 1:3])
+    np.testing.assert_array_equal(l2[:, 1:3, 17:60], l[:, 1:3, 17:60])
+    assert np.all(o2[:, :17] == 0) and np.all(np.isneginf(l2[:, 0]))
+    do = np.random.default_rng(2).normal(size=q.shape)
+    full = oracle.attn_bwd(q, k, v, do, **kw)
+    parts = [oracle.attn_bwd(q, k, v, do, rows=r, heads=hh, **kw)
+             for r in ((0, 50), (50, 96)) for hh in ((0, 1), (1, 4))]
+    for t in range(4):
+        np.testing.assert_allclose(sum(pp[t] for pp in parts), full[t], atol=1e-12)
