@@ -32,6 +32,61 @@ namespace {
 
 constexpr uint32_t kIdescT = idesc_bf16(128, 128, false, false); // S^T / dP^T / S / dP
 
+// Visibility bits of query rows q0..q0+127 for one kv row (dkdv: bit c of
+// word c/32 = query row q0+c sees this kv row).
+__device__ __forceinline__ void col_visibility(const Problem &p, int b, int q0, int kv_seg,
+                                               int kv_pos, uint32_t vis[4])
+{
+    const int4 *qp4 = p.q_pos ? reinterpret_cast<const int4 *>(p.q_pos + (size_t)b * p.Lq + q0) : nullptr;
+    const int4 *qs4 = p.q_seg ? reinterpret_cast<const int4 *>(p.q_seg + (size_t)b * p.Lq + q0) : nullptr;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t bits = 0;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int c = w * 32 + jj * 4;
+            const int4 pv = qp4 ? __ldg(qp4 + (c >> 2)) : make_int4(q0 + c, q0 + c + 1, q0 + c + 2, q0 + c + 3);
+            const int4 sv = qs4 ? __ldg(qs4 + (c >> 2)) : make_int4(0, 0, 0, 0);
+            const int pa[4] = {pv.x, pv.y, pv.z, pv.w};
+            const int sa[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                bool v = (sa[z] == kv_seg) && !(p.q_seg && sa[z] == p.pad_id);
+                if (p.causal) v = v && (pa[z] >= kv_pos);
+                bits |= (v ? 1u : 0u) << (jj * 4 + z);
+            }
+        }
+        vis[w] = bits;
+    }
+}
+
+// Visibility bits of kv rows k0..k0+127 for one query row (dq).
+__device__ __forceinline__ void row_visibility(const Problem &p, int b, int k0, int q_seg,
+                                               bool q_pad, int q_pos, uint32_t vis[4])
+{
+    const int4 *kp4 = p.kv_pos ? reinterpret_cast<const int4 *>(p.kv_pos + (size_t)b * p.Lkv + k0) : nullptr;
+    const int4 *ks4 = p.kv_seg ? reinterpret_cast<const int4 *>(p.kv_seg + (size_t)b * p.Lkv + k0) : nullptr;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t bits = 0;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int c = w * 32 + jj * 4;
+            const int4 pv = kp4 ? __ldg(kp4 + (c >> 2)) : make_int4(k0 + c, k0 + c + 1, k0 + c + 2, k0 + c + 3);
+            const int4 sv = ks4 ? __ldg(ks4 + (c >> 2)) : make_int4(0, 0, 0, 0);
+            const int pa[4] = {pv.x, pv.y, pv.z, pv.w};
+            const int sa[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                bool v = (sa[z] == q_seg) && !q_pad;
+                if (p.causal) v = v && (q_pos >= pa[z]);
+                bits |= (v ? 1u : 0u) << (jj * 4 + z);
+            }
+        }
+        vis[w] = bits;
+    }
+}
+
 // ====================================================================== dkdv
 template <int D>
 struct DkdvCfg {
@@ -282,6 +337,9 @@ __global__ void __launch_bounds__(192, 1)
                         p.tile_class[((size_t)x.b * p.nq + qt) * p.nk + x.kt] == RA_TILE_PARTIAL;
                     if (!(ok = wait_all(bars.s_full, n & 1))) break;
                     tc_fence_after();
+                    // ---- visibility bits of the 128 query columns (partial tiles only)
+                    uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+                    if (partial) col_visibility(p, x.b, qt * kTile, my_seg, my_pos, vis);
                     // ---- P^T (bf16 -> TMEM) and Pc = P * (1 - tanh^2) kept packed
                     uint32_t pc[64];
 #pragma unroll
@@ -290,38 +348,45 @@ __global__ void __launch_bounds__(192, 1)
                         tmem_ld32(lane_base + hh * 64, s);
                         tmem_ld32(lane_base + hh * 64 + 32, s + 32);
                         tmem_ld_wait();
+                        const float4 *l4 = reinterpret_cast<const float4 *>(lse_s + hh * 64);
                         uint32_t pk[32];
+                        if (cap > 0.f) {
 #pragma unroll
-                        for (int j = 0; j < 64; j += 2) {
-                            float pv[2], cv[2];
+                            for (int j = 0; j < 64; j += 4) {
+                                const float4 lv = l4[j >> 2];
+                                const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+                                float pr[4], cr[4];
 #pragma unroll
-                            for (int z = 0; z < 2; ++z) {
-                                const int ci = hh * 64 + j + z; // q column in the tile
-                                float x2, cg = 1.f;
-                                if (cap > 0.f) {
-                                    const float t = tanh_fast(s[j + z] * scale_over_cap);
-                                    x2 = cap2 * t;
-                                    cg = 1.f - t * t;
-                                } else {
-                                    x2 = s[j + z] * scale2;
+                                for (int z = 0; z < 4; ++z) {
+                                    const int c = j + z;
+                                    const float t = tanh_fast(s[c] * scale_over_cap);
+                                    float e = ex2_approx(fmaf(cap2, t, -la[z] * kLog2e));
+                                    e = ((vis[2 * hh + (c >> 5)] >> (c & 31)) & 1u) ? e : 0.f;
+                                    pr[z] = e;
+                                    cr[z] = e * (1.f - t * t);
                                 }
-                                const float l2 = lse_s[ci] * kLog2e;
-                                float pr = (l2 == -INFINITY) ? 0.f : ex2_approx(x2 - l2);
-                                if (partial) {
-                                    const int qi = qt * kTile + ci;
-                                    const int qs = p.q_seg ? p.q_seg[(size_t)x.b * p.Lq + qi] : 0;
-                                    bool vis = (qs == my_seg) && !(p.q_seg && qs == p.pad_id);
-                                    if (p.causal) {
-                                        const int qp = p.q_pos ? p.q_pos[(size_t)x.b * p.Lq + qi] : qi;
-                                        vis = vis && (qp >= my_pos);
-                                    }
-                                    if (!vis) pr = 0.f;
-                                }
-                                pv[z] = pr;
-                                cv[z] = pr * cg;
+                                pk[j >> 1] = pack_bf16x2(pr[0], pr[1]);
+                                pk[(j >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
+                                pc[hh * 32 + (j >> 1)] = pack_bf16x2(cr[0], cr[1]);
+                                pc[hh * 32 + (j >> 1) + 1] = pack_bf16x2(cr[2], cr[3]);
                             }
-                            pk[j >> 1] = pack_bf16x2(pv[0], pv[1]);
-                            pc[hh * 32 + (j >> 1)] = pack_bf16x2(cv[0], cv[1]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 64; j += 4) {
+                                const float4 lv = l4[j >> 2];
+                                const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+                                float pr[4];
+#pragma unroll
+                                for (int z = 0; z < 4; ++z) {
+                                    const int c = j + z;
+                                    float e = ex2_approx(fmaf(s[c], scale2, -la[z] * kLog2e));
+                                    pr[z] = ((vis[2 * hh + (c >> 5)] >> (c & 31)) & 1u) ? e : 0.f;
+                                }
+                                pk[j >> 1] = pack_bf16x2(pr[0], pr[1]);
+                                pk[(j >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
+                                pc[hh * 32 + (j >> 1)] = pk[j >> 1];
+                                pc[hh * 32 + (j >> 1) + 1] = pk[(j >> 1) + 1];
+                            }
                         }
                         tmem_st32(lane_base + hh * 32, pk);
                     }
@@ -335,15 +400,18 @@ __global__ void __launch_bounds__(192, 1)
                         tmem_ld32(lane_base + C::kColDP + hh * 64, dpv);
                         tmem_ld32(lane_base + C::kColDP + hh * 64 + 32, dpv + 32);
                         tmem_ld_wait();
+                        const float4 *d4 = reinterpret_cast<const float4 *>(dl_s + hh * 64);
                         uint32_t dk2[32];
 #pragma unroll
-                        for (int j = 0; j < 64; j += 2) {
-                            const uint32_t w = pc[hh * 32 + (j >> 1)];
-                            const float c0 = __uint_as_float(w << 16);
-                            const float c1 = __uint_as_float(w & 0xffff0000u);
-                            const float d0 = c0 * (dpv[j] - dl_s[hh * 64 + j]);
-                            const float d1 = c1 * (dpv[j + 1] - dl_s[hh * 64 + j + 1]);
-                            dk2[j >> 1] = pack_bf16x2(d0, d1);
+                        for (int j = 0; j < 64; j += 4) {
+                            const float4 dl = d4[j >> 2];
+                            const uint32_t w0 = pc[hh * 32 + (j >> 1)];
+                            const uint32_t w1 = pc[hh * 32 + (j >> 1) + 1];
+                            dk2[j >> 1] = pack_bf16x2(__uint_as_float(w0 << 16) * (dpv[j] - dl.x),
+                                                      __uint_as_float(w0 & 0xffff0000u) * (dpv[j + 1] - dl.y));
+                            dk2[(j >> 1) + 1] =
+                                pack_bf16x2(__uint_as_float(w1 << 16) * (dpv[j + 2] - dl.z),
+                                            __uint_as_float(w1 & 0xffff0000u) * (dpv[j + 3] - dl.w));
                         }
                         tmem_st32(lane_base + C::kColDP + hh * 32, dk2);
                     }
@@ -633,6 +701,8 @@ __global__ void __launch_bounds__(192, 1)
             __nv_bfloat16 *qrow = dq + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D;
             if (x.cnt > 0) {
                 const size_t li = ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
+                // a row with lse = -inf has no visible pair: it only meets partial
+                // tiles, where the mask zeroes every P, so no guard is needed
                 const float l2 = lse[li] * kLog2e;
                 const float dl = delta[li];
                 const int my_pos = p.q_pos ? p.q_pos[(size_t)x.b * p.Lq + qi] : qi;
@@ -642,6 +712,8 @@ __global__ void __launch_bounds__(192, 1)
                 for (int e = 0; e < x.cnt; ++e, ++g) {
                     const int kt = x.list[e];
                     const bool partial = crow[kt] == RA_TILE_PARTIAL;
+                    uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+                    if (partial) row_visibility(p, x.b, kt * kTile, my_seg, my_pad, my_pos, vis);
                     if (!(ok = wait_all(bars.s_full, g & 1))) break;
                     tc_fence_after();
 #pragma unroll
@@ -653,34 +725,33 @@ __global__ void __launch_bounds__(192, 1)
                         tmem_ld32(lane_base + C::kColDP + hh * 64 + 32, dpv + 32);
                         tmem_ld_wait();
                         uint32_t pk[32];
+                        if (cap > 0.f) {
 #pragma unroll
-                        for (int j = 0; j < 64; j += 2) {
-                            float dsv[2];
+                            for (int j = 0; j < 64; j += 2) {
+                                float dsv[2];
 #pragma unroll
-                            for (int z = 0; z < 2; ++z) {
-                                const int cj = hh * 64 + j + z;
-                                float x2, cg = 1.f;
-                                if (cap > 0.f) {
-                                    const float t = tanh_fast(s[j + z] * scale_over_cap);
-                                    x2 = cap2 * t;
-                                    cg = 1.f - t * t;
-                                } else {
-                                    x2 = s[j + z] * scale2;
+                                for (int z = 0; z < 2; ++z) {
+                                    const int c = j + z;
+                                    const float t = tanh_fast(s[c] * scale_over_cap);
+                                    float e = ex2_approx(fmaf(cap2, t, -l2));
+                                    e = ((vis[2 * hh + (c >> 5)] >> (c & 31)) & 1u) ? e : 0.f;
+                                    dsv[z] = e * (1.f - t * t) * (dpv[c] - dl);
                                 }
-                                float pr = (l2 == -INFINITY) ? 0.f : ex2_approx(x2 - l2);
-                                if (partial) {
-                                    const int kj = kt * kTile + cj;
-                                    const int ks = p.kv_seg ? p.kv_seg[(size_t)x.b * p.Lkv + kj] : 0;
-                                    bool vis = (ks == my_seg) && !my_pad;
-                                    if (p.causal) {
-                                        const int kp = p.kv_pos ? p.kv_pos[(size_t)x.b * p.Lkv + kj] : kj;
-                                        vis = vis && (my_pos >= kp);
-                                    }
-                                    if (!vis) pr = 0.f;
-                                }
-                                dsv[z] = pr * cg * (dpv[j + z] - dl);
+                                pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
                             }
-                            pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 64; j += 2) {
+                                float dsv[2];
+#pragma unroll
+                                for (int z = 0; z < 2; ++z) {
+                                    const int c = j + z;
+                                    float e = ex2_approx(fmaf(s[c], scale2, -l2));
+                                    e = ((vis[2 * hh + (c >> 5)] >> (c & 31)) & 1u) ? e : 0.f;
+                                    dsv[z] = e * (dpv[c] - dl);
+                                }
+                                pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                            }
                         }
                         tmem_st32(lane_base + hh * 32, pk);
                     }
