@@ -25,7 +25,8 @@ __all__ = [
     "lib", "ra_last_error", "ra_version", "ra_set_wait_timeout_ns", "ra_block_mask_bytes",
     "ra_build_block_mask", "ra_attn_fwd_workspace_size", "ra_attn_fwd", "ra_merge_out_lse",
     "ra_attn_bwd_workspace_size", "ra_attn_bwd", "ra_attn_bwd_prep", "ra_attn_bwd_dkdv",
-    "ra_attn_bwd_dq", "ra_permute_tokens", "ra_unpermute_tokens",
+    "ra_attn_bwd_dq", "ra_attn_bwd_noalloc", "ra_attn_bwd_noalloc_max_workspace",
+    "ra_permute_tokens", "ra_unpermute_tokens",
     "ra_get_device_status", "ra_launch_count", "make_params", "build_mask", "forward", "backward", "permute",
     "unpermute",
 ]
@@ -109,6 +110,8 @@ def lib():
             L.ra_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, vp, M, vp, vp, sz, vp]
             L.ra_permute_tokens.argtypes = [vp, vp, ci, ci, sz, ci, vp]
             L.ra_unpermute_tokens.argtypes = [vp, vp, ci, ci, sz, ci, vp]
+            L.ra_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, M, vp, vp, vp, vp, vp]
+            L.ra_attn_bwd_noalloc_max_workspace.restype = sz
             L.ra_get_device_status.argtypes = [vp]
             L.ra_launch_count.restype = ctypes.c_uint64
             _lib = L
@@ -189,6 +192,17 @@ def ra_attn_bwd(params, q, k, v, out, lse, dout, mask, dq, dk, dv, dsinks, ws, s
     _check(lib().ra_attn_bwd(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
                              _ptr(lse), _ptr(dout), ctypes.byref(mask), _ptr(dq), _ptr(dk),
                              _ptr(dv), _ptr(dsinks), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def ra_attn_bwd_noalloc(params, q, k, v, out, lse, dout, mask, dq, dk, dv, dsinks, stream=None):
+    """ra_attn_bwd with the library's built-in scratch instead of a workspace."""
+    _check(lib().ra_attn_bwd_noalloc(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                     _ptr(lse), _ptr(dout), ctypes.byref(mask), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), _ptr(dsinks), _stream(stream)))
+
+
+def ra_attn_bwd_noalloc_max_workspace() -> int:
+    return int(lib().ra_attn_bwd_noalloc_max_workspace())
 
 
 def _wsb(ws):

@@ -240,6 +240,9 @@ int encode_rows(CUtensorMap *map, const void *base, int B, int L, int H, int D)
 }
 
 } // namespace
+
+int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 } // namespace ra
 
 using namespace ra;

@@ -67,4 +67,7 @@ cudaError_t fwd_tc_set_attributes(int D);
 cudaError_t bwd_tc_set_attributes(int D);
 cudaError_t simt_set_attributes(int D);
 
+// Records `msg` as this thread's last error message and returns `code`.
+int set_last_error(int code, const char *msg);
+
 } // namespace ra

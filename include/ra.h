@@ -245,6 +245,33 @@ RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k,
                           void *dq, void *ws, size_t ws_bytes, ra_stream_t stream);
 
 /*
+ * ra_attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory themselves (code running inside a host runtime that owns all
+ * of the GPU's memory, or plain-C callers with no allocator at hand).  The
+ * pages have no counterpart of this call; it is a convenience of this
+ * library.
+ *   Same arguments, results and errors as ra_attn_bwd, minus ws / ws_bytes.
+ *   The workspace comes from a fixed array of ra_attn_bwd_noalloc_max_workspace()
+ *   bytes (8 MiB) in the library's device memory, held by every GPU that loads
+ *   the library until the process exits.  Problems whose
+ *   ra_attn_bwd_workspace_size() exceeds it fail with RA_ERR_WORKSPACE
+ *   (roughly B * Hq * Lq above two million query rows); use ra_attn_bwd then.
+ *   Nothing is allocated: no cudaMalloc / cudaFree is ever called.
+ *   The first call on a device looks up the array's device address on that
+ *   device (a synchronous runtime query); make that first call before any
+ *   stream capture begins.
+ *   All calls share the one array and it keeps the last call's contents.
+ *   Calls whose GPU work overlaps in time (different streams, different
+ *   threads, without ordering between them) race on it and give wrong
+ *   results: order them on one stream.
+ */
+RA_API int ra_attn_bwd_noalloc(const ra_attn_params *p, const void *q, const void *k,
+                               const void *v, const void *out, const float *lse,
+                               const void *dout, const ra_block_mask *mask, void *dq, void *dk,
+                               void *dv, float *dsinks, ra_stream_t stream);
+RA_API size_t ra_attn_bwd_noalloc_max_workspace(void);
+
+/*
  * Zigzag load-balancing permutation along the sequence (Kvax context
  * parallelism).  The sequence of L rows is split into 2N chunks of L/(2N);
  * virtual device d holds chunk d followed by chunk 2N-1-d, so permuted row
