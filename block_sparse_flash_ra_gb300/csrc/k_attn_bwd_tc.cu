@@ -32,15 +32,25 @@ namespace {
 
 constexpr uint32_t kIdescT = idesc_bf16(128, 128, false, false); // S^T / dP^T / S / dP
 
-// Visibility bits of query rows q0..q0+127 for one kv row (dkdv: bit c of
+// Warps 0-7: the softmax-gradient work in two warpgroups, each over 64 of the
+// 128 tile columns; warp 8: TMA producer; warp 9: TMEM owner and MMA issuer.
+// The bf16 operand (P^T, dS^T or dS) each group writes back to TMEM lands on
+// columns [0,32) (group 0) or [64,96) (group 1) of the fp32 tile it read,
+// so the 16-row K chunks kk of the next MMA sit at column 8*kk + 32*(kk>=4).
+constexpr int kSoftmaxThreads = 256;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kBwdThreads = 320;
+
+// Visibility bits of query rows q0..q0+63 for one kv row (dkdv: bit c of
 // word c/32 = query row q0+c sees this kv row).
 __device__ __forceinline__ void col_visibility(const Problem &p, int b, int q0, int kv_seg,
-                                               int kv_pos, uint32_t vis[4])
+                                               int kv_pos, uint32_t vis[2])
 {
     const int4 *qp4 = p.q_pos ? reinterpret_cast<const int4 *>(p.q_pos + (size_t)b * p.Lq + q0) : nullptr;
     const int4 *qs4 = p.q_seg ? reinterpret_cast<const int4 *>(p.q_seg + (size_t)b * p.Lq + q0) : nullptr;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < 2; ++w) {
         uint32_t bits = 0;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
@@ -60,14 +70,14 @@ __device__ __forceinline__ void col_visibility(const Problem &p, int b, int q0, 
     }
 }
 
-// Visibility bits of kv rows k0..k0+127 for one query row (dq).
+// Visibility bits of kv rows k0..k0+63 for one query row (dq).
 __device__ __forceinline__ void row_visibility(const Problem &p, int b, int k0, int q_seg,
-                                               bool q_pad, int q_pos, uint32_t vis[4])
+                                               bool q_pad, int q_pos, uint32_t vis[2])
 {
     const int4 *kp4 = p.kv_pos ? reinterpret_cast<const int4 *>(p.kv_pos + (size_t)b * p.Lkv + k0) : nullptr;
     const int4 *ks4 = p.kv_seg ? reinterpret_cast<const int4 *>(p.kv_seg + (size_t)b * p.Lkv + k0) : nullptr;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < 2; ++w) {
         uint32_t bits = 0;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
@@ -102,6 +112,7 @@ struct DkdvCfg {
     // at least 120 KB so that one CTA (which takes all 512 TMEM columns)
     // occupies an SM on its own
     static constexpr int kSmem = (kMiscOff + 16 + 1024) > 122880 ? (kMiscOff + 16 + 1024) : 122880;
+    static_assert(kSmem <= 232448, "dK/dV shared memory exceeds the 227 KB per-block limit");
     static constexpr uint32_t kColDP = 128, kColDV = 256, kColDK = 256 + D;
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);
 };
@@ -147,7 +158,7 @@ __device__ __forceinline__ ColUnit col_unit(const Problem &p, int u)
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     Problem p, const float *__restrict__ lse, const float *__restrict__ delta,
@@ -173,18 +184,18 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bars.st_empty + s, 1);
         }
         mbar_init(bars.s_full, 1);
-        mbar_init(bars.p_ready, 128);
-        mbar_init(bars.ds_ready, 128);
+        mbar_init(bars.p_ready, kSoftmaxThreads);
+        mbar_init(bars.ds_ready, kSoftmaxThreads);
         mbar_init(bars.acc_ready, 1);
         mbar_init(bars.drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             uint32_t n = 0, uk = 0;
@@ -243,7 +254,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (uk) wait_drain(bars.kv_full, (uk - 1) & 1, kDrainNs);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t k_base = smem_u32(smem + C::kKOff);
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(192, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + C::kColDV, tmem + kk * 8,
+                        mma_ts(tmem + C::kColDV, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
                                sdesc_sw128(do_base + kk * 2048, 16384, 1024), C::kIdescAcc,
                                (i > 0 || kk > 0) ? 1u : 0u);
                     // dK += dS^T Q
@@ -292,7 +303,7 @@ __global__ void __launch_bounds__(192, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                        mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
                                sdesc_sw128(q_base + kk * 2048, 16384, 1024), C::kIdescAcc,
                                (i > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bars.st_empty + st);
@@ -306,8 +317,15 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ---------------------------------------------------------- softmax-grad
-        const int row = threadIdx.x; // kv row within the tile
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        // Warps 0-7 in two warpgroups: group wg handles query columns
+        // 64*wg..64*wg+63 (and D/2 columns of dK, dV) of kv row 32*(w%4)+lane.
+        const int wg = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane; // kv row within the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int c0 = wg * 64;
+        constexpr int kOH = D / 2;
+        const uint32_t o_col = wg * kOH;
         const float scale2 = p.scale * kLog2e;
         const float cap = p.soft_cap;
         const float cap2 = cap * kLog2e;
@@ -322,7 +340,7 @@ __global__ void __launch_bounds__(192, 1)
             if (u >= U) continue;
             const ColUnit x = col_unit(p, u);
             const int kj = x.kt * kTile + row;
-            const size_t orow = (((size_t)x.b * p.Lkv + kj) * p.Hkv + x.hkv) * D;
+            const size_t orow = (((size_t)x.b * p.Lkv + kj) * p.Hkv + x.hkv) * D + o_col;
             if (x.cnt > 0) {
                 const int my_pos = p.kv_pos ? p.kv_pos[(size_t)x.b * p.Lkv + kj] : kj;
                 const int my_seg = p.kv_seg ? p.kv_seg[(size_t)x.b * p.Lkv + kj] : 0;
@@ -331,24 +349,23 @@ __global__ void __launch_bounds__(192, 1)
                     const int qt = x.list[i % x.cnt];
                     const int st = n % C::kStages;
                     const float *lse_s = reinterpret_cast<const float *>(
-                        smem + C::kStageOff + st * C::kStageBytes + 2 * C::kTileBytes);
+                        smem + C::kStageOff + st * C::kStageBytes + 2 * C::kTileBytes) + c0;
                     const float *dl_s = lse_s + 128;
                     const bool partial =
                         p.tile_class[((size_t)x.b * p.nq + qt) * p.nk + x.kt] == RA_TILE_PARTIAL;
+                    // ---- visibility bits of this half's 64 query columns (partial tiles only)
+                    uint32_t vis[2] = {~0u, ~0u};
+                    if (partial) col_visibility(p, x.b, qt * kTile + c0, my_seg, my_pos, vis);
                     if (!(ok = wait_all(bars.s_full, n & 1))) break;
                     tc_fence_after();
-                    // ---- visibility bits of the 128 query columns (partial tiles only)
-                    uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
-                    if (partial) col_visibility(p, x.b, qt * kTile, my_seg, my_pos, vis);
                     // ---- P^T (bf16 -> TMEM) and Pc = P * (1 - tanh^2) kept packed
-                    uint32_t pc[64];
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pc[32];
+                    {
                         float s[64];
-                        tmem_ld32(lane_base + hh * 64, s);
-                        tmem_ld32(lane_base + hh * 64 + 32, s + 32);
+                        tmem_ld32(lane_base + c0, s);
+                        tmem_ld32(lane_base + c0 + 32, s + 32);
                         tmem_ld_wait();
-                        const float4 *l4 = reinterpret_cast<const float4 *>(lse_s + hh * 64);
+                        const float4 *l4 = reinterpret_cast<const float4 *>(lse_s);
                         uint32_t pk[32];
                         if (cap > 0.f) {
 #pragma unroll
@@ -361,14 +378,14 @@ __global__ void __launch_bounds__(192, 1)
                                     const int c = j + z;
                                     const float t = tanh_fast(s[c] * scale_over_cap);
                                     float e = ex2_approx(fmaf(cap2, t, -la[z] * kLog2e));
-                                    e = ((vis[2 * hh + (c >> 5)] >> (c & 31)) & 1u) ? e : 0.f;
+                                    e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
                                     pr[z] = e;
                                     cr[z] = e * (1.f - t * t);
                                 }
                                 pk[j >> 1] = pack_bf16x2(pr[0], pr[1]);
                                 pk[(j >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
-                                pc[hh * 32 + (j >> 1)] = pack_bf16x2(cr[0], cr[1]);
-                                pc[hh * 32 + (j >> 1) + 1] = pack_bf16x2(cr[2], cr[3]);
+                                pc[j >> 1] = pack_bf16x2(cr[0], cr[1]);
+                                pc[(j >> 1) + 1] = pack_bf16x2(cr[2], cr[3]);
                             }
                         } else {
 #pragma unroll
@@ -379,56 +396,56 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                                 for (int z = 0; z < 4; ++z) {
                                     const int c = j + z;
-                                    float e = ex2_approx(fmaf(s[c], scale2, -la[z] * kLog2e));
-                                    pr[z] = ((vis[2 * hh + (c >> 5)] >> (c & 31)) & 1u) ? e : 0.f;
+                                    const float e = ex2_approx(fmaf(s[c], scale2, -la[z] * kLog2e));
+                                    pr[z] = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
                                 }
                                 pk[j >> 1] = pack_bf16x2(pr[0], pr[1]);
                                 pk[(j >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
-                                pc[hh * 32 + (j >> 1)] = pk[j >> 1];
-                                pc[hh * 32 + (j >> 1) + 1] = pk[(j >> 1) + 1];
+                                pc[j >> 1] = pk[j >> 1];
+                                pc[(j >> 1) + 1] = pk[(j >> 1) + 1];
                             }
                         }
-                        tmem_st32(lane_base + hh * 32, pk);
+                        // this half's P^T over the S^T columns it has just read
+                        tmem_st32(lane_base + c0, pk);
                     }
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(bars.p_ready);
                     // ---- dS^T = Pc (dP^T - Delta)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    {
                         float dpv[64];
-                        tmem_ld32(lane_base + C::kColDP + hh * 64, dpv);
-                        tmem_ld32(lane_base + C::kColDP + hh * 64 + 32, dpv + 32);
+                        tmem_ld32(lane_base + C::kColDP + c0, dpv);
+                        tmem_ld32(lane_base + C::kColDP + c0 + 32, dpv + 32);
                         tmem_ld_wait();
-                        const float4 *d4 = reinterpret_cast<const float4 *>(dl_s + hh * 64);
+                        const float4 *d4 = reinterpret_cast<const float4 *>(dl_s);
                         uint32_t dk2[32];
 #pragma unroll
                         for (int j = 0; j < 64; j += 4) {
                             const float4 dl = d4[j >> 2];
-                            const uint32_t w0 = pc[hh * 32 + (j >> 1)];
-                            const uint32_t w1 = pc[hh * 32 + (j >> 1) + 1];
+                            const uint32_t w0 = pc[j >> 1];
+                            const uint32_t w1 = pc[(j >> 1) + 1];
                             dk2[j >> 1] = pack_bf16x2(__uint_as_float(w0 << 16) * (dpv[j] - dl.x),
                                                       __uint_as_float(w0 & 0xffff0000u) * (dpv[j + 1] - dl.y));
                             dk2[(j >> 1) + 1] =
                                 pack_bf16x2(__uint_as_float(w1 << 16) * (dpv[j + 2] - dl.z),
                                             __uint_as_float(w1 & 0xffff0000u) * (dpv[j + 3] - dl.w));
                         }
-                        tmem_st32(lane_base + C::kColDP + hh * 32, dk2);
+                        tmem_st32(lane_base + C::kColDP + c0, dk2);
                     }
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(bars.ds_ready);
                 }
                 if (!ok) break;
-                // ---- epilogue: dV, scale * dK -> bf16
+                // ---- epilogue: this half of dV and scale * dK -> bf16
                 if (!(ok = wait_all(bars.acc_ready, ua & 1))) break;
                 ++ua;
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < kOH / 32; ++c) {
                     float a[32], bk[32];
-                    tmem_ld32(lane_base + C::kColDV + c * 32, a);
-                    tmem_ld32(lane_base + C::kColDK + c * 32, bk);
+                    tmem_ld32(lane_base + C::kColDV + o_col + c * 32, a);
+                    tmem_ld32(lane_base + C::kColDK + o_col + c * 32, bk);
                     tmem_ld_wait();
                     uint4 *dvp = reinterpret_cast<uint4 *>(dv + orow + c * 32);
                     uint4 *dkp = reinterpret_cast<uint4 *>(dk + orow + c * 32);
@@ -450,7 +467,7 @@ __global__ void __launch_bounds__(192, 1)
             } else {
                 uint4 *dvp = reinterpret_cast<uint4 *>(dv + orow);
                 uint4 *dkp = reinterpret_cast<uint4 *>(dk + orow);
-                for (int k4 = 0; k4 < D / 8; ++k4) {
+                for (int k4 = 0; k4 < kOH / 8; ++k4) {
                     dvp[k4] = make_uint4(0, 0, 0, 0);
                     dkp[k4] = make_uint4(0, 0, 0, 0);
                 }
@@ -460,7 +477,7 @@ __global__ void __launch_bounds__(192, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -480,6 +497,7 @@ struct DqCfg {
     static constexpr int kNumBars = 2 + 4 * kStages + 4;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmem = (kMiscOff + 16 + 1024) > 122880 ? (kMiscOff + 16 + 1024) : 122880;
+    static_assert(kSmem <= 232448, "dQ shared memory exceeds the 227 KB per-block limit");
     static constexpr uint32_t kColDP = 128, kColDQ = 256;
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);
 };
@@ -526,7 +544,7 @@ __device__ __forceinline__ RowUnit row_unit(const Problem &p, int u)
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   Problem p, const float *__restrict__ lse, const float *__restrict__ delta,
@@ -554,17 +572,17 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bars.v_empty + s, 1);
         }
         mbar_init(bars.s_full, 1);
-        mbar_init(bars.ds_ready, 128);
+        mbar_init(bars.ds_ready, kSoftmaxThreads);
         mbar_init(bars.acc_ready, 1);
         mbar_init(bars.drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
@@ -575,7 +593,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             uint32_t g = 0, uq = 0;
@@ -623,7 +641,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t q_base = smem_u32(smem + C::kQOff);
@@ -669,7 +687,7 @@ __global__ void __launch_bounds__(192, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + C::kColDQ, tmem + kk * 8,
+                        mma_ts(tmem + C::kColDQ, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
                                sdesc_sw128(kb + kk * 2048, 16384, 1024), C::kIdescAcc,
                                (e > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bars.k_empty + st);
@@ -682,8 +700,15 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ---------------------------------------------------------- softmax-grad
-        const int row = threadIdx.x;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        // Warps 0-7 in two warpgroups: group wg handles kv columns
+        // 64*wg..64*wg+63 (and D/2 columns of dQ) of query row 32*(w%4)+lane.
+        const int wg = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int c0 = wg * 64;
+        constexpr int kOH = D / 2;
+        const uint32_t o_col = wg * kOH;
         const float scale2 = p.scale * kLog2e;
         const float cap = p.soft_cap;
         const float cap2 = cap * kLog2e;
@@ -698,7 +723,7 @@ __global__ void __launch_bounds__(192, 1)
             if (u >= U) continue;
             const RowUnit x = row_unit(p, u);
             const int qi = x.qt * kTile + row;
-            __nv_bfloat16 *qrow = dq + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D;
+            __nv_bfloat16 *qrow = dq + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D + o_col;
             if (x.cnt > 0) {
                 const size_t li = ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
                 // a row with lse = -inf has no visible pair: it only meets partial
@@ -712,49 +737,47 @@ __global__ void __launch_bounds__(192, 1)
                 for (int e = 0; e < x.cnt; ++e, ++g) {
                     const int kt = x.list[e];
                     const bool partial = crow[kt] == RA_TILE_PARTIAL;
-                    uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
-                    if (partial) row_visibility(p, x.b, kt * kTile, my_seg, my_pad, my_pos, vis);
+                    uint32_t vis[2] = {~0u, ~0u};
+                    if (partial) row_visibility(p, x.b, kt * kTile + c0, my_seg, my_pad, my_pos, vis);
                     if (!(ok = wait_all(bars.s_full, g & 1))) break;
                     tc_fence_after();
+                    float s[64], dpv[64];
+                    tmem_ld32(lane_base + c0, s);
+                    tmem_ld32(lane_base + c0 + 32, s + 32);
+                    tmem_ld32(lane_base + C::kColDP + c0, dpv);
+                    tmem_ld32(lane_base + C::kColDP + c0 + 32, dpv + 32);
+                    tmem_ld_wait();
+                    uint32_t pk[32];
+                    if (cap > 0.f) {
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float s[64], dpv[64];
-                        tmem_ld32(lane_base + hh * 64, s);
-                        tmem_ld32(lane_base + hh * 64 + 32, s + 32);
-                        tmem_ld32(lane_base + C::kColDP + hh * 64, dpv);
-                        tmem_ld32(lane_base + C::kColDP + hh * 64 + 32, dpv + 32);
-                        tmem_ld_wait();
-                        uint32_t pk[32];
-                        if (cap > 0.f) {
+                        for (int j = 0; j < 64; j += 2) {
+                            float dsv[2];
 #pragma unroll
-                            for (int j = 0; j < 64; j += 2) {
-                                float dsv[2];
-#pragma unroll
-                                for (int z = 0; z < 2; ++z) {
-                                    const int c = j + z;
-                                    const float t = tanh_fast(s[c] * scale_over_cap);
-                                    float e = ex2_approx(fmaf(cap2, t, -l2));
-                                    e = ((vis[2 * hh + (c >> 5)] >> (c & 31)) & 1u) ? e : 0.f;
-                                    dsv[z] = e * (1.f - t * t) * (dpv[c] - dl);
-                                }
-                                pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                            for (int z = 0; z < 2; ++z) {
+                                const int c = j + z;
+                                const float t = tanh_fast(s[c] * scale_over_cap);
+                                float e = ex2_approx(fmaf(cap2, t, -l2));
+                                e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
+                                dsv[z] = e * (1.f - t * t) * (dpv[c] - dl);
                             }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 64; j += 2) {
-                                float dsv[2];
-#pragma unroll
-                                for (int z = 0; z < 2; ++z) {
-                                    const int c = j + z;
-                                    float e = ex2_approx(fmaf(s[c], scale2, -l2));
-                                    e = ((vis[2 * hh + (c >> 5)] >> (c & 31)) & 1u) ? e : 0.f;
-                                    dsv[z] = e * (dpv[c] - dl);
-                                }
-                                pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
-                            }
+                            pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
                         }
-                        tmem_st32(lane_base + hh * 32, pk);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 64; j += 2) {
+                            float dsv[2];
+#pragma unroll
+                            for (int z = 0; z < 2; ++z) {
+                                const int c = j + z;
+                                float e = ex2_approx(fmaf(s[c], scale2, -l2));
+                                e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
+                                dsv[z] = e * (dpv[c] - dl);
+                            }
+                            pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                        }
                     }
+                    // this half's dS over the S columns it has just read
+                    tmem_st32(lane_base + c0, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(bars.ds_ready);
@@ -764,9 +787,9 @@ __global__ void __launch_bounds__(192, 1)
                 ++ua;
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < kOH / 32; ++c) {
                     float a[32];
-                    tmem_ld32(lane_base + C::kColDQ + c * 32, a);
+                    tmem_ld32(lane_base + C::kColDQ + o_col + c * 32, a);
                     tmem_ld_wait();
                     uint4 *dst = reinterpret_cast<uint4 *>(qrow + c * 32);
 #pragma unroll
@@ -781,14 +804,14 @@ __global__ void __launch_bounds__(192, 1)
                 }
             } else {
                 uint4 *dst = reinterpret_cast<uint4 *>(qrow);
-                for (int k4 = 0; k4 < D / 8; ++k4) dst[k4] = make_uint4(0, 0, 0, 0);
+                for (int k4 = 0; k4 < kOH / 8; ++k4) dst[k4] = make_uint4(0, 0, 0, 0);
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -830,9 +853,9 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *t
     const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
     __nv_bfloat16 *gk = static_cast<__nv_bfloat16 *>(dk), *gv = static_cast<__nv_bfloat16 *>(dv);
     if (p.D == 64)
-        bwd_dkdv_kernel<64><<<grid, 192, DkdvCfg<64>::kSmem, s>>>(q, k, v, d, p, lse, delta, gk, gv);
+        bwd_dkdv_kernel<64><<<grid, kBwdThreads, DkdvCfg<64>::kSmem, s>>>(q, k, v, d, p, lse, delta, gk, gv);
     else
-        bwd_dkdv_kernel<128><<<grid, 192, DkdvCfg<128>::kSmem, s>>>(q, k, v, d, p, lse, delta, gk, gv);
+        bwd_dkdv_kernel<128><<<grid, kBwdThreads, DkdvCfg<128>::kSmem, s>>>(q, k, v, d, p, lse, delta, gk, gv);
     return cudaGetLastError();
 }
 
@@ -848,9 +871,9 @@ cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_
     const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
     __nv_bfloat16 *gq = static_cast<__nv_bfloat16 *>(dq);
     if (p.D == 64)
-        bwd_dq_kernel<64><<<grid, 192, DqCfg<64>::kSmem, s>>>(q, k, v, d, p, lse, delta, gq);
+        bwd_dq_kernel<64><<<grid, kBwdThreads, DqCfg<64>::kSmem, s>>>(q, k, v, d, p, lse, delta, gq);
     else
-        bwd_dq_kernel<128><<<grid, 192, DqCfg<128>::kSmem, s>>>(q, k, v, d, p, lse, delta, gq);
+        bwd_dq_kernel<128><<<grid, kBwdThreads, DqCfg<128>::kSmem, s>>>(q, k, v, d, p, lse, delta, gq);
     return cudaGetLastError();
 }
 

@@ -14,13 +14,16 @@
 // the sigmoid/softplus update.  Output is bf16, lse fp32.
 //
 // Design (one CTA per SM, persistent, longest-row-first static schedule):
-//   warps 0-3  softmax / merge / epilogue; thread t owns query row t, which
-//              is TMEM lane t (warp w may only touch lanes 32w..32w+31)
-//   warp 4     TMA producer: Q once per work unit, K and V tiles into a
-//              kStages-deep ring of shared-memory stages
-//   warp 5     TMEM allocator and single-thread MMA issuer
+//   warps 0-7  softmax / merge / epilogue in two warpgroups that split the
+//              128 columns of each S row (and the D columns of O); the two
+//              threads of a query row exchange row max and row sum through
+//              shared memory (warp w may only touch TMEM lanes 32(w%4)..+31)
+//   warp 8     TMA producer: Q once per work unit, K and V tiles into a
+//              rings of shared-memory stages (2 for K, 3 for V at D = 128)
+//   warp 9     TMEM allocator and single-thread MMA issuer
 // TMEM (512 columns x 128 lanes, fp32):
-//   [0,128)   S buffer 0   (P of that tile overwrites its first 64 columns)
+//   [0,128)   S buffer 0   (P of the tile, bf16, overwrites columns [0,32)
+//                           and [64,96): each half over columns it has read)
 //   [128,256) S buffer 1
 //   [256,256+D)      O_acc  shard accumulator
 //   [256+D,256+2D)   O_run  running merged output of the ring
@@ -38,15 +41,21 @@ namespace {
 template <int D>
 struct FwdCfg {
     static constexpr int kTileBytes = kTile * D * 2; // one 128-row bf16 tile
-    static constexpr int kStages = (D == 128) ? 3 : 4;
+    // K tiles are consumed at once by S = Q K^T; V tiles wait for the softmax,
+    // so the V ring is the deeper one
+    static constexpr int kKStages = (D == 128) ? 2 : 3;
+    static constexpr int kVStages = (D == 128) ? 3 : 4;
+    static constexpr int kMaxStages = kVStages;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kTileBytes;
-    static constexpr int kVOff = kKOff + kStages * kTileBytes;
-    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 2 + 4 * kStages + 5 + 1;
+    static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+    static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 5 + 1 + 4;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kSmemUsed = kMiscOff + 16;
+    static constexpr int kXOff = kMiscOff + 16;                  // row max / sum exchange
+    static constexpr int kSmemUsed = kXOff + 2 * 2 * 2 * 128 * 4;
     static constexpr int kSmem = kSmemUsed + 1024; // slack for 1024-byte alignment
+    static_assert(kSmem <= 232448, "forward shared memory exceeds the 227 KB per-block limit");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 256;
     static constexpr uint32_t kColRun = 256 + D;
@@ -56,7 +65,7 @@ struct FwdCfg {
 
 struct Bars {
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full, *pv_done,
-        *drain;
+        *drain, *xsync;
 };
 
 template <int D>
@@ -68,13 +77,14 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *smem)
     r.q_full = b;
     r.q_empty = b + 1;
     r.k_full = b + 2;
-    r.k_empty = r.k_full + C::kStages;
-    r.v_full = r.k_empty + C::kStages;
-    r.v_empty = r.v_full + C::kStages;
-    r.s_full = r.v_empty + C::kStages;
+    r.k_empty = r.k_full + C::kKStages;
+    r.v_full = r.k_empty + C::kKStages;
+    r.v_empty = r.v_full + C::kVStages;
+    r.s_full = r.v_empty + C::kVStages;
     r.p_full = r.s_full + 2;
     r.pv_done = r.p_full + 2;
     r.drain = r.pv_done + 1;
+    r.xsync = r.drain + 1;
     return r;
 }
 
@@ -105,8 +115,13 @@ __device__ __forceinline__ void shard_range(const Problem &p, const Unit &x, int
     hi = lower_bound_i32(x.list, x.cnt, (src + 1) * p.tk);
 }
 
+constexpr int kSoftmaxThreads = 256; // warps 0-7
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kFwdThreads = 320;
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, Problem p,
@@ -128,26 +143,29 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0) {
         mbar_init(bars.q_full, 1);
         mbar_init(bars.q_empty, 1);
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bars.k_full + s, 1);
             mbar_init(bars.k_empty + s, 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(bars.v_full + s, 1);
             mbar_init(bars.v_empty + s, 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bars.s_full + s, 1);
-            mbar_init(bars.p_full + s, 128);
+            mbar_init(bars.p_full + s, kSoftmaxThreads);
         }
         mbar_init(bars.pv_done, 1);
         mbar_init(bars.drain, 1);
+        for (int q4 = 0; q4 < 4; ++q4) mbar_init(bars.xsync + q4, 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_holder, C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
@@ -157,11 +175,11 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t g = 0, uq = 0;
-            uint32_t k_issued[C::kStages] = {}, v_issued[C::kStages] = {};
+            uint32_t k_issued[C::kMaxStages] = {}, v_issued[C::kMaxStages] = {};
             bool ok = true;
             for (int r = 0; ok && r * G < U; ++r) {
                 const int u = unit_index(r, blockIdx.x, G);
@@ -180,34 +198,34 @@ __global__ void __launch_bounds__(192, 1)
                     shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
                     for (int e = lo; e < hi; ++e) {
                         const int kt = x.list[e];
-                        const int st = g % C::kStages;
-                        const uint32_t ph = (g / C::kStages) & 1;
-                        if (!(ok = mbar_wait(bars.k_empty + st, ph ^ 1, ctx))) break;
-                        mbar_expect_tx(bars.k_full + st, C::kTileBytes);
+                        const int sk = g % C::kKStages;
+                        if (!(ok = mbar_wait(bars.k_empty + sk, ((g / C::kKStages) & 1) ^ 1, ctx))) break;
+                        mbar_expect_tx(bars.k_full + sk, C::kTileBytes);
                         for (int hb = 0; hb < D / 64; ++hb)
-                            tma_load_4d(smem + C::kKOff + st * C::kTileBytes + hb * 16384, &tm_k,
-                                        bars.k_full + st, hb * 64, g_kv, kt * kTile, x.b);
-                        ++k_issued[st];
-                        if (!(ok = mbar_wait(bars.v_empty + st, ph ^ 1, ctx))) break;
-                        mbar_expect_tx(bars.v_full + st, C::kTileBytes);
+                            tma_load_4d(smem + C::kKOff + sk * C::kTileBytes + hb * 16384, &tm_k,
+                                        bars.k_full + sk, hb * 64, g_kv, kt * kTile, x.b);
+                        ++k_issued[sk];
+                        const int sv = g % C::kVStages;
+                        if (!(ok = mbar_wait(bars.v_empty + sv, ((g / C::kVStages) & 1) ^ 1, ctx))) break;
+                        mbar_expect_tx(bars.v_full + sv, C::kTileBytes);
                         for (int hb = 0; hb < D / 64; ++hb)
-                            tma_load_4d(smem + C::kVOff + st * C::kTileBytes + hb * 16384, &tm_v,
-                                        bars.v_full + st, hb * 64, g_kv, kt * kTile, x.b);
-                        ++v_issued[st];
+                            tma_load_4d(smem + C::kVOff + sv * C::kTileBytes + hb * 16384, &tm_v,
+                                        bars.v_full + sv, hb * 64, g_kv, kt * kTile, x.b);
+                        ++v_issued[sv];
                         ++g;
                     }
                 }
             }
             if (!ok) {
                 // let the copies already issued land before the CTA exits
-                for (int s = 0; s < C::kStages; ++s) {
+                for (int s = 0; s < C::kKStages; ++s)
                     if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
+                for (int s = 0; s < C::kVStages; ++s)
                     if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
-                }
                 if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t q_base = smem_u32(smem + C::kQOff);
@@ -220,14 +238,17 @@ __global__ void __launch_bounds__(192, 1)
             auto issue_pv = [&](uint32_t pg, bool first) -> bool {
                 const int sb = pg & 1;
                 if (!mbar_wait(bars.p_full + sb, (pg >> 1) & 1, ctx)) return false;
-                const int st = pg % C::kStages;
-                if (!mbar_wait(bars.v_full + st, (pg / C::kStages) & 1, ctx)) return false;
+                const int st = pg % C::kVStages;
+                if (!mbar_wait(bars.v_full + st, (pg / C::kVStages) & 1, ctx)) return false;
                 tc_fence_after();
                 const uint32_t vb = v_base + st * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, 16384, 1024);
-                    mma_ts(tmem + C::kColO, tmem + sb * 128 + kk * 8, bdesc, C::kIdescPV,
+                    // P of kv rows 16kk..16kk+15: the half of warps 0-3 (kk < 4) sits
+                    // in columns [0,32) of the S buffer, the other half in [64,96)
+                    const uint32_t acol = sb * 128 + kk * 8 + (kk >= 4 ? 32 : 0);
+                    mma_ts(tmem + C::kColO, tmem + acol, bdesc, C::kIdescPV,
                            (kk > 0 || !first) ? 1u : 0u);
                 }
                 tc_commit(bars.v_empty + st);
@@ -247,8 +268,8 @@ __global__ void __launch_bounds__(192, 1)
                     int lo, hi;
                     shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
                     for (int e = lo; e < hi; ++e) {
-                        const int st = g % C::kStages;
-                        if (!(ok = mbar_wait(bars.k_full + st, (g / C::kStages) & 1, ctx))) break;
+                        const int st = g % C::kKStages;
+                        if (!(ok = mbar_wait(bars.k_full + st, (g / C::kKStages) & 1, ctx))) break;
                         tc_fence_after();
                         const int sb = g & 1;
                         const uint32_t kb = k_base + st * C::kTileBytes;
@@ -276,13 +297,25 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int row = threadIdx.x; // 0..127 == TMEM lane
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        // Two warpgroups split the 128 S columns of every query row: warps
+        // 0-3 take columns 0-63, warps 4-7 columns 64-127.  Warp w may only
+        // touch TMEM lanes 32*(w%4)..+31, so thread t of both groups owns
+        // query row 32*(w%4) + lane.  Row maxima and row sums are exchanged
+        // between the two threads of a row through shared memory.
+        const int wg = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int c0 = wg * 64;                 // first S column of this half
+        constexpr int kOH = D / 2;              // O columns of this half
+        const uint32_t o_col = wg * kOH;
+        float *xmax = reinterpret_cast<float *>(smem + C::kXOff);   // [2 slots][2 halves][128]
+        float *xsum = xmax + 2 * 2 * 128;                          // [2 slots][2 halves][128]
         const float scale2 = p.scale * kLog2e;
         const float cap = p.soft_cap;
         const float cap2 = cap * kLog2e;
         const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
-        uint32_t g = 0, pv_seen = 0;
+        uint32_t g = 0, pv_seen = 0, nshard = 0;
         bool ok = true;
         // waits of the softmax warps are made warp-uniform, so that no warp
         // reaches a .sync.aligned tcgen05 instruction with some lanes gone
@@ -296,12 +329,20 @@ __global__ void __launch_bounds__(192, 1)
             }
             return true;
         };
+        // the two threads of a row meet at mbarrier xsync[quarter] (64
+        // arrivals per phase); unlike a named barrier its wait is bounded, so
+        // a group whose partner aborted gives up too
+        uint32_t xph = 0;
+        auto pair_sync = [&]() -> bool {
+            mbar_arrive(bars.xsync + quarter);
+            return wait_all(bars.xsync + quarter, (xph++) & 1);
+        };
         for (int r = 0; ok && r * G < U; ++r) {
             const int u = unit_index(r, blockIdx.x, G);
             if (u >= U) continue;
             const Unit x = unit_of(p, u);
             const int qi = x.qt * kTile + row;
-            __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D;
+            __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D + o_col;
             float *lrow = lse + ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
             const bool has_sink = p.sinks != nullptr;
             const float sink2 = has_sink ? p.sinks[x.h] * kLog2e : 0.f;
@@ -320,9 +361,7 @@ __global__ void __launch_bounds__(192, 1)
                         // empty shard: partial is (0, -inf), or (0, sink) at t = 0
                         if (sink_here) {
                             const float ls = sink2 * kLn2;
-                            if (lse_run == -INFINITY) lse_run = ls;
-                            else lse_run = lse_run + softplus_f(ls - lse_run);
-                            // O_run = O_run * (1 - w): only possible when t == 0, so O_run == 0
+                            lse_run = (lse_run == -INFINITY) ? ls : lse_run + softplus_f(ls - lse_run);
                         }
                         continue;
                     }
@@ -331,55 +370,67 @@ __global__ void __launch_bounds__(192, 1)
                         const int kt = x.list[e];
                         const bool partial = crow[kt] == RA_TILE_PARTIAL;
                         const int sb = g & 1;
+                        uint32_t vis0 = ~0u, vis1 = ~0u;
+                        if (partial) {
+                            // visibility of kv columns kt*128 + c0 .. +63 for this row
+                            const int j0 = kt * kTile + c0;
+                            const int4 *kp4 = p.kv_pos
+                                ? reinterpret_cast<const int4 *>(p.kv_pos + (size_t)x.b * p.Lkv + j0) : nullptr;
+                            const int4 *ks4 = p.kv_seg
+                                ? reinterpret_cast<const int4 *>(p.kv_seg + (size_t)x.b * p.Lkv + j0) : nullptr;
+                            uint32_t bits[2] = {0u, 0u};
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) {
+                                const int4 pv = kp4 ? __ldg(kp4 + jj)
+                                                    : make_int4(j0 + 4 * jj, j0 + 4 * jj + 1,
+                                                                j0 + 4 * jj + 2, j0 + 4 * jj + 3);
+                                const int4 sv = ks4 ? __ldg(ks4 + jj) : make_int4(0, 0, 0, 0);
+                                const int pa[4] = {pv.x, pv.y, pv.z, pv.w};
+                                const int sa[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+                                for (int z = 0; z < 4; ++z) {
+                                    bool vis = (sa[z] == my_seg) && !my_pad;
+                                    if (p.causal) vis = vis && (my_pos >= pa[z]);
+                                    bits[jj >> 3] |= (vis ? 1u : 0u) << ((4 * jj + z) & 31);
+                                }
+                            }
+                            vis0 = bits[0];
+                            vis1 = bits[1];
+                        }
                         if (!(ok = wait_all(bars.s_full + sb, (g >> 1) & 1))) break;
                         tc_fence_after();
-                        float s[128];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + sb * 128 + c * 32, s + c * 32);
+                        float s[64];
+                        tmem_ld32(lane_base + sb * 128 + c0, s);
+                        tmem_ld32(lane_base + sb * 128 + c0 + 32, s + 32);
                         tmem_ld_wait();
                         if (cap > 0.f) {
 #pragma unroll
-                            for (int j = 0; j < 128; ++j) s[j] = cap2 * tanh_fast(s[j] * scale_over_cap);
+                            for (int j = 0; j < 64; ++j) s[j] = cap2 * tanh_fast(s[j] * scale_over_cap);
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 128; ++j) s[j] *= scale2;
+                            for (int j = 0; j < 64; ++j) s[j] *= scale2;
                         }
                         if (partial) {
-                            const int j0 = kt * kTile;
-                            const int4 *kp4 = p.kv_pos
-                                ? reinterpret_cast<const int4 *>(p.kv_pos + (size_t)x.b * p.Lkv + j0)
-                                : nullptr;
-                            const int4 *ks4 = p.kv_seg
-                                ? reinterpret_cast<const int4 *>(p.kv_seg + (size_t)x.b * p.Lkv + j0)
-                                : nullptr;
 #pragma unroll
-                            for (int jj = 0; jj < 32; ++jj) {
-                                int4 pv = kp4 ? __ldg(kp4 + jj)
-                                              : make_int4(j0 + 4 * jj, j0 + 4 * jj + 1,
-                                                          j0 + 4 * jj + 2, j0 + 4 * jj + 3);
-                                int4 sv = ks4 ? __ldg(ks4 + jj) : make_int4(0, 0, 0, 0);
-                                const int pj[4] = {pv.x, pv.y, pv.z, pv.w};
-                                const int sj[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-                                for (int q4 = 0; q4 < 4; ++q4) {
-                                    bool vis = (sj[q4] == my_seg) && !my_pad;
-                                    if (p.causal) vis = vis && (my_pos >= pj[q4]);
-                                    if (!vis) s[4 * jj + q4] = -INFINITY;
-                                }
-                            }
+                            for (int j = 0; j < 64; ++j)
+                                if (!(((j < 32 ? vis0 : vis1) >> (j & 31)) & 1u)) s[j] = -INFINITY;
                         }
                         float mx[8];
 #pragma unroll
                         for (int k = 0; k < 8; ++k) mx[k] = s[k];
 #pragma unroll
-                        for (int j = 8; j < 128; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
-                        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                        for (int j = 8; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+                        float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                        float *xm = xmax + (g & 1) * 256;
+                        xm[wg * 128 + row] = tmax;
+                        if (!(ok = pair_sync())) break;
+                        tmax = fmaxf(tmax, xm[(wg ^ 1) * 128 + row]);
                         const float m_new = fmaxf(m_ref, tmax);
                         const bool need = (m_ref != -INFINITY) && (m_new > m_ref + 8.f);
                         if (m_ref == -INFINITY) m_ref = m_new;
                         if (__any_sync(0xffffffffu, need)) {
-                            // rescale O_acc: the previous PV product must be complete
+                            // rescale this half of O_acc: the previous PV product must be complete
                             if (!(ok = wait_pv_upto(g))) break;
                             tc_fence_after();
                             const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
@@ -388,30 +439,31 @@ __global__ void __launch_bounds__(192, 1)
                                 m_ref = m_new;
                             }
 #pragma unroll
-                            for (int c = 0; c < D / 32; ++c) {
+                            for (int c = 0; c < kOH / 32; ++c) {
                                 float o[32];
-                                tmem_ld32(lane_base + C::kColO + c * 32, o);
+                                tmem_ld32(lane_base + C::kColO + o_col + c * 32, o);
                                 tmem_ld_wait();
                                 uint32_t w32[32];
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) w32[j] = __float_as_uint(o[j] * f);
-                                tmem_st32(lane_base + C::kColO + c * 32, w32);
+                                tmem_st32(lane_base + C::kColO + o_col + c * 32, w32);
                             }
                             tmem_st_wait();
                         }
                         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
                         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        uint32_t pk[64];
+                        uint32_t pk[32];
 #pragma unroll
-                        for (int j = 0; j < 128; j += 2) {
+                        for (int j = 0; j < 64; j += 2) {
                             const float a = ex2_approx(s[j] - m_use);
                             const float b2 = ex2_approx(s[j + 1] - m_use);
                             ls[(j >> 1) & 7] += a + b2;
                             pk[j >> 1] = pack_bf16x2(a, b2);
                         }
                         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                        tmem_st32(lane_base + sb * 128, pk);
-                        tmem_st32(lane_base + sb * 128 + 32, pk + 32);
+                        // P of this half: columns [64*wg, 64*wg + 32) of the S buffer,
+                        // which this half has already read
+                        tmem_st32(lane_base + sb * 128 + c0, pk);
                         tmem_st_wait();
                         // PV(g-1) must be complete before P(g) is published
                         if (!(ok = wait_pv_upto(g))) break;
@@ -423,6 +475,11 @@ __global__ void __launch_bounds__(192, 1)
                     // ---- shard end: normalise, add the sink (t == 0), merge
                     if (!(ok = wait_pv_upto(g))) break;
                     tc_fence_after();
+                    float *xs = xsum + (nshard & 1) * 256;
+                    ++nshard;
+                    xs[wg * 128 + row] = l;
+                    if (!(ok = pair_sync())) break;
+                    l += xs[(wg ^ 1) * 128 + row];
                     float m_fin = m_ref, fac = 1.f;
                     if (sink_here) {
                         m_fin = fmaxf(m_ref, sink2);
@@ -440,10 +497,10 @@ __global__ void __launch_bounds__(192, 1)
                     const bool first = (lse_run == -INFINITY);
                     const float w = first ? 1.f : sigmoid_f(lse_s - lse_run);
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < kOH / 32; ++c) {
                         float a[32], cur[32];
-                        tmem_ld32(lane_base + C::kColO + c * 32, a);
-                        if (orun_set) tmem_ld32(lane_base + C::kColRun + c * 32, cur);
+                        tmem_ld32(lane_base + C::kColO + o_col + c * 32, a);
+                        if (orun_set) tmem_ld32(lane_base + C::kColRun + o_col + c * 32, cur);
                         tmem_ld_wait();
                         uint32_t nv[32];
 #pragma unroll
@@ -452,7 +509,7 @@ __global__ void __launch_bounds__(192, 1)
                             const float cv = orun_set ? cur[j] : 0.f;
                             nv[j] = __float_as_uint(first ? os : cv - w * (cv - os));
                         }
-                        tmem_st32(lane_base + C::kColRun + c * 32, nv);
+                        tmem_st32(lane_base + C::kColRun + o_col + c * 32, nv);
                     }
                     tmem_st_wait();
                     lse_run = first ? lse_s : lse_run + softplus_f(lse_s - lse_run);
@@ -462,12 +519,12 @@ __global__ void __launch_bounds__(192, 1)
             } else if (has_sink) {
                 lse_run = sink2 * kLn2;
             }
-            // ---- epilogue: O_run -> bf16, lse
+            // ---- epilogue: this half of O_run -> bf16, lse
             if (orun_set) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < kOH / 32; ++c) {
                     float a[32];
-                    tmem_ld32(lane_base + C::kColRun + c * 32, a);
+                    tmem_ld32(lane_base + C::kColRun + o_col + c * 32, a);
                     tmem_ld_wait();
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
@@ -483,15 +540,15 @@ __global__ void __launch_bounds__(192, 1)
             } else {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-                for (int k = 0; k < D / 8; ++k) dst[k] = make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < kOH / 8; ++k) dst[k] = make_uint4(0, 0, 0, 0);
             }
-            *lrow = lse_run;
+            if (wg == 0) *lrow = lse_run;
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -524,9 +581,9 @@ cudaError_t launch_fwd_tc(const Problem &p, const void *tm_q, const void *tm_k, 
     const CUtensorMap &v = *static_cast<const CUtensorMap *>(tm_v);
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
     if (p.D == 64)
-        fwd_tc_kernel<64><<<grid, 192, FwdCfg<64>::kSmem, s>>>(q, k, v, p, o, lse);
+        fwd_tc_kernel<64><<<grid, kFwdThreads, FwdCfg<64>::kSmem, s>>>(q, k, v, p, o, lse);
     else
-        fwd_tc_kernel<128><<<grid, 192, FwdCfg<128>::kSmem, s>>>(q, k, v, p, o, lse);
+        fwd_tc_kernel<128><<<grid, kFwdThreads, FwdCfg<128>::kSmem, s>>>(q, k, v, p, o, lse);
     return cudaGetLastError();
 }
 
