@@ -20,7 +20,7 @@
 //   dq:   one work unit per (b, q head, 128-row query tile); it walks the
 //         non-empty kv tiles of its block-map row.  Thread t owns query row
 //         t.  TMEM: S [0,128), dP [128,256), dQ [256,256+D); dS (bf16)
-//         overwrites S and feeds dQ += dS K from TMEM.
+//         overwrites dP and feeds dQ += dS K from TMEM.
 // The dkdv kernel recomputes S and dP per tile and the dq kernel recomputes
 // them again: 7 tile products instead of 5, in exchange for no fp32 atomics.
 #include <math.h>
@@ -107,7 +107,7 @@ struct DkdvCfg {
     static constexpr int kStageOff = 2 * kTileBytes;
     static constexpr int kStages = 2;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    static constexpr int kNumBars = 2 + 2 * kStages + 5;
+    static constexpr int kNumBars = 2 + 2 * kStages + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // at least 120 KB so that one CTA (which takes all 512 TMEM columns)
     // occupies an SM on its own
@@ -118,8 +118,8 @@ struct DkdvCfg {
 };
 
 struct DkdvBars {
-    uint64_t *kv_full, *kv_empty, *st_full, *st_empty, *s_full, *p_ready, *ds_ready, *acc_ready,
-        *drain;
+    uint64_t *kv_full, *kv_empty, *st_full, *st_empty, *s_full, *dp_full, *p_ready, *ds_ready,
+        *acc_ready, *drain;
 };
 
 template <int D>
@@ -133,7 +133,8 @@ __device__ __forceinline__ DkdvBars dkdv_bars(uint8_t *smem)
     r.st_full = b + 2;
     r.st_empty = r.st_full + C::kStages;
     r.s_full = r.st_empty + C::kStages;
-    r.p_ready = r.s_full + 1;
+    r.dp_full = r.s_full + 1;
+    r.p_ready = r.dp_full + 1;
     r.ds_ready = r.p_ready + 1;
     r.acc_ready = r.ds_ready + 1;
     r.drain = r.acc_ready + 1;
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bars.st_empty + s, 1);
         }
         mbar_init(bars.s_full, 1);
+        mbar_init(bars.dp_full, 1);
         mbar_init(bars.p_ready, kSoftmaxThreads);
         mbar_init(bars.ds_ready, kSoftmaxThreads);
         mbar_init(bars.acc_ready, 1);
@@ -261,6 +263,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t v_base = smem_u32(smem + C::kVOff);
             uint32_t n = 0, uk = 0;
             bool ok = true;
+            auto stage_base = [&](uint32_t step) {
+                return smem_u32(smem + C::kStageOff + (step % C::kStages) * C::kStageBytes);
+            };
+            auto wait_stage = [&](uint32_t step) -> bool {
+                if (!mbar_wait(bars.st_full + step % C::kStages, (step / C::kStages) & 1, ctx)) return false;
+                tc_fence_after();
+                return true;
+            };
+            // S^T = K Q^T into columns [0,128)
+            auto issue_s = [&](uint32_t q_base) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tmem, sdesc_sw128(k_base + off, 16, 1024),
+                           sdesc_sw128(q_base + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bars.s_full);
+            };
+            // dP^T = V dO^T into columns [128,256)
+            auto issue_dp = [&](uint32_t do_base) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
+                           sdesc_sw128(do_base + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bars.dp_full);
+            };
+            // Issue order per step n (each product overlaps a softmax phase):
+            //   dP(n) | phase A(n);  dV(n), S(n+1) | phase B(n);
+            //   dK(n), dP(n+1) | phase A(n+1).
+            // S(n+1) may overwrite P^T(n) once dV(n) is issued (MMAs run in
+            // order); dP(n+1) may overwrite dS^T(n) once dK(n) is issued.
             for (int r = 0; ok && r * Gd < U; ++r) {
                 const int u = unit_index(r, blockIdx.x, Gd);
                 if (u >= U) continue;
@@ -270,26 +305,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 ++uk;
                 const int steps = p.G * x.cnt;
+                if (!(ok = wait_stage(n))) break;
+                issue_s(stage_base(n));
                 for (int i = 0; i < steps; ++i, ++n) {
-                    const int st = n % C::kStages;
-                    if (!(ok = mbar_wait(bars.st_full + st, (n / C::kStages) & 1, ctx))) break;
-                    tc_fence_after();
-                    const uint32_t q_base = smem_u32(smem + C::kStageOff + st * C::kStageBytes);
+                    const uint32_t q_base = stage_base(n);
                     const uint32_t do_base = q_base + C::kTileBytes;
-                    // S^T = K Q^T and dP^T = V dO^T
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem, sdesc_sw128(k_base + off, 16, 1024),
-                               sdesc_sw128(q_base + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
-                               sdesc_sw128(do_base + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(bars.s_full);
+                    issue_dp(do_base);
                     // dV += P^T dO   (A = P^T from TMEM, B = dO as a K=q x N=D MN-major tile)
                     if (!(ok = mbar_wait(bars.p_ready, n & 1, ctx))) break;
                     tc_fence_after();
@@ -298,6 +319,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_ts(tmem + C::kColDV, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
                                sdesc_sw128(do_base + kk * 2048, 16384, 1024), C::kIdescAcc,
                                (i > 0 || kk > 0) ? 1u : 0u);
+                    if (i + 1 < steps) {
+                        if (!(ok = wait_stage(n + 1))) break;
+                        issue_s(stage_base(n + 1));
+                    }
                     // dK += dS^T Q
                     if (!(ok = mbar_wait(bars.ds_ready, n & 1, ctx))) break;
                     tc_fence_after();
@@ -306,7 +331,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
                                sdesc_sw128(q_base + kk * 2048, 16384, 1024), C::kIdescAcc,
                                (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bars.st_empty + st);
+                    tc_commit(bars.st_empty + n % C::kStages);
                 }
                 if (!ok) break;
                 tc_commit(bars.kv_empty);
@@ -412,6 +437,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tc_fence_before();
                     mbar_arrive(bars.p_ready);
                     // ---- dS^T = Pc (dP^T - Delta)
+                    if (!(ok = wait_all(bars.dp_full, n & 1))) break;
+                    tc_fence_after();
                     {
                         float dpv[64];
                         tmem_ld32(lane_base + C::kColDP + c0, dpv);
@@ -494,7 +521,7 @@ struct DqCfg {
     static constexpr int kStages = 2;
     static constexpr int kVOff = kKOff + kStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 2 + 4 * kStages + 4;
+    static constexpr int kNumBars = 2 + 4 * kStages + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmem = (kMiscOff + 16 + 1024) > 122880 ? (kMiscOff + 16 + 1024) : 122880;
     static_assert(kSmem <= 232448, "dQ shared memory exceeds the 227 KB per-block limit");
@@ -503,8 +530,8 @@ struct DqCfg {
 };
 
 struct DqBars {
-    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *ds_ready,
-        *acc_ready, *drain;
+    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *dp_full, *s_free,
+        *ds_ready, *acc_ready, *drain;
 };
 
 template <int D>
@@ -520,7 +547,9 @@ __device__ __forceinline__ DqBars dq_bars(uint8_t *smem)
     r.v_full = r.k_empty + C::kStages;
     r.v_empty = r.v_full + C::kStages;
     r.s_full = r.v_empty + C::kStages;
-    r.ds_ready = r.s_full + 1;
+    r.dp_full = r.s_full + 1;
+    r.s_free = r.dp_full + 1;
+    r.ds_ready = r.s_free + 1;
     r.acc_ready = r.ds_ready + 1;
     r.drain = r.acc_ready + 1;
     return r;
@@ -572,6 +601,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bars.v_empty + s, 1);
         }
         mbar_init(bars.s_full, 1);
+        mbar_init(bars.dp_full, 1);
+        mbar_init(bars.s_free, kSoftmaxThreads);
         mbar_init(bars.ds_ready, kSoftmaxThreads);
         mbar_init(bars.acc_ready, 1);
         mbar_init(bars.drain, 1);
@@ -650,6 +681,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t v_base = smem_u32(smem + C::kVOff);
             uint32_t g = 0, uq = 0;
             bool ok = true;
+            auto wait_kv = [&](uint32_t t) -> bool {
+                const int st = t % C::kStages;
+                const uint32_t ph = (t / C::kStages) & 1;
+                if (!mbar_wait(bars.k_full + st, ph, ctx)) return false;
+                if (!mbar_wait(bars.v_full + st, ph, ctx)) return false;
+                tc_fence_after();
+                return true;
+            };
+            // S = Q K^T of tile t into columns [0,128)
+            auto issue_s = [&](uint32_t t) {
+                const uint32_t kb = k_base + (t % C::kStages) * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tmem, sdesc_sw128(q_base + off, 16, 1024),
+                           sdesc_sw128(kb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bars.s_full);
+            };
+            // dP = dO V^T of tile t into columns [128,256)
+            auto issue_dp = [&](uint32_t t) {
+                const uint32_t vb = v_base + (t % C::kStages) * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tmem + C::kColDP, sdesc_sw128(do_base + off, 16, 1024),
+                           sdesc_sw128(vb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bars.dp_full);
+            };
+            // Issue order per tile g (each product overlaps a softmax phase):
+            //   dP(g) | phase A(g) (P from S);  S(g+1) | phase B(g) (dS from dP);
+            //   dQ(g), dP(g+1) | phase A(g+1).
+            // dS(g) is written over dP(g), so S(g+1) only needs phase A(g) to
+            // have read S(g); dP(g+1) follows dQ(g), the last reader of dS(g).
             for (int r = 0; ok && r * Gd < U; ++r) {
                 const int u = unit_index(r, blockIdx.x, Gd);
                 if (u >= U) continue;
@@ -658,36 +724,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
                 tc_fence_after();
                 ++uq;
+                if (!(ok = wait_kv(g))) break;
+                issue_s(g);
                 for (int e = 0; e < x.cnt; ++e, ++g) {
                     const int st = g % C::kStages;
-                    const uint32_t ph = (g / C::kStages) & 1;
-                    if (!(ok = mbar_wait(bars.k_full + st, ph, ctx))) break;
-                    if (!(ok = mbar_wait(bars.v_full + st, ph, ctx))) break;
-                    tc_fence_after();
-                    const uint32_t kb = k_base + st * C::kTileBytes;
-                    const uint32_t vb = v_base + st * C::kTileBytes;
-                    // S = Q K^T, dP = dO V^T
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem, sdesc_sw128(q_base + off, 16, 1024),
-                               sdesc_sw128(kb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem + C::kColDP, sdesc_sw128(do_base + off, 16, 1024),
-                               sdesc_sw128(vb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
-                    }
+                    issue_dp(g);
                     tc_commit(bars.v_empty + st);
-                    tc_commit(bars.s_full);
                     if (e == x.cnt - 1) tc_commit(bars.q_empty);
+                    if (!(ok = mbar_wait(bars.s_free, g & 1, ctx))) break;
+                    if (e + 1 < x.cnt) {
+                        if (!(ok = wait_kv(g + 1))) break;
+                        issue_s(g + 1);
+                    }
                     // dQ += dS K   (A = dS from TMEM, B = K as a K=kv x N=D MN-major tile)
                     if (!(ok = mbar_wait(bars.ds_ready, g & 1, ctx))) break;
                     tc_fence_after();
+                    const uint32_t kb = k_base + st * C::kTileBytes;
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + C::kColDQ, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
+                        mma_ts(tmem + C::kColDQ, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
                                sdesc_sw128(kb + kk * 2048, 16384, 1024), C::kIdescAcc,
                                (e > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bars.k_empty + st);
@@ -741,43 +796,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (partial) row_visibility(p, x.b, kt * kTile + c0, my_seg, my_pad, my_pos, vis);
                     if (!(ok = wait_all(bars.s_full, g & 1))) break;
                     tc_fence_after();
-                    float s[64], dpv[64];
-                    tmem_ld32(lane_base + c0, s);
-                    tmem_ld32(lane_base + c0 + 32, s + 32);
-                    tmem_ld32(lane_base + C::kColDP + c0, dpv);
-                    tmem_ld32(lane_base + C::kColDP + c0 + 32, dpv + 32);
-                    tmem_ld_wait();
-                    uint32_t pk[32];
-                    if (cap > 0.f) {
+                    // ---- phase A: Pc = P * (1 - tanh^2), packed bf16 (P from S)
+                    uint32_t pc[32];
+                    {
+                        float s[64];
+                        tmem_ld32(lane_base + c0, s);
+                        tmem_ld32(lane_base + c0 + 32, s + 32);
+                        tmem_ld_wait();
+                        if (cap > 0.f) {
 #pragma unroll
-                        for (int j = 0; j < 64; j += 2) {
-                            float dsv[2];
+                            for (int j = 0; j < 64; j += 2) {
+                                float cv[2];
 #pragma unroll
-                            for (int z = 0; z < 2; ++z) {
-                                const int c = j + z;
-                                const float t = tanh_fast(s[c] * scale_over_cap);
-                                float e = ex2_approx(fmaf(cap2, t, -l2));
-                                e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
-                                dsv[z] = e * (1.f - t * t) * (dpv[c] - dl);
+                                for (int z = 0; z < 2; ++z) {
+                                    const int c = j + z;
+                                    const float t = tanh_fast(s[c] * scale_over_cap);
+                                    float e = ex2_approx(fmaf(cap2, t, -l2));
+                                    e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
+                                    cv[z] = e * (1.f - t * t);
+                                }
+                                pc[j >> 1] = pack_bf16x2(cv[0], cv[1]);
                             }
-                            pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
-                        }
-                    } else {
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < 64; j += 2) {
-                            float dsv[2];
+                            for (int j = 0; j < 64; j += 2) {
+                                float cv[2];
 #pragma unroll
-                            for (int z = 0; z < 2; ++z) {
-                                const int c = j + z;
-                                float e = ex2_approx(fmaf(s[c], scale2, -l2));
-                                e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
-                                dsv[z] = e * (dpv[c] - dl);
+                                for (int z = 0; z < 2; ++z) {
+                                    const int c = j + z;
+                                    const float e = ex2_approx(fmaf(s[c], scale2, -l2));
+                                    cv[z] = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
+                                }
+                                pc[j >> 1] = pack_bf16x2(cv[0], cv[1]);
                             }
-                            pk[j >> 1] = pack_bf16x2(dsv[0], dsv[1]);
                         }
                     }
-                    // this half's dS over the S columns it has just read
-                    tmem_st32(lane_base + c0, pk);
+                    tc_fence_before();
+                    mbar_arrive(bars.s_free);
+                    // ---- phase B: dS = Pc (dP - Delta), written over this half's dP columns
+                    if (!(ok = wait_all(bars.dp_full, g & 1))) break;
+                    tc_fence_after();
+                    {
+                        float dpv[64];
+                        tmem_ld32(lane_base + C::kColDP + c0, dpv);
+                        tmem_ld32(lane_base + C::kColDP + c0 + 32, dpv + 32);
+                        tmem_ld_wait();
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int j = 0; j < 64; j += 2) {
+                            const uint32_t w = pc[j >> 1];
+                            pk[j >> 1] = pack_bf16x2(__uint_as_float(w << 16) * (dpv[j] - dl),
+                                                     __uint_as_float(w & 0xffff0000u) * (dpv[j + 1] - dl));
+                        }
+                        tmem_st32(lane_base + C::kColDP + c0, pk);
+                    }
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(bars.ds_ready);
