@@ -40,9 +40,15 @@ from workloads import WORKLOADS, make_inputs  # noqa: E402
 METRIC = "masked-attention TFLOP/s fwd and fwd+bwd (unmasked tiles) and % BF16 tensor peak"
 UNIT = "TFLOP/s"
 
-# DRAM traffic per launch of each kernel from an ncu capture (bytes), with the
-# sha256 of the kernel source it was taken on; a changed source reports null.
-TRAFFIC = {}
+# DRAM traffic per launch of each kernel from an ncu capture (bytes), keyed by
+# (workload, kernel), with the sha256 of the kernel source it was taken on; a
+# changed source, or another workload, reports null.
+TRAFFIC = {
+    # profiles/dram_attention_gqa32k.md (gqa32k, one launch each)
+    ("gqa32k", "fwd_tc_kernel"): (3.15e9 + 0.278e9, "1adb6381766b5f8e"),
+    ("gqa32k", "bwd_dkdv_kernel"): (4.24e9 + 0.118e9, "21f166d1fdaad727"),
+    ("gqa32k", "bwd_dq_kernel"): (3.47e9 + 0.240e9, "21f166d1fdaad727"),
+}
 
 
 def _peaks():
@@ -280,7 +286,7 @@ def run_ours(args, w, ws_, rank, local):
     d_ms, d_flops, d_src = kern[dom]
     achieved = tf(d_flops, d_ms)
     peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
-    tr = TRAFFIC.get(dom)
+    tr = TRAFFIC.get((w.name, dom))
     traffic = tr[0] if tr and tr[1] == _src_hash(d_src) else None
     value = tf(pipe.f_fwd_bwd, ms_step) * ws_
     fwd_tf = tf(pipe.f_fwd, per["fwd"])
