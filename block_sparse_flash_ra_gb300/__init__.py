@@ -69,8 +69,9 @@ class RaBlockMask(ctypes.Structure):
         ("tile_class", ctypes.c_void_p), ("fwd_cnt", ctypes.c_void_p),
         ("fwd_idx", ctypes.c_void_p), ("bwd_cnt", ctypes.c_void_p),
         ("bwd_idx", ctypes.c_void_p), ("fwd_order", ctypes.c_void_p),
-        ("bwd_order", ctypes.c_void_p), ("B", ctypes.c_int), ("nq", ctypes.c_int),
-        ("nk", ctypes.c_int), ("key", ctypes.c_uint64),
+        ("bwd_order", ctypes.c_void_p), ("fwd_shard", ctypes.c_void_p), ("B", ctypes.c_int),
+        ("nq", ctypes.c_int), ("nk", ctypes.c_int), ("n_shards", ctypes.c_int),
+        ("key", ctypes.c_uint64),
     ]
 
 

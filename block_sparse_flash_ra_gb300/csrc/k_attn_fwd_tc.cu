@@ -92,6 +92,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *smem)
 struct Unit {
     int b, qt, h, row, cnt, dev;
     const int32_t *list;
+    const int32_t *shard; // N+1 offsets into list: where each KV shard's tiles begin
 };
 
 __device__ __forceinline__ Unit unit_of(const Problem &p, int u)
@@ -104,6 +105,7 @@ __device__ __forceinline__ Unit unit_of(const Problem &p, int u)
     x.cnt = p.fwd_cnt[x.row];
     x.dev = x.qt / p.tq;
     x.list = p.fwd_idx + (size_t)x.row * p.nk;
+    x.shard = p.fwd_shard + (size_t)x.row * (p.N + 1);
     return x;
 }
 
@@ -111,8 +113,8 @@ __device__ __forceinline__ Unit unit_of(const Problem &p, int u)
 __device__ __forceinline__ void shard_range(const Problem &p, const Unit &x, int src, int &lo,
                                             int &hi)
 {
-    lo = lower_bound_i32(x.list, x.cnt, src * p.tk);
-    hi = lower_bound_i32(x.list, x.cnt, (src + 1) * p.tk);
+    lo = x.shard[src];
+    hi = x.shard[src + 1];
 }
 
 constexpr int kSoftmaxThreads = 256; // warps 0-7

@@ -12,7 +12,8 @@
 //    exactly from the summaries (disjoint segment ranges; one common segment,
 //    where the causal predicate reduces to comparing position ranges) are
 //    classified from them; the rest are counted pair by pair.  The block then
-//    compacts the non-empty kt of its row into fwd_idx.
+//    compacts the non-empty kt of its row into fwd_idx and records where the
+//    tiles of each KV shard begin in that list (fwd_shard).
 // 3. columns: one block per (b, kt) compacts the non-empty qt into bwd_idx.
 // 4. order: stable counting sort of rows (columns) by descending count.
 #include "ra_internal.h"
@@ -86,7 +87,8 @@ constexpr int kCls = 256; // threads of classify / column kernels
 // grid (nq, B)
 __global__ void __launch_bounds__(kCls) classify_rows_kernel(Problem p, const TileSum *qsum,
                                                              const TileSum *ksum, uint8_t *cls,
-                                                             int32_t *fwd_cnt, int32_t *fwd_idx)
+                                                             int32_t *fwd_cnt, int32_t *fwd_idx,
+                                                             int32_t *fwd_shard)
 {
     const int b = blockIdx.y, qt = blockIdx.x, nk = p.nk;
     __shared__ int q_seg_s[kTile], q_pos_s[kTile], k_seg_s[kTile], k_pos_s[kTile];
@@ -167,6 +169,20 @@ __global__ void __launch_bounds__(kCls) classify_rows_kernel(Problem p, const Ti
     const int cnt = base;
     for (int r = cnt + threadIdx.x; r < nk; r += kCls) irow[r] = -1;
     if (threadIdx.x == 0) fwd_cnt[(size_t)b * p.nq + qt] = cnt;
+    // shard s of the ring covers kt in [s*tk, (s+1)*tk): its first list
+    // position is the number of listed tiles below s*tk (the compacted row
+    // is visible to the whole block after the barrier above)
+    int32_t *srow = fwd_shard + ((size_t)b * p.nq + qt) * (p.N + 1);
+    for (int sh = threadIdx.x; sh <= p.N; sh += kCls) {
+        const int key = sh * p.tk;
+        int lo = 0, hi = cnt;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (irow[mid] < key) lo = mid + 1;
+            else hi = mid;
+        }
+        srow[sh] = lo;
+    }
 }
 
 // grid (nk, B): column compaction
@@ -266,13 +282,15 @@ size_t mask_scratch_ints(int B, int nq, int nk)
 
 cudaError_t launch_mask_build(const Problem &p, uint8_t *cls, int32_t *fwd_cnt, int32_t *fwd_idx,
                               int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order,
-                              int32_t *bwd_order, int32_t *scratch, cudaStream_t s)
+                              int32_t *bwd_order, int32_t *fwd_shard, int32_t *scratch,
+                              cudaStream_t s)
 {
     TileSum *qsum = reinterpret_cast<TileSum *>(scratch);
     TileSum *ksum = qsum + (size_t)p.B * p.nq;
     tile_summary_kernel<<<dim3(p.nq, p.B), 128, 0, s>>>(p.q_seg, p.q_pos, p.Lq, p.pad_id, qsum);
     tile_summary_kernel<<<dim3(p.nk, p.B), 128, 0, s>>>(p.kv_seg, p.kv_pos, p.Lkv, p.pad_id, ksum);
-    classify_rows_kernel<<<dim3(p.nq, p.B), kCls, 0, s>>>(p, qsum, ksum, cls, fwd_cnt, fwd_idx);
+    classify_rows_kernel<<<dim3(p.nq, p.B), kCls, 0, s>>>(p, qsum, ksum, cls, fwd_cnt, fwd_idx,
+                                                          fwd_shard);
     columns_kernel<<<dim3(p.nk, p.B), kCls, 0, s>>>(cls, p.nq, p.nk, bwd_cnt, bwd_idx);
     const size_t sm_f = sizeof(int) * ((size_t)p.nk + 1 + 1024);
     const size_t sm_b = sizeof(int) * ((size_t)p.nq + 1 + 1024);

@@ -140,6 +140,7 @@ uint64_t mask_key(const ra_attn_params *p)
     h = mix(h, (uint64_t)p->Lq);
     h = mix(h, (uint64_t)p->Lkv);
     h = mix(h, (uint64_t)p->causal);
+    h = mix(h, (uint64_t)p->n_virtual_shards);
     h = mix(h, (uint64_t)(uint32_t)p->pad_segment_id);
     h = mix(h, reinterpret_cast<uintptr_t>(p->q_pos));
     h = mix(h, reinterpret_cast<uintptr_t>(p->kv_pos));
@@ -149,7 +150,7 @@ uint64_t mask_key(const ra_attn_params *p)
 }
 
 struct MaskLayout {
-    size_t cls, fwd_cnt, fwd_idx, bwd_cnt, bwd_idx, fwd_order, bwd_order, scratch, total;
+    size_t cls, fwd_cnt, fwd_idx, bwd_cnt, bwd_idx, fwd_order, bwd_order, fwd_shard, scratch, total;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -166,6 +167,7 @@ MaskLayout mask_layout(const ra_attn_params *p)
     m.bwd_idx = o;   o += up256(4 * B * nk * nq);
     m.fwd_order = o; o += up256(4 * B * nq);
     m.bwd_order = o; o += up256(4 * B * nk);
+    m.fwd_shard = o; o += up256(4 * B * nq * ((size_t)p->n_virtual_shards + 1));
     m.scratch = o;   o += up256(4 * mask_scratch_ints((int)B, (int)nq, (int)nk));
     m.total = o;
     return m;
@@ -203,6 +205,7 @@ Problem make_problem(const ra_attn_params *p, const ra_block_mask *m, int *statu
         x.bwd_idx = m->bwd_idx;
         x.fwd_order = m->fwd_order;
         x.bwd_order = m->bwd_order;
+        x.fwd_shard = m->fwd_shard;
     }
     x.status = status;
     x.timeout_ns = g_timeout_ns.load();
@@ -213,12 +216,12 @@ int check_mask(const ra_attn_params *p, const ra_block_mask *m)
 {
     if (!m) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
     if (!m->tile_class || !m->fwd_cnt || !m->fwd_idx || !m->bwd_cnt || !m->bwd_idx ||
-        !m->fwd_order || !m->bwd_order)
+        !m->fwd_order || !m->bwd_order || !m->fwd_shard)
         return fail(RA_ERR_INVALID_ARG, "mask has NULL arrays (not built?)");
     if (m->B != p->B || m->nq != p->Lq / RA_TILE || m->nk != p->Lkv / RA_TILE ||
-        m->key != mask_key(p))
-        return fail(RA_ERR_INVALID_ARG,
-                    "mask was built for other params (sizes, causal, padding id or pos/seg arrays)");
+        m->n_shards != p->n_virtual_shards || m->key != mask_key(p))
+        return fail(RA_ERR_INVALID_ARG, "mask was built for other params (sizes, causal, shards, "
+                                        "padding id or pos/seg arrays)");
     return RA_OK;
 }
 
@@ -286,13 +289,15 @@ RA_API int ra_build_block_mask(const ra_attn_params *p, void *buf, size_t buf_by
     m.bwd_idx = reinterpret_cast<int32_t *>(b + L.bwd_idx);
     m.fwd_order = reinterpret_cast<int32_t *>(b + L.fwd_order);
     m.bwd_order = reinterpret_cast<int32_t *>(b + L.bwd_order);
+    m.fwd_shard = reinterpret_cast<int32_t *>(b + L.fwd_shard);
     m.B = p->B;
     m.nq = p->Lq / RA_TILE;
     m.nk = p->Lkv / RA_TILE;
+    m.n_shards = p->n_virtual_shards;
     m.key = mask_key(p);
     const Problem pr = make_problem(p, nullptr, dc->status);
     cudaError_t e = launch_mask_build(pr, m.tile_class, m.fwd_cnt, m.fwd_idx, m.bwd_cnt, m.bwd_idx,
-                                      m.fwd_order, m.bwd_order,
+                                      m.fwd_order, m.bwd_order, m.fwd_shard,
                                       reinterpret_cast<int32_t *>(b + L.scratch),
                                       reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "mask build launch");

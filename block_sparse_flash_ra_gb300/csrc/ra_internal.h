@@ -27,6 +27,7 @@ struct Problem {
     // block map
     const uint8_t *tile_class;
     const int32_t *fwd_cnt, *fwd_idx, *bwd_cnt, *bwd_idx, *fwd_order, *bwd_order;
+    const int32_t *fwd_shard; // (B*nq, N+1) first fwd_idx position of each KV shard
     // failure reporting
     int *status;
     uint64_t timeout_ns;
@@ -37,7 +38,8 @@ cudaError_t launch_permute(const void *in, void *out, int B, int L, size_t row_b
                            int inverse, cudaStream_t s);
 cudaError_t launch_mask_build(const Problem &p, uint8_t *cls, int32_t *fwd_cnt, int32_t *fwd_idx,
                               int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order,
-                              int32_t *bwd_order, int32_t *scratch, cudaStream_t s);
+                              int32_t *bwd_order, int32_t *fwd_shard, int32_t *scratch,
+                              cudaStream_t s);
 size_t mask_scratch_ints(int B, int nq, int nk);
 cudaError_t launch_merge(float *out, float *lse, const float *bout, const float *blse, int B,
                          int L, int H, int D, cudaStream_t s);

@@ -1,6 +1,6 @@
 // ra_sched.cuh -- work-unit scheduling helpers shared by the persistent
 // tensor-core kernels: snake round-robin over a longest-first unit order,
-// tile-list range search, bounded drain waits and the scalar merge math.
+// bounded drain waits and the scalar merge math.
 #pragma once
 
 #include "ra_device.cuh"
@@ -12,18 +12,6 @@ namespace ra {
 __device__ __forceinline__ int unit_index(int round, int cta, int G)
 {
     return round * G + ((round & 1) ? (G - 1 - cta) : cta);
-}
-
-// First position in the ascending list with list[pos] >= key.
-__device__ __forceinline__ int lower_bound_i32(const int32_t *list, int n, int key)
-{
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (list[mid] < key) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
 }
 
 // Wait used only while tearing down after an abort: bounded, ignores the

@@ -129,6 +129,11 @@ typedef struct {
  *   fwd_order   (B*nq) row ids b*nq+qt by descending fwd_cnt, ties by id
  *               (the longest-first schedule of the forward).
  *   bwd_order   (B*nk) column ids b*nk+kt, same rule (backward schedule).
+ *   fwd_shard   (B*nq, N+1) with N = n_virtual_shards: entry s of a row is
+ *               the position in its fwd_idx row of the first tile with
+ *               kt >= s*nk/N, so KV shard s owns fwd_idx[fwd_shard[s] ..
+ *               fwd_shard[s+1]) (entry N = fwd_cnt).  The forward walks a
+ *               row's shards in ring order through these offsets.
  *   key         fingerprint of the ra_attn_params fields the map depends on;
  *               attention calls reject a map built for other params.
  */
@@ -140,7 +145,8 @@ typedef struct {
     int32_t *bwd_idx;
     int32_t *fwd_order;
     int32_t *bwd_order;
-    int B, nq, nk;
+    int32_t *fwd_shard;
+    int B, nq, nk, n_shards;
     uint64_t key;
 } ra_block_mask;
 

@@ -178,10 +178,11 @@ def test_block_mask_bit_exact(seed):
     seg, pos = random_structure(g, B, L, n_docs_max=1 + 2 * seed, pad_max=150 * seed,
                                 shuffle_positions=(seed == 4))
     causal = seed != 3
+    n_shards = (4, 3, 5, 11, 6)[seed]  # divides nq = 8 + seed
     q = torch.zeros(B, L, 1, 64, dtype=torch.bfloat16, device="cuda")
     dseg, dpos = seg.cuda(), pos.cuda()
     p = ra.make_params(q, q, scale=1.0, causal=causal, q_pos=dpos, kv_pos=dpos, q_seg=dseg,
-                       kv_seg=dseg)
+                       kv_seg=dseg, n_virtual_shards=n_shards)
     m = ra.build_mask(p)
     torch.cuda.synchronize()
     ref = oracle.block_mask(B, L, L, causal=causal, q_pos=pos.numpy(), kv_pos=pos.numpy(),
@@ -204,6 +205,14 @@ def test_block_mask_bit_exact(seed):
                bwd_order=dev_arr(m.bwd_order, B * nk, torch.int32))
     for key, val in got.items():
         assert np.array_equal(val.reshape(-1), np.asarray(ref[key]).reshape(-1)), key
+    # shard offsets: entry s of a row counts the oracle's listed tiles below s*nk/N
+    shard = dev_arr(m.fwd_shard, B * nq * (n_shards + 1), torch.int32).reshape(B * nq, -1)
+    idx = np.asarray(ref["fwd_idx"]).reshape(B * nq, nk)
+    tk = nk // n_shards
+    for r in range(B * nq):
+        listed = idx[r][idx[r] >= 0]
+        want = [int(np.sum(listed < s_ * tk)) for s_ in range(n_shards + 1)]
+        assert shard[r].tolist() == want, r
 
 
 def test_block_mask_sequential_positions_bit_exact():
