@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float cap = p.soft_cap;
         const float cap2 = cap * kLog2e;
         const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
+        const float a_mul = cap > 0.f ? 1.f : scale2; // log2-unit logit = s * a_mul
         uint32_t g = 0, pv_seen = 0, nshard = 0;
         bool ok = true;
         // waits of the softmax warps are made warp-uniform, so that no warp
@@ -405,12 +406,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         tmem_ld32(lane_base + sb * 128 + c0, s);
                         tmem_ld32(lane_base + sb * 128 + c0 + 32, s + 32);
                         tmem_ld_wait();
+                        // with a soft cap the logits are formed here in log2 units;
+                        // without one s stays raw and the scale rides in the exponent
                         if (cap > 0.f) {
 #pragma unroll
                             for (int j = 0; j < 64; ++j) s[j] = cap2 * tanh_fast(s[j] * scale_over_cap);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 64; ++j) s[j] *= scale2;
                         }
                         if (partial) {
 #pragma unroll
@@ -419,11 +419,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         }
                         float mx[8];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) mx[k] = s[k];
-#pragma unroll
-                        for (int j = 8; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
-                        float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                        for (int k = 0; k < 8; ++k) {
+                            mx[k] = max3(s[k], s[k + 8], s[k + 16]);
+                            mx[k] = max3(mx[k], s[k + 24], s[k + 32]);
+                            mx[k] = max3(mx[k], s[k + 40], s[k + 48]);
+                            mx[k] = fmaxf(mx[k], s[k + 56]);
+                        }
+                        // a_mul > 0, so scaling commutes with the max
+                        float tmax = a_mul * max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]),
+                                                  fmaxf(mx[6], mx[7]));
                         float *xm = xmax + (g & 1) * 256;
                         xm[wg * 128 + row] = tmax;
                         if (!(ok = pair_sync())) break;
@@ -453,16 +457,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             tmem_st_wait();
                         }
                         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        // p = 2^(s * a_mul - m), two lanes per instruction
+                        const float2 am2 = make_float2(a_mul, a_mul);
+                        const float2 nm2 = make_float2(-m_use, -m_use);
+                        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                        make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                         uint32_t pk[32];
 #pragma unroll
                         for (int j = 0; j < 64; j += 2) {
-                            const float a = ex2_approx(s[j] - m_use);
-                            const float b2 = ex2_approx(s[j + 1] - m_use);
-                            ls[(j >> 1) & 7] += a + b2;
-                            pk[j >> 1] = pack_bf16x2(a, b2);
+                            const float2 x2 = ffma2(make_float2(s[j], s[j + 1]), am2, nm2);
+                            const float2 e2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
+                            ls[(j >> 1) & 3] = fadd2(ls[(j >> 1) & 3], e2);
+                            pk[j >> 1] = pack_bf16x2(e2.x, e2.y);
                         }
-                        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                        const float2 l01 = fadd2(ls[0], ls[1]), l23 = fadd2(ls[2], ls[3]);
+                        const float2 l03 = fadd2(l01, l23);
+                        l += l03.x + l03.y;
                         // P of this half: columns [64*wg, 64*wg + 32) of the S buffer,
                         // which this half has already read
                         tmem_st32(lane_base + sb * 128 + c0, pk);
