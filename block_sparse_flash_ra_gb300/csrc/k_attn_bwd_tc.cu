@@ -413,19 +413,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 pc[(j >> 1) + 1] = pack_bf16x2(cr[2], cr[3]);
                             }
                         } else {
+                            // masked logits -> -inf, so that 2^(...) = 0 below
+                            if (partial) {
+#pragma unroll
+                                for (int c = 0; c < 64; ++c)
+                                    if (!((vis[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
+                            }
+                            // P = 2^(s * scale * log2 e - lse * log2 e), two lanes per instruction
+                            const float2 sc2 = make_float2(scale2, scale2);
+                            const float2 nl2e = make_float2(-kLog2e, -kLog2e);
 #pragma unroll
                             for (int j = 0; j < 64; j += 4) {
                                 const float4 lv = l4[j >> 2];
-                                const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-                                float pr[4];
-#pragma unroll
-                                for (int z = 0; z < 4; ++z) {
-                                    const int c = j + z;
-                                    const float e = ex2_approx(fmaf(s[c], scale2, -la[z] * kLog2e));
-                                    pr[z] = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
-                                }
-                                pk[j >> 1] = pack_bf16x2(pr[0], pr[1]);
-                                pk[(j >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
+                                const float2 a0 = fmul2(make_float2(lv.x, lv.y), nl2e);
+                                const float2 a1 = fmul2(make_float2(lv.z, lv.w), nl2e);
+                                const float2 x0 = ffma2(make_float2(s[j], s[j + 1]), sc2, a0);
+                                const float2 x1 = ffma2(make_float2(s[j + 2], s[j + 3]), sc2, a1);
+                                pk[j >> 1] = pack_bf16x2(ex2_approx(x0.x), ex2_approx(x0.y));
+                                pk[(j >> 1) + 1] = pack_bf16x2(ex2_approx(x1.x), ex2_approx(x1.y));
                                 pc[j >> 1] = pk[j >> 1];
                                 pc[(j >> 1) + 1] = pk[(j >> 1) + 1];
                             }
@@ -449,13 +454,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 64; j += 4) {
                             const float4 dl = d4[j >> 2];
-                            const uint32_t w0 = pc[j >> 1];
-                            const uint32_t w1 = pc[(j >> 1) + 1];
-                            dk2[j >> 1] = pack_bf16x2(__uint_as_float(w0 << 16) * (dpv[j] - dl.x),
-                                                      __uint_as_float(w0 & 0xffff0000u) * (dpv[j + 1] - dl.y));
-                            dk2[(j >> 1) + 1] =
-                                pack_bf16x2(__uint_as_float(w1 << 16) * (dpv[j + 2] - dl.z),
-                                            __uint_as_float(w1 & 0xffff0000u) * (dpv[j + 3] - dl.w));
+                            const float2 r0 = fmul2(unpack_bf16x2(pc[j >> 1]),
+                                                    fsub2(make_float2(dpv[j], dpv[j + 1]), make_float2(dl.x, dl.y)));
+                            const float2 r1 = fmul2(unpack_bf16x2(pc[(j >> 1) + 1]),
+                                                    fsub2(make_float2(dpv[j + 2], dpv[j + 3]), make_float2(dl.z, dl.w)));
+                            dk2[j >> 1] = pack_bf16x2(r0.x, r0.y);
+                            dk2[(j >> 1) + 1] = pack_bf16x2(r1.x, r1.y);
                         }
                         tmem_st32(lane_base + C::kColDP + c0, dk2);
                     }
@@ -818,16 +822,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 pc[j >> 1] = pack_bf16x2(cv[0], cv[1]);
                             }
                         } else {
+                            // masked logits -> -inf, so that 2^(...) = 0 below
+                            if (partial) {
+#pragma unroll
+                                for (int c = 0; c < 64; ++c)
+                                    if (!((vis[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
+                            }
+                            const float2 sc2 = make_float2(scale2, scale2);
+                            const float2 nl2 = make_float2(-l2, -l2);
 #pragma unroll
                             for (int j = 0; j < 64; j += 2) {
-                                float cv[2];
-#pragma unroll
-                                for (int z = 0; z < 2; ++z) {
-                                    const int c = j + z;
-                                    const float e = ex2_approx(fmaf(s[c], scale2, -l2));
-                                    cv[z] = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
-                                }
-                                pc[j >> 1] = pack_bf16x2(cv[0], cv[1]);
+                                const float2 x2 = ffma2(make_float2(s[j], s[j + 1]), sc2, nl2);
+                                pc[j >> 1] = pack_bf16x2(ex2_approx(x2.x), ex2_approx(x2.y));
                             }
                         }
                     }
@@ -842,11 +848,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tmem_ld32(lane_base + C::kColDP + c0 + 32, dpv + 32);
                         tmem_ld_wait();
                         uint32_t pk[32];
+                        const float2 dl2 = make_float2(dl, dl);
 #pragma unroll
                         for (int j = 0; j < 64; j += 2) {
-                            const uint32_t w = pc[j >> 1];
-                            pk[j >> 1] = pack_bf16x2(__uint_as_float(w << 16) * (dpv[j] - dl),
-                                                     __uint_as_float(w & 0xffff0000u) * (dpv[j + 1] - dl));
+                            const float2 r = fmul2(unpack_bf16x2(pc[j >> 1]),
+                                                   fsub2(make_float2(dpv[j], dpv[j + 1]), dl2));
+                            pk[j >> 1] = pack_bf16x2(r.x, r.y);
                         }
                         tmem_st32(lane_base + C::kColDP + c0, pk);
                     }
