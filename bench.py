@@ -75,6 +75,28 @@ def _dist():
     return ws, rank, local
 
 
+# ---- multi-rank logic (weak scaling: every rank runs its own batch of the
+# workload, the data path has no collective; only the timing is reduced)
+def rank_workload(w, rank):
+    """The batch rank `rank` processes: same shapes, its own input seed."""
+    return w.scaled(seed=w.seed + rank, backward=True)
+
+
+def max_over_ranks(x, ws_):
+    """Max of a per-rank float over all ranks (the slowest rank's time)."""
+    if ws_ <= 1:
+        return float(x)
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank, ms_max, ws_):
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return flops_per_rank * ws_ / (ms_max * 1e-3) / 1e12
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
 
@@ -138,8 +160,7 @@ class Pipeline:
         import block_sparse_flash_ra_gb300 as ra
         self.ra = ra
         self.w = w
-        ws = w.scaled(seed=w.seed + seed_offset, backward=True)
-        inp = make_inputs(ws, with_dout=True)
+        inp = make_inputs(rank_workload(w, seed_offset), with_dout=True)
         self.host = inp
         self.dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
         N, B, L = w.n_shards, w.B, w.L
@@ -214,11 +235,11 @@ class Pipeline:
         ra.ra_attn_bwd_prep(self.params, self.out, self.lse, p["dout"], self.dsinks, self.ws)
         mark("bwd_prep", 1)
         mark("bwd_dkdv", 0)
-        ra.ra_attn_bwd_dkdv(self.params, p["q"], p["k"], p["v"], self.lse, p["dout"], self.mask,
+        ra.ra_attn_bwd_dkdv(self.params, p["q"], p["k"], p["v"], p["dout"], self.mask,
                             self.dk, self.dv, self.ws)
         mark("bwd_dkdv", 1)
         mark("bwd_dq", 0)
-        ra.ra_attn_bwd_dq(self.params, p["q"], p["k"], p["v"], self.lse, p["dout"], self.mask,
+        ra.ra_attn_bwd_dq(self.params, p["q"], p["k"], p["v"], p["dout"], self.mask,
                           self.dq, self.ws)
         mark("bwd_dq", 1)
         mark("unpermute_bwd", 0)
@@ -263,11 +284,7 @@ def run_ours(args, w, ws_, rank, local):
     per = {n: sum(ev[n][i][0].elapsed_time(ev[n][i][1]) for i in range(K)) / K for n in pipe.names}
     if ra.ra_get_device_status() != ra.RA_OK:
         raise RuntimeError("device status after timing: " + ra.ra_last_error())
-    ms_step = ms_total / K
-    if ws_ > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_total / K, ws_)
 
     # end to end through the C ABI with host buffers: H2D inputs, step, D2H results
     e2e = None
@@ -288,7 +305,7 @@ def run_ours(args, w, ws_, rank, local):
     peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
     tr = TRAFFIC.get((w.name, dom))
     traffic = tr[0] if tr and tr[1] == _src_hash(d_src) else None
-    value = tf(pipe.f_fwd_bwd, ms_step) * ws_
+    value = job_tflops(pipe.f_fwd_bwd, ms_step, ws_)
     fwd_tf = tf(pipe.f_fwd, per["fwd"])
     fb_tf = tf(pipe.f_fwd_bwd, per["fwd"] + bwd_ms)
     line = {
@@ -353,12 +370,8 @@ def run_e2e(pipe, K, ws_):
         one()
     e.record()
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / K
-    if ws_ > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    v = pipe.f_fwd_bwd / (ms * 1e-3) / 1e12 * ws_
+    ms = max_over_ranks(s.elapsed_time(e) / K, ws_)
+    v = job_tflops(pipe.f_fwd_bwd, ms, ws_)
     return {"value": round(v, 2), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K}
 

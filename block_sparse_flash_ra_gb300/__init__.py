@@ -27,7 +27,7 @@ __all__ = [
     "ra_attn_bwd_workspace_size", "ra_attn_bwd", "ra_attn_bwd_prep", "ra_attn_bwd_dkdv",
     "ra_attn_bwd_dq", "ra_attn_bwd_noalloc", "ra_attn_bwd_noalloc_max_workspace",
     "ra_permute_tokens", "ra_unpermute_tokens",
-    "ra_get_device_status", "ra_launch_count", "make_params", "build_mask", "forward", "backward", "permute",
+    "ra_get_device_status", "ra_launch_count", "ra_selftest_wait_timeout", "make_params", "build_mask", "forward", "backward", "permute",
     "unpermute",
 ]
 
@@ -107,13 +107,14 @@ def lib():
             L.ra_attn_bwd_workspace_size.restype = sz
             L.ra_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, M, vp, vp, vp, vp, vp, sz, vp]
             L.ra_attn_bwd_prep.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
-            L.ra_attn_bwd_dkdv.argtypes = [P, vp, vp, vp, vp, vp, M, vp, vp, vp, sz, vp]
-            L.ra_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, vp, M, vp, vp, sz, vp]
+            L.ra_attn_bwd_dkdv.argtypes = [P, vp, vp, vp, vp, M, vp, vp, vp, sz, vp]
+            L.ra_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, M, vp, vp, sz, vp]
             L.ra_permute_tokens.argtypes = [vp, vp, ci, ci, sz, ci, vp]
             L.ra_unpermute_tokens.argtypes = [vp, vp, ci, ci, sz, ci, vp]
             L.ra_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, M, vp, vp, vp, vp, vp]
             L.ra_attn_bwd_noalloc_max_workspace.restype = sz
             L.ra_get_device_status.argtypes = [vp]
+            L.ra_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
             L.ra_launch_count.restype = ctypes.c_uint64
             _lib = L
     return _lib
@@ -215,16 +216,15 @@ def ra_attn_bwd_prep(params, out, lse, dout, dsinks, ws, stream=None):
                                   _ptr(dsinks), _ptr(ws), _wsb(ws), _stream(stream)))
 
 
-def ra_attn_bwd_dkdv(params, q, k, v, lse, dout, mask, dk, dv, ws, stream=None):
-    _check(lib().ra_attn_bwd_dkdv(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(lse),
-                                  _ptr(dout), ctypes.byref(mask), _ptr(dk), _ptr(dv), _ptr(ws),
-                                  _wsb(ws), _stream(stream)))
+def ra_attn_bwd_dkdv(params, q, k, v, dout, mask, dk, dv, ws, stream=None):
+    _check(lib().ra_attn_bwd_dkdv(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                  ctypes.byref(mask), _ptr(dk), _ptr(dv), _ptr(ws), _wsb(ws),
+                                  _stream(stream)))
 
 
-def ra_attn_bwd_dq(params, q, k, v, lse, dout, mask, dq, ws, stream=None):
-    _check(lib().ra_attn_bwd_dq(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(lse),
-                                _ptr(dout), ctypes.byref(mask), _ptr(dq), _ptr(ws), _wsb(ws),
-                                _stream(stream)))
+def ra_attn_bwd_dq(params, q, k, v, dout, mask, dq, ws, stream=None):
+    _check(lib().ra_attn_bwd_dq(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                ctypes.byref(mask), _ptr(dq), _ptr(ws), _wsb(ws), _stream(stream)))
 
 
 def ra_permute_tokens(inp, out, B, L, row_bytes, n_shards, stream=None) -> None:
@@ -243,6 +243,12 @@ def ra_launch_count() -> int:
 
 def ra_get_device_status(stream=None) -> int:
     return int(lib().ra_get_device_status(_stream(stream)))
+
+
+def ra_selftest_wait_timeout(timeout_ns, gave_up, stream=None) -> None:
+    """One in-kernel wait that can never complete gives up after timeout_ns;
+    ``gave_up`` is a device int32 tensor of one element."""
+    _check(lib().ra_selftest_wait_timeout(int(timeout_ns), _ptr(gave_up), _stream(stream)))
 
 
 # ------------------------------------------------------------- helpers

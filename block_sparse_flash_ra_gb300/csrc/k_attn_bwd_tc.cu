@@ -4,7 +4,9 @@
 // out and lse, dq accumulates locally, dk/dv accumulate with their chunk,
 // everything in fp32 and cast back at the end).  Summing over every
 // non-empty tile of every chunk gives, with P = exp(s - lse) on visible
-// pairs and Delta = <dO, O> (from the preprocessing kernel):
+// pairs and Delta = <dO, O> (from the preprocessing kernel, which also
+// stores -lse * log2 e so that P = 2^(s * scale * log2 e - lse * log2 e) is
+// one fused multiply-add per logit):
 //   dV_j = sum_i P_ij dO_i                      dP_ij = <dO_i, V_j>
 //   dS_ij = P_ij (dP_ij - Delta_i) (1 - tanh^2)  (tanh term only with a cap)
 //   dK_j = scale sum_i dS_ij Q_i                dQ_i = scale sum_j dS_ij K_j
@@ -101,7 +103,7 @@ __device__ __forceinline__ void row_visibility(const Problem &p, int b, int k0, 
 template <int D>
 struct DkdvCfg {
     static constexpr int kTileBytes = kTile * D * 2;
-    static constexpr int kStageBytes = 2 * kTileBytes + 1024; // Q, dO, lse[128], delta[128]
+    static constexpr int kStageBytes = 2 * kTileBytes + 1024; // Q, dO, nlse2[128], delta[128]
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kTileBytes;
     static constexpr int kStageOff = 2 * kTileBytes;
@@ -162,7 +164,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    Problem p, const float *__restrict__ lse, const float *__restrict__ delta,
+                    Problem p, const float *__restrict__ nlse2, const float *__restrict__ delta,
                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv)
 {
     using C = DkdvCfg<D>;
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                         hb * 64, h, qt * kTile, x.b);
                         }
                         const size_t li = ((size_t)x.b * p.Hq + h) * p.Lq + (size_t)qt * kTile;
-                        bulk_load(sb + 2 * C::kTileBytes, lse + li, 512, bars.st_full + st);
+                        bulk_load(sb + 2 * C::kTileBytes, nlse2 + li, 512, bars.st_full + st);
                         bulk_load(sb + 2 * C::kTileBytes + 512, delta + li, 512, bars.st_full + st);
                         ++st_issued[st];
                         ++n;
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 for (int z = 0; z < 4; ++z) {
                                     const int c = j + z;
                                     const float t = tanh_fast(s[c] * scale_over_cap);
-                                    float e = ex2_approx(fmaf(cap2, t, -la[z] * kLog2e));
+                                    float e = ex2_approx(fmaf(cap2, t, la[z]));
                                     e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
                                     pr[z] = e;
                                     cr[z] = e * (1.f - t * t);
@@ -419,16 +421,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 for (int c = 0; c < 64; ++c)
                                     if (!((vis[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
                             }
-                            // P = 2^(s * scale * log2 e - lse * log2 e), two lanes per instruction
+                            // P = 2^(s * scale * log2 e + nlse2), two lanes per instruction
                             const float2 sc2 = make_float2(scale2, scale2);
-                            const float2 nl2e = make_float2(-kLog2e, -kLog2e);
 #pragma unroll
                             for (int j = 0; j < 64; j += 4) {
                                 const float4 lv = l4[j >> 2];
-                                const float2 a0 = fmul2(make_float2(lv.x, lv.y), nl2e);
-                                const float2 a1 = fmul2(make_float2(lv.z, lv.w), nl2e);
-                                const float2 x0 = ffma2(make_float2(s[j], s[j + 1]), sc2, a0);
-                                const float2 x1 = ffma2(make_float2(s[j + 2], s[j + 3]), sc2, a1);
+                                const float2 x0 = ffma2(make_float2(s[j], s[j + 1]), sc2, make_float2(lv.x, lv.y));
+                                const float2 x1 = ffma2(make_float2(s[j + 2], s[j + 3]), sc2, make_float2(lv.z, lv.w));
                                 pk[j >> 1] = pack_bf16x2(ex2_approx(x0.x), ex2_approx(x0.y));
                                 pk[(j >> 1) + 1] = pack_bf16x2(ex2_approx(x1.x), ex2_approx(x1.y));
                                 pc[j >> 1] = pk[j >> 1];
@@ -580,7 +579,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  Problem p, const float *__restrict__ lse, const float *__restrict__ delta,
+                  Problem p, const float *__restrict__ nlse2, const float *__restrict__ delta,
                   __nv_bfloat16 *__restrict__ dq)
 {
     using C = DqCfg<D>;
@@ -785,9 +784,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __nv_bfloat16 *qrow = dq + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D + o_col;
             if (x.cnt > 0) {
                 const size_t li = ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
-                // a row with lse = -inf has no visible pair: it only meets partial
-                // tiles, where the mask zeroes every P, so no guard is needed
-                const float l2 = lse[li] * kLog2e;
+                // exponent offset -lse * log2 e (0 for a row with nothing visible:
+                // it only meets partial tiles, where the mask zeroes every P)
+                const float nl2 = nlse2[li];
                 const float dl = delta[li];
                 const int my_pos = p.q_pos ? p.q_pos[(size_t)x.b * p.Lq + qi] : qi;
                 const int my_seg = p.q_seg ? p.q_seg[(size_t)x.b * p.Lq + qi] : 0;
@@ -815,7 +814,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 for (int z = 0; z < 2; ++z) {
                                     const int c = j + z;
                                     const float t = tanh_fast(s[c] * scale_over_cap);
-                                    float e = ex2_approx(fmaf(cap2, t, -l2));
+                                    float e = ex2_approx(fmaf(cap2, t, nl2));
                                     e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
                                     cv[z] = e * (1.f - t * t);
                                 }
@@ -829,10 +828,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                     if (!((vis[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
                             }
                             const float2 sc2 = make_float2(scale2, scale2);
-                            const float2 nl2 = make_float2(-l2, -l2);
+                            const float2 nl22 = make_float2(nl2, nl2);
 #pragma unroll
                             for (int j = 0; j < 64; j += 2) {
-                                const float2 x2 = ffma2(make_float2(s[j], s[j + 1]), sc2, nl2);
+                                const float2 x2 = ffma2(make_float2(s[j], s[j + 1]), sc2, nl22);
                                 pc[j >> 1] = pack_bf16x2(ex2_approx(x2.x), ex2_approx(x2.y));
                             }
                         }
@@ -920,7 +919,7 @@ cudaError_t bwd_tc_set_attributes(int D)
 }
 
 cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *tm_k,
-                               const void *tm_v, const void *tm_do, const float *lse,
+                               const void *tm_v, const void *tm_do, const float *nlse2,
                                const float *delta, void *dk, void *dv, int num_sms,
                                cudaStream_t s)
 {
@@ -932,14 +931,14 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *t
     const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
     __nv_bfloat16 *gk = static_cast<__nv_bfloat16 *>(dk), *gv = static_cast<__nv_bfloat16 *>(dv);
     if (p.D == 64)
-        bwd_dkdv_kernel<64><<<grid, kBwdThreads, DkdvCfg<64>::kSmem, s>>>(q, k, v, d, p, lse, delta, gk, gv);
+        bwd_dkdv_kernel<64><<<grid, kBwdThreads, DkdvCfg<64>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gk, gv);
     else
-        bwd_dkdv_kernel<128><<<grid, kBwdThreads, DkdvCfg<128>::kSmem, s>>>(q, k, v, d, p, lse, delta, gk, gv);
+        bwd_dkdv_kernel<128><<<grid, kBwdThreads, DkdvCfg<128>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gk, gv);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
-                             const void *tm_v, const void *tm_do, const float *lse,
+                             const void *tm_v, const void *tm_do, const float *nlse2,
                              const float *delta, void *dq, int num_sms, cudaStream_t s)
 {
     const int U = p.B * p.nq * p.Hq;
@@ -950,9 +949,9 @@ cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_
     const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
     __nv_bfloat16 *gq = static_cast<__nv_bfloat16 *>(dq);
     if (p.D == 64)
-        bwd_dq_kernel<64><<<grid, kBwdThreads, DqCfg<64>::kSmem, s>>>(q, k, v, d, p, lse, delta, gq);
+        bwd_dq_kernel<64><<<grid, kBwdThreads, DqCfg<64>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gq);
     else
-        bwd_dq_kernel<128><<<grid, kBwdThreads, DqCfg<128>::kSmem, s>>>(q, k, v, d, p, lse, delta, gq);
+        bwd_dq_kernel<128><<<grid, kBwdThreads, DqCfg<128>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gq);
     return cudaGetLastError();
 }
 

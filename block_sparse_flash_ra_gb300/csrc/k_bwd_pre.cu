@@ -3,6 +3,10 @@
 // accumulated and summed over the ring):
 //   Delta[b, h, i] = <dO[b, i, h, :], O[b, i, h, :]>           (fp32)
 //   dsinks[h]      = - sum_{b, i} exp(sink_h - lse[b, h, i]) * Delta[b, h, i]
+// and, for the gradient kernels, nlse2[b, h, i] = -lse * log2(e): the
+// exponent offset of P = 2^(s * scale * log2 e + nlse2).  A row with nothing
+// visible (lse = -inf) gets 0 instead of +inf; all its entries are masked, so
+// its P stays 0 and no inf - inf can arise.
 // The dsinks sum is taken in two deterministic passes: per-(b, q-tile)
 // partials, then one block per head.  HBM-bound: reads O and dO once.
 #include <cuda_bf16.h>
@@ -31,6 +35,7 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(Problem p, const T *__rest
                                                       const T *__restrict__ dout,
                                                       const float *__restrict__ lse,
                                                       float *__restrict__ delta,
+                                                      float *__restrict__ nlse2,
                                                       float *__restrict__ dsink_part)
 {
     const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -46,10 +51,9 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(Problem p, const T *__rest
         const size_t li = ((size_t)b * p.Hq + h) * p.Lq + i;
         if (lane == 0) {
             delta[li] = acc;
-            if (p.sinks) {
-                const float l = lse[li];
-                if (l != -INFINITY) ds += __expf(sink - l) * acc;
-            }
+            const float l = lse[li];
+            nlse2[li] = (l == -INFINITY) ? 0.f : -l * 1.4426950408889634f;
+            if (p.sinks && l != -INFINITY) ds += __expf(sink - l) * acc;
         }
     }
     if (p.sinks) {
@@ -80,18 +84,18 @@ __global__ void __launch_bounds__(256) dsink_reduce_kernel(const float *part, in
 } // namespace
 
 cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, int dtype,
-                           const float *lse, float *delta, float *dsink_part, float *dsinks,
-                           cudaStream_t s)
+                           const float *lse, float *delta, float *nlse2, float *dsink_part,
+                           float *dsinks, cudaStream_t s)
 {
     const dim3 grid(p.nq, p.Hq, p.B);
     if (dtype == RA_BF16)
         bwd_pre_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
             p, static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout),
-            lse, delta, dsink_part);
+            lse, delta, nlse2, dsink_part);
     else
         bwd_pre_kernel<float><<<grid, 128, 0, s>>>(p, static_cast<const float *>(out),
                                                    static_cast<const float *>(dout), lse, delta,
-                                                   dsink_part);
+                                                   nlse2, dsink_part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !p.sinks) return e;
     dsink_reduce_kernel<<<p.Hq, 256, 0, s>>>(dsink_part, p.B * p.nq, dsinks);

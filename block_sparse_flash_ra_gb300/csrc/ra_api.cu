@@ -380,7 +380,7 @@ RA_API size_t ra_attn_bwd_workspace_size(const ra_attn_params *p)
     if (check_params(p) != RA_OK) return 0;
     const size_t rows = (size_t)p->B * p->Hq * p->Lq;
     const size_t part = (size_t)p->Hq * p->B * (p->Lq / RA_TILE);
-    return up256(rows * 4) + up256(part * 4);
+    return 2 * up256(rows * 4) + up256(part * 4);
 }
 
 } // extern "C"
@@ -390,11 +390,15 @@ namespace {
 
 enum BwdStage { kPrep = 1, kDkdv = 2, kDq = 4 };
 
+// Backward workspace: Delta rows, the rows' -lse * log2 e, dsinks partials.
+struct BwdWs {
+    float *delta, *nlse2, *part;
+};
+
 // Shared checks of the backward entry points; on success fills the device
-// cache and the workspace split (Delta rows, then dsinks partials).
+// cache and the workspace split.
 int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
-               const ra_block_mask *mask, void *ws, size_t ws_bytes, DevCache **dc,
-               float **delta, float **part)
+               const ra_block_mask *mask, void *ws, size_t ws_bytes, DevCache **dc, BwdWs *w)
 {
     int rc = check_params(p);
     if (rc) return rc;
@@ -412,16 +416,17 @@ int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
     if (reinterpret_cast<uintptr_t>(ws) & 255u)
         return fail(RA_ERR_WORKSPACE, "backward workspace must be 256-byte aligned");
     if ((rc = device_cache(dc))) return rc;
-    *delta = static_cast<float *>(ws);
-    *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
-                                      up256((size_t)p->B * p->Hq * p->Lq * 4));
+    const size_t rows_bytes = up256((size_t)p->B * p->Hq * p->Lq * 4);
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    w->delta = reinterpret_cast<float *>(b);
+    w->nlse2 = reinterpret_cast<float *>(b + rows_bytes);
+    w->part = reinterpret_cast<float *>(b + 2 * rows_bytes);
     return RA_OK;
 }
 
 int bwd_tc_kernels(const ra_attn_params *p, DevCache *dc, const Problem &pr, int stages,
-                   const void *q, const void *k, const void *v, const float *lse,
-                   const void *dout, const float *delta, void *dq, void *dk, void *dv,
-                   cudaStream_t s)
+                   const void *q, const void *k, const void *v, const void *dout,
+                   const BwdWs &w, void *dq, void *dk, void *dv, cudaStream_t s)
 {
     cudaError_t e;
     bool &done = p->D == 64 ? dc->attr_bwd64 : dc->attr_bwd128;
@@ -436,12 +441,12 @@ int bwd_tc_kernels(const ra_attn_params *p, DevCache *dc, const Problem &pr, int
     if ((rc = encode_rows(&tv, v, p->B, p->Lkv, p->Hkv, p->D))) return rc;
     if ((rc = encode_rows(&tdo, dout, p->B, p->Lq, p->Hq, p->D))) return rc;
     if (stages & kDkdv) {
-        e = launch_bwd_dkdv_tc(pr, &tq, &tk, &tv, &tdo, lse, delta, dk, dv, dc->num_sms, s);
+        e = launch_bwd_dkdv_tc(pr, &tq, &tk, &tv, &tdo, w.nlse2, w.delta, dk, dv, dc->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
         count(1);
     }
     if (stages & kDq) {
-        e = launch_bwd_dq_tc(pr, &tq, &tk, &tv, &tdo, lse, delta, dq, dc->num_sms, s);
+        e = launch_bwd_dq_tc(pr, &tq, &tk, &tv, &tdo, w.nlse2, w.delta, dq, dc->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
         count(1);
     }
@@ -459,12 +464,12 @@ RA_API int ra_attn_bwd_prep(const ra_attn_params *p, const void *out, const floa
 {
     const void *ptrs[3] = {out, lse, dout};
     DevCache *dc = nullptr;
-    float *delta = nullptr, *part = nullptr;
-    int rc = bwd_common(p, ptrs, 3, nullptr, ws, ws_bytes, &dc, &delta, &part);
+    BwdWs w{};
+    int rc = bwd_common(p, ptrs, 3, nullptr, ws, ws_bytes, &dc, &w);
     if (rc) return rc;
     if (p->sinks && !dsinks) return fail(RA_ERR_INVALID_ARG, "dsinks is NULL but sinks are given");
     const Problem pr = make_problem(p, nullptr, dc->status);
-    cudaError_t e = launch_bwd_pre(pr, out, dout, p->dtype, lse, delta, part, dsinks,
+    cudaError_t e = launch_bwd_pre(pr, out, dout, p->dtype, lse, w.delta, w.nlse2, w.part, dsinks,
                                    reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward preprocessing launch");
     count(p->sinks ? 2 : 1);
@@ -472,32 +477,32 @@ RA_API int ra_attn_bwd_prep(const ra_attn_params *p, const void *out, const floa
 }
 
 RA_API int ra_attn_bwd_dkdv(const ra_attn_params *p, const void *q, const void *k, const void *v,
-                            const float *lse, const void *dout, const ra_block_mask *mask,
-                            void *dk, void *dv, void *ws, size_t ws_bytes, ra_stream_t stream)
+                            const void *dout, const ra_block_mask *mask, void *dk, void *dv,
+                            void *ws, size_t ws_bytes, ra_stream_t stream)
 {
     if (!mask) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
-    const void *ptrs[7] = {q, k, v, lse, dout, dk, dv};
+    const void *ptrs[6] = {q, k, v, dout, dk, dv};
     DevCache *dc = nullptr;
-    float *delta = nullptr, *part = nullptr;
-    int rc = bwd_common(p, ptrs, 7, mask, ws, ws_bytes, &dc, &delta, &part);
+    BwdWs w{};
+    int rc = bwd_common(p, ptrs, 6, mask, ws, ws_bytes, &dc, &w);
     if (rc) return rc;
     const Problem pr = make_problem(p, mask, dc->status);
-    return bwd_tc_kernels(p, dc, pr, kDkdv, q, k, v, lse, dout, delta, nullptr, dk, dv,
+    return bwd_tc_kernels(p, dc, pr, kDkdv, q, k, v, dout, w, nullptr, dk, dv,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k, const void *v,
-                          const float *lse, const void *dout, const ra_block_mask *mask,
-                          void *dq, void *ws, size_t ws_bytes, ra_stream_t stream)
+                          const void *dout, const ra_block_mask *mask, void *dq, void *ws,
+                          size_t ws_bytes, ra_stream_t stream)
 {
     if (!mask) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
-    const void *ptrs[6] = {q, k, v, lse, dout, dq};
+    const void *ptrs[5] = {q, k, v, dout, dq};
     DevCache *dc = nullptr;
-    float *delta = nullptr, *part = nullptr;
-    int rc = bwd_common(p, ptrs, 6, mask, ws, ws_bytes, &dc, &delta, &part);
+    BwdWs w{};
+    int rc = bwd_common(p, ptrs, 5, mask, ws, ws_bytes, &dc, &w);
     if (rc) return rc;
     const Problem pr = make_problem(p, mask, dc->status);
-    return bwd_tc_kernels(p, dc, pr, kDq, q, k, v, lse, dout, delta, dq, nullptr, nullptr,
+    return bwd_tc_kernels(p, dc, pr, kDq, q, k, v, dout, w, dq, nullptr, nullptr,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -510,15 +515,15 @@ RA_API int ra_attn_bwd(const ra_attn_params *p, const void *q, const void *k, co
     if (p && p->sinks && !dsinks) return fail(RA_ERR_INVALID_ARG, "dsinks is NULL but sinks are given");
     const void *ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
     DevCache *dc = nullptr;
-    float *delta = nullptr, *part = nullptr;
-    int rc = bwd_common(p, ptrs, 9, mask, ws, ws_bytes, &dc, &delta, &part);
+    BwdWs w{};
+    int rc = bwd_common(p, ptrs, 9, mask, ws, ws_bytes, &dc, &w);
     if (rc) return rc;
     const Problem pr = make_problem(p, mask, dc->status);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_bwd_pre(pr, out, dout, p->dtype, lse, delta, part, dsinks, s);
+    cudaError_t e = launch_bwd_pre(pr, out, dout, p->dtype, lse, w.delta, w.nlse2, w.part, dsinks, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward preprocessing launch");
     count(p->sinks ? 2 : 1);
-    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, lse, dout, delta, dq, dk, dv, s);
+    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, dout, w, dq, dk, dv, s);
 }
 
 RA_API int ra_permute_tokens(const void *in, void *out, int B, int L, size_t row_bytes,
@@ -551,6 +556,19 @@ RA_API int ra_unpermute_tokens(const void *in, void *out, int B, int L, size_t r
     cudaError_t e = launch_permute(in, out, B, L, row_bytes, n_shards, 1,
                                    reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "unpermute launch");
+    count(1);
+    return RA_OK;
+}
+
+RA_API int ra_selftest_wait_timeout(uint64_t timeout_ns, int *gave_up, ra_stream_t stream)
+{
+    if (!gave_up) return fail(RA_ERR_INVALID_ARG, "gave_up is NULL");
+    DevCache *dc = nullptr;
+    int rc = device_cache(&dc);
+    if (rc) return rc;
+    const uint64_t ns = timeout_ns ? timeout_ns : g_timeout_ns.load();
+    cudaError_t e = launch_wait_selftest(dc->status, ns, gave_up, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
     count(1);
     return RA_OK;
 }

@@ -48,18 +48,20 @@ cudaError_t launch_fwd_simt_f32(const Problem &p, const float *q, const float *k
 cudaError_t launch_fwd_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,
                           void *out, float *lse, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, int dtype,
-                           const float *lse, float *delta, float *dsink_part, float *dsinks,
-                           cudaStream_t s);
+                           const float *lse, float *delta, float *nlse2, float *dsink_part,
+                           float *dsinks, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *tm_k,
-                               const void *tm_v, const void *tm_do, const float *lse,
+                               const void *tm_v, const void *tm_do, const float *nlse2,
                                const float *delta, void *dk, void *dv, int num_sms,
                                cudaStream_t s);
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
-                             const void *tm_v, const void *tm_do, const float *lse,
+                             const void *tm_v, const void *tm_do, const float *nlse2,
                              const float *delta, void *dq, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,
                                 const float *dout, const float *lse, const float *delta,
                                 float *dq, float *dk, float *dv, cudaStream_t s);
+
+cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, int *gave_up, cudaStream_t s);
 
 // dynamic shared memory the tensor-core kernels request (for attribute setup)
 int fwd_tc_smem_bytes(int D);

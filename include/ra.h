@@ -211,8 +211,8 @@ RA_API int ra_merge_out_lse(float *out, float *lse, const float *block_out,
                             const float *block_lse, int B, int L, int H, int D,
                             ra_stream_t stream);
 
-/* Workspace bytes of ra_attn_bwd: per-row Delta = <dO, O> (fp32, B*Hq*Lq)
- * and per-tile partial sums of dsinks. */
+/* Workspace bytes of ra_attn_bwd: per-row Delta = <dO, O> and per-row
+ * -lse * log2(e) (fp32, B*Hq*Lq each) and per-tile partial sums of dsinks. */
 RA_API size_t ra_attn_bwd_workspace_size(const ra_attn_params *p);
 
 /*
@@ -236,19 +236,21 @@ RA_API int ra_attn_bwd(const ra_attn_params *p, const void *q, const void *k, co
  * one by one.  Arguments mean what they mean for ra_attn_bwd and obey the
  * same rules; the stages communicate through `ws`, so for one problem they
  * must run in this order on one stream (or be ordered by the caller):
- *   ra_attn_bwd_prep  Delta = rowsum(dO * O) into ws and dsinks (if sinks);
+ *   ra_attn_bwd_prep  Delta = rowsum(dO * O) and -lse * log2(e) into ws,
+ *                     and dsinks (if sinks);
  *   ra_attn_bwd_dkdv  dk, dv (one work unit per kv head and 128-row kv tile);
  *   ra_attn_bwd_dq    dq     (one work unit per query head and query tile).
+ * dkdv and dq read lse and Delta only through ws.
  */
 RA_API int ra_attn_bwd_prep(const ra_attn_params *p, const void *out, const float *lse,
                             const void *dout, float *dsinks, void *ws, size_t ws_bytes,
                             ra_stream_t stream);
 RA_API int ra_attn_bwd_dkdv(const ra_attn_params *p, const void *q, const void *k, const void *v,
-                            const float *lse, const void *dout, const ra_block_mask *mask,
-                            void *dk, void *dv, void *ws, size_t ws_bytes, ra_stream_t stream);
+                            const void *dout, const ra_block_mask *mask, void *dk, void *dv,
+                            void *ws, size_t ws_bytes, ra_stream_t stream);
 RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k, const void *v,
-                          const float *lse, const void *dout, const ra_block_mask *mask,
-                          void *dq, void *ws, size_t ws_bytes, ra_stream_t stream);
+                          const void *dout, const ra_block_mask *mask, void *dq, void *ws,
+                          size_t ws_bytes, ra_stream_t stream);
 
 /*
  * ra_attn_bwd without a workspace argument, for callers that cannot allocate
@@ -261,7 +263,7 @@ RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k,
  *   bytes (8 MiB) in the library's device memory, held by every GPU that loads
  *   the library until the process exits.  Problems whose
  *   ra_attn_bwd_workspace_size() exceeds it fail with RA_ERR_WORKSPACE
- *   (roughly B * Hq * Lq above two million query rows); use ra_attn_bwd then.
+ *   (roughly B * Hq * Lq above one million query rows); use ra_attn_bwd then.
  *   Nothing is allocated: no cudaMalloc / cudaFree is ever called.
  *   The first call on a device looks up the array's device address on that
  *   device (a synchronous runtime query); make that first call before any
@@ -307,6 +309,18 @@ RA_API uint64_t ra_launch_count(void);
 /* Upper bound, in nanoseconds, of any single in-kernel wait (default 2e9).
  * Applies to launches made after the call, from any thread. */
 RA_API void ra_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Failure-detection self-test: launches one block whose single in-kernel
+ * wait can never complete (an mbarrier nothing arrives at).  The wait gives
+ * up after timeout_ns (0 = the current ra_set_wait_timeout_ns limit), exactly
+ * as the waits of the attention kernels do, and records the timeout in the
+ * device status word; the kernel then returns and the context stays usable.
+ *   gave_up: device int, set to 1 when the wait gave up (0 otherwise).
+ * Read the outcome with ra_get_device_status (RA_ERR_TIMEOUT expected).
+ * Errors: RA_ERR_INVALID_ARG (gave_up NULL), RA_ERR_CUDA.
+ */
+RA_API int ra_selftest_wait_timeout(uint64_t timeout_ns, int *gave_up, ra_stream_t stream);
 
 #ifdef __cplusplus
 }

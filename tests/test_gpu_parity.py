@@ -307,3 +307,22 @@ def test_backward_packed_docs_with_padding():
     grads = ra.backward(c.params, d["q"], d["k"], d["v"], out, lse, d["dout"], m)
     torch.cuda.synchronize()
     _check_bwd(c, grads)
+
+
+def test_backward_padding_rows_inside_a_tile_without_sinks():
+    # rows 700..767 are padding: nothing visible, lse = -inf, and they share
+    # the last 128-row tile with document rows, so that tile is partial for
+    # them (no sink keeps their lse finite here)
+    B, L = 1, 768
+    seg = torch.zeros((B, L), dtype=torch.int32)
+    seg[:, 700:] = -1
+    pos = torch.arange(L, dtype=torch.int32).unsqueeze(0).clone()
+    c = Case(W(B=B, L=L, Hq=2, Hkv=1, seed=36, n_shards=3), dout=True,
+             overrides=dict(q_seg=seg, kv_seg=seg.clone(), q_pos=pos, kv_pos=pos.clone()))
+    out, lse, m = c.gpu_fwd()
+    d = c.dev
+    grads = ra.backward(c.params, d["q"], d["k"], d["v"], out, lse, d["dout"], m)
+    torch.cuda.synchronize()
+    for g in grads[:3]:
+        assert torch.isfinite(g).all()
+    _check_bwd(c, grads)
