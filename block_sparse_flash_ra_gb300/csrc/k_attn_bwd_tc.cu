@@ -21,8 +21,9 @@
 //         dV += P^T dO and dK += dS^T Q products straight from TMEM.
 //   dq:   one work unit per (b, q head, 128-row query tile); it walks the
 //         non-empty kv tiles of its block-map row.  Thread t owns query row
-//         t.  TMEM: S [0,128), dP [128,256), dQ [256,256+D); dS (bf16)
-//         overwrites dP and feeds dQ += dS K from TMEM.
+//         t.  TMEM: S [0,128), dP of even tiles [128,256), dQ [256,256+D),
+//         dP of odd tiles [384,512); dS (bf16) overwrites its dP and feeds
+//         dQ += dS K from TMEM.
 // The dkdv kernel recomputes S and dP per tile and the dq kernel recomputes
 // them again: 7 tile products instead of 5, in exchange for no fp32 atomics.
 #include <math.h>
@@ -521,15 +522,19 @@ struct DqCfg {
     static constexpr int kQOff = 0;
     static constexpr int kDoOff = kTileBytes;
     static constexpr int kKOff = 2 * kTileBytes;
-    static constexpr int kStages = 2;
-    static constexpr int kVOff = kKOff + kStages * kTileBytes;
-    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 2 + 4 * kStages + 6;
+    // a K tile is held from S(g) to dQ(g), a V tile only until dP(g)
+    static constexpr int kKStages = 3;
+    static constexpr int kVStages = 2;
+    static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+    static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 8;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmem = (kMiscOff + 16 + 1024) > 122880 ? (kMiscOff + 16 + 1024) : 122880;
     static_assert(kSmem <= 232448, "dQ shared memory exceeds the 227 KB per-block limit");
-    static constexpr uint32_t kColDP = 128, kColDQ = 256;
+    // dP / dS double buffer: tile g uses kColDP[g & 1]
+    static constexpr uint32_t kColDP0 = 128, kColDP1 = 384, kColDQ = 256;
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);
+    static __device__ __forceinline__ uint32_t dp_col(uint32_t g) { return (g & 1) ? kColDP1 : kColDP0; }
 };
 
 struct DqBars {
@@ -546,14 +551,14 @@ __device__ __forceinline__ DqBars dq_bars(uint8_t *smem)
     r.q_full = b;
     r.q_empty = b + 1;
     r.k_full = b + 2;
-    r.k_empty = r.k_full + C::kStages;
-    r.v_full = r.k_empty + C::kStages;
-    r.v_empty = r.v_full + C::kStages;
-    r.s_full = r.v_empty + C::kStages;
-    r.dp_full = r.s_full + 1;
-    r.s_free = r.dp_full + 1;
-    r.ds_ready = r.s_free + 1;
-    r.acc_ready = r.ds_ready + 1;
+    r.k_empty = r.k_full + C::kKStages;
+    r.v_full = r.k_empty + C::kKStages;
+    r.v_empty = r.v_full + C::kVStages;
+    r.s_full = r.v_empty + C::kVStages;
+    r.dp_full = r.s_full + 1;    // [2], one per dP buffer
+    r.s_free = r.dp_full + 2;
+    r.ds_ready = r.s_free + 1;   // [2], one per dP buffer
+    r.acc_ready = r.ds_ready + 2;
     r.drain = r.acc_ready + 1;
     return r;
 }
@@ -597,16 +602,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bars.q_full, 1);
         mbar_init(bars.q_empty, 1);
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bars.k_full + s, 1);
             mbar_init(bars.k_empty + s, 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(bars.v_full + s, 1);
             mbar_init(bars.v_empty + s, 1);
         }
         mbar_init(bars.s_full, 1);
-        mbar_init(bars.dp_full, 1);
         mbar_init(bars.s_free, kSoftmaxThreads);
-        mbar_init(bars.ds_ready, kSoftmaxThreads);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bars.dp_full + s, 1);
+            mbar_init(bars.ds_ready + s, kSoftmaxThreads);
+        }
         mbar_init(bars.acc_ready, 1);
         mbar_init(bars.drain, 1);
         *abort_flag = 0;
@@ -631,7 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             uint32_t g = 0, uq = 0;
-            uint32_t k_issued[C::kStages] = {}, v_issued[C::kStages] = {};
+            uint32_t k_issued[C::kKStages] = {}, v_issued[C::kVStages] = {};
             bool ok = true;
             for (int r = 0; ok && r * Gd < U; ++r) {
                 const int u = unit_index(r, blockIdx.x, Gd);
@@ -650,28 +659,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int g_kv = x.h / p.G;
                 for (int e = 0; e < x.cnt; ++e) {
                     const int kt = x.list[e];
-                    const int st = g % C::kStages;
-                    const uint32_t ph = (g / C::kStages) & 1;
-                    if (!(ok = mbar_wait(bars.k_empty + st, ph ^ 1, ctx))) break;
-                    mbar_expect_tx(bars.k_full + st, C::kTileBytes);
+                    const int sk = g % C::kKStages;
+                    if (!(ok = mbar_wait(bars.k_empty + sk, ((g / C::kKStages) & 1) ^ 1, ctx))) break;
+                    mbar_expect_tx(bars.k_full + sk, C::kTileBytes);
                     for (int hb = 0; hb < D / 64; ++hb)
-                        tma_load_4d(smem + C::kKOff + st * C::kTileBytes + hb * 16384, &tm_k,
-                                    bars.k_full + st, hb * 64, g_kv, kt * kTile, x.b);
-                    ++k_issued[st];
-                    if (!(ok = mbar_wait(bars.v_empty + st, ph ^ 1, ctx))) break;
-                    mbar_expect_tx(bars.v_full + st, C::kTileBytes);
+                        tma_load_4d(smem + C::kKOff + sk * C::kTileBytes + hb * 16384, &tm_k,
+                                    bars.k_full + sk, hb * 64, g_kv, kt * kTile, x.b);
+                    ++k_issued[sk];
+                    const int sv = g % C::kVStages;
+                    if (!(ok = mbar_wait(bars.v_empty + sv, ((g / C::kVStages) & 1) ^ 1, ctx))) break;
+                    mbar_expect_tx(bars.v_full + sv, C::kTileBytes);
                     for (int hb = 0; hb < D / 64; ++hb)
-                        tma_load_4d(smem + C::kVOff + st * C::kTileBytes + hb * 16384, &tm_v,
-                                    bars.v_full + st, hb * 64, g_kv, kt * kTile, x.b);
-                    ++v_issued[st];
+                        tma_load_4d(smem + C::kVOff + sv * C::kTileBytes + hb * 16384, &tm_v,
+                                    bars.v_full + sv, hb * 64, g_kv, kt * kTile, x.b);
+                    ++v_issued[sv];
                     ++g;
                 }
             }
             if (!ok) {
-                for (int s = 0; s < C::kStages; ++s) {
+                for (int s = 0; s < C::kKStages; ++s)
                     if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
+                for (int s = 0; s < C::kVStages; ++s)
                     if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
-                }
                 if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
             }
         }
@@ -685,16 +694,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t g = 0, uq = 0;
             bool ok = true;
             auto wait_kv = [&](uint32_t t) -> bool {
-                const int st = t % C::kStages;
-                const uint32_t ph = (t / C::kStages) & 1;
-                if (!mbar_wait(bars.k_full + st, ph, ctx)) return false;
-                if (!mbar_wait(bars.v_full + st, ph, ctx)) return false;
+                if (!mbar_wait(bars.k_full + t % C::kKStages, (t / C::kKStages) & 1, ctx)) return false;
+                if (!mbar_wait(bars.v_full + t % C::kVStages, (t / C::kVStages) & 1, ctx)) return false;
                 tc_fence_after();
                 return true;
             };
             // S = Q K^T of tile t into columns [0,128)
             auto issue_s = [&](uint32_t t) {
-                const uint32_t kb = k_base + (t % C::kStages) * C::kTileBytes;
+                const uint32_t kb = k_base + (t % C::kKStages) * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -703,22 +710,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 tc_commit(bars.s_full);
             };
-            // dP = dO V^T of tile t into columns [128,256)
+            // dP = dO V^T of tile t into its dP buffer; V's stage is free after it
             auto issue_dp = [&](uint32_t t) {
-                const uint32_t vb = v_base + (t % C::kStages) * C::kTileBytes;
+                const uint32_t vb = v_base + (t % C::kVStages) * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem + C::kColDP, sdesc_sw128(do_base + off, 16, 1024),
+                    mma_ss(tmem + C::dp_col(t), sdesc_sw128(do_base + off, 16, 1024),
                            sdesc_sw128(vb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bars.dp_full);
+                tc_commit(bars.dp_full + (t & 1));
+                tc_commit(bars.v_empty + t % C::kVStages);
             };
-            // Issue order per tile g (each product overlaps a softmax phase):
-            //   dP(g) | phase A(g) (P from S);  S(g+1) | phase B(g) (dS from dP);
-            //   dQ(g), dP(g+1) | phase A(g+1).
-            // dS(g) is written over dP(g), so S(g+1) only needs phase A(g) to
-            // have read S(g); dP(g+1) follows dQ(g), the last reader of dS(g).
+            // Issue order: S(g) and dP(g) together, as soon as phase A(g-1) has
+            // read S(g-1) (S is single-buffered); dQ(g) once phase B(g) has
+            // written dS(g) over dP(g).  dP is double-buffered, so dP(g+1)
+            // never waits for dQ(g): the softmax phases of tile g+1 overlap
+            // the products dQ(g), S(g+2), dP(g+2).  dP(g+1) overwrites the
+            // buffer of dS(g-1), whose reader dQ(g-1) is already issued.
             for (int r = 0; ok && r * Gd < U; ++r) {
                 const int u = unit_index(r, blockIdx.x, Gd);
                 if (u >= U) continue;
@@ -729,26 +738,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ++uq;
                 if (!(ok = wait_kv(g))) break;
                 issue_s(g);
+                issue_dp(g);
+                if (x.cnt == 1) tc_commit(bars.q_empty);
                 for (int e = 0; e < x.cnt; ++e, ++g) {
-                    const int st = g % C::kStages;
-                    issue_dp(g);
-                    tc_commit(bars.v_empty + st);
-                    if (e == x.cnt - 1) tc_commit(bars.q_empty);
                     if (!(ok = mbar_wait(bars.s_free, g & 1, ctx))) break;
                     if (e + 1 < x.cnt) {
                         if (!(ok = wait_kv(g + 1))) break;
                         issue_s(g + 1);
+                        issue_dp(g + 1);
+                        // Q and dO of the unit are read by nothing after this
+                        if (e + 2 == x.cnt) tc_commit(bars.q_empty);
                     }
                     // dQ += dS K   (A = dS from TMEM, B = K as a K=kv x N=D MN-major tile)
-                    if (!(ok = mbar_wait(bars.ds_ready, g & 1, ctx))) break;
+                    if (!(ok = mbar_wait(bars.ds_ready + (g & 1), (g >> 1) & 1, ctx))) break;
                     tc_fence_after();
-                    const uint32_t kb = k_base + st * C::kTileBytes;
+                    const int sk = g % C::kKStages;
+                    const uint32_t kb = k_base + sk * C::kTileBytes;
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + C::kColDQ, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
+                        mma_ts(tmem + C::kColDQ, tmem + C::dp_col(g) + kk * 8 + (kk >= 4 ? 32 : 0),
                                sdesc_sw128(kb + kk * 2048, 16384, 1024), C::kIdescAcc,
                                (e > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bars.k_empty + st);
+                    tc_commit(bars.k_empty + sk);
                 }
                 if (!ok) break;
                 tc_commit(bars.acc_ready);
@@ -839,12 +850,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tc_fence_before();
                     mbar_arrive(bars.s_free);
                     // ---- phase B: dS = Pc (dP - Delta), written over this half's dP columns
-                    if (!(ok = wait_all(bars.dp_full, g & 1))) break;
+                    const uint32_t dpc = C::dp_col(g);
+                    if (!(ok = wait_all(bars.dp_full + (g & 1), (g >> 1) & 1))) break;
                     tc_fence_after();
                     {
                         float dpv[64];
-                        tmem_ld32(lane_base + C::kColDP + c0, dpv);
-                        tmem_ld32(lane_base + C::kColDP + c0 + 32, dpv + 32);
+                        tmem_ld32(lane_base + dpc + c0, dpv);
+                        tmem_ld32(lane_base + dpc + c0 + 32, dpv + 32);
                         tmem_ld_wait();
                         uint32_t pk[32];
                         const float2 dl2 = make_float2(dl, dl);
@@ -854,11 +866,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                    fsub2(make_float2(dpv[j], dpv[j + 1]), dl2));
                             pk[j >> 1] = pack_bf16x2(r.x, r.y);
                         }
-                        tmem_st32(lane_base + C::kColDP + c0, pk);
+                        tmem_st32(lane_base + dpc + c0, pk);
                     }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(bars.ds_ready);
+                    mbar_arrive(bars.ds_ready + (g & 1));
                 }
                 if (!ok) break;
                 if (!(ok = wait_all(bars.acc_ready, ua & 1))) break;
