@@ -369,9 +369,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         continue;
                     }
                     float m_ref = -INFINITY, l = 0.f;
+                    // the next tile's id and class are fetched one tile ahead
+                    int kt_next = x.list[lo];
+                    uint8_t cls_next = crow[kt_next];
                     for (int e = lo; ok && e < hi; ++e) {
-                        const int kt = x.list[e];
-                        const bool partial = crow[kt] == RA_TILE_PARTIAL;
+                        const int kt = kt_next;
+                        const bool partial = cls_next == RA_TILE_PARTIAL;
+                        if (e + 1 < hi) {
+                            kt_next = x.list[e + 1];
+                            cls_next = crow[kt_next];
+                        }
                         const int sb = g & 1;
                         uint32_t vis0 = ~0u, vis1 = ~0u;
                         if (partial) {
