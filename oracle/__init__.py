@@ -52,7 +52,8 @@ class _Params(ctypes.Structure):
         ("causal", ctypes.c_int), ("pad_segment_id", ctypes.c_int),
         ("q_pos", ctypes.c_void_p), ("kv_pos", ctypes.c_void_p),
         ("q_seg", ctypes.c_void_p), ("kv_seg", ctypes.c_void_p),
-        ("sinks", ctypes.c_void_p),
+        ("sinks", ctypes.c_void_p), ("local_mask", ctypes.c_void_p),
+        ("lq_s", ctypes.c_int), ("lk_s", ctypes.c_int),
     ]
 
 
@@ -106,21 +107,35 @@ def _ptr(a):
     return None if a is None else a.ctypes.data
 
 
+def _local(mask, Lq, Lkv):
+    """A local (per-device) 2-D mask as contiguous uint8, with its shape (R-local)."""
+    if mask is None:
+        return None, 1, 1
+    m = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    lq_s, lk_s = m.shape
+    if Lq % lq_s or Lkv % lk_s:
+        raise ValueError("the local mask's shape must divide (Lq, Lkv)")
+    return m, int(lq_s), int(lk_s)
+
+
 class _Call:
     """Holds the numpy buffers referenced by one params struct alive."""
 
     def __init__(self, q, k, v, *, scale, soft_cap=None, causal=False, q_pos=None,
-                 kv_pos=None, q_seg=None, kv_seg=None, sinks=None, pad_segment_id=-1):
+                 kv_pos=None, q_seg=None, kv_seg=None, sinks=None, pad_segment_id=-1,
+                 local_mask=None):
         self.q, self.k, self.v = _f64(q), _f64(k), _f64(v)
         B, Lq, Hq, D = self.q.shape
         _, Lkv, Hkv, _ = self.k.shape
         self.q_pos, self.kv_pos = _i32(q_pos), _i32(kv_pos)
         self.q_seg, self.kv_seg = _i32(q_seg), _i32(kv_seg)
         self.sinks = None if sinks is None else _f64(sinks)
+        self.local_mask, lq_s, lk_s = _local(local_mask, Lq, Lkv)
         self.p = _Params(B, Lq, Lkv, Hq, Hkv, D, float(scale),
                          float(soft_cap) if soft_cap else 0.0, int(bool(causal)),
                          int(pad_segment_id), _ptr(self.q_pos), _ptr(self.kv_pos),
-                         _ptr(self.q_seg), _ptr(self.kv_seg), _ptr(self.sinks))
+                         _ptr(self.q_seg), _ptr(self.kv_seg), _ptr(self.sinks),
+                         _ptr(self.local_mask), lq_s, lk_s)
         self.shape = (B, Lq, Lkv, Hq, Hkv, D)
 
 
@@ -192,11 +207,12 @@ def merge(out, lse, block_out, block_lse):
 
 
 def block_mask(B, Lq, Lkv, *, causal, q_pos=None, kv_pos=None, q_seg=None, kv_seg=None,
-               pad_segment_id=-1):
+               pad_segment_id=-1, local_mask=None):
     """Tile classes (0 empty, 1 partial, 2 full) and tile lists, see ra_oracle.c."""
     q_pos, kv_pos, q_seg, kv_seg = map(_i32, (q_pos, kv_pos, q_seg, kv_seg))
+    lm, lq_s, lk_s = _local(local_mask, Lq, Lkv)
     p = _Params(B, Lq, Lkv, 1, 1, 1, 1.0, 0.0, int(bool(causal)), int(pad_segment_id),
-                _ptr(q_pos), _ptr(kv_pos), _ptr(q_seg), _ptr(kv_seg), None)
+                _ptr(q_pos), _ptr(kv_pos), _ptr(q_seg), _ptr(kv_seg), None, _ptr(lm), lq_s, lk_s)
     nq, nk = Lq // TILE, Lkv // TILE
     cls = np.zeros((B, nq, nk), np.uint8)
     fcnt = np.zeros(B * nq, np.int32)

@@ -27,6 +27,12 @@
  *            positions mean the token's index in the sequence as given.
  *   R-gqa    kv head of query head h is h / (Hq / Hkv).
  *   R-zig    zigzag: 2N chunks, virtual device d holds chunks d and 2N-1-d.
+ *   R-local  without causal masking the ring of [RS] (_ring_attention_forward,
+ *            non-causal branch) applies the one 2-D mask given to
+ *            make_ring_attention -- local query length x local kv length --
+ *            at every ring step; the pair (i, j) is then visible only where
+ *            local_mask[i mod Lq_s][j mod Lkv_s] is set (Lq_s, Lkv_s = the
+ *            per-device lengths), in addition to the segment rule.
  */
 #include <math.h>
 #include <stdint.h>
@@ -48,12 +54,15 @@ typedef struct {
     const int32_t *q_pos, *kv_pos; /* NULL -> index in the sequence */
     const int32_t *q_seg, *kv_seg; /* NULL -> one segment, no padding */
     const double *sinks;           /* NULL -> no sink */
+    const uint8_t *local_mask;     /* [lq_s][lk_s], nonzero = visible; NULL -> none (R-local) */
+    int lq_s, lk_s;                /* per-device query / kv lengths of local_mask */
 } ora_params;
 
 /* ------------------------------------------------------------------ */
-/* visibility of one (query, key) pair: same non-padding segment and, if
- * causal, query position >= key position.  [KVAX] flash_attention
- * (segment ids, positions, PADDING_SEGMENT_ID); [RS] causal_mask_fn. */
+/* visibility of one (query, key) pair: same non-padding segment, if causal
+ * query position >= key position, and the local mask if one is given.
+ * [KVAX] flash_attention (segment ids, positions, PADDING_SEGMENT_ID);
+ * [RS] causal_mask_fn and the non-causal ring's per-step mask. */
 static int ora_visible(const ora_params *p, int b, int i, int j)
 {
     if (p->q_seg || p->kv_seg) {
@@ -67,6 +76,8 @@ static int ora_visible(const ora_params *p, int b, int i, int j)
         int pk = p->kv_pos ? p->kv_pos[(size_t)b * p->Lkv + j] : j;
         if (pq < pk) return 0;
     }
+    if (p->local_mask && !p->local_mask[(size_t)(i % p->lq_s) * p->lk_s + (j % p->lk_s)])
+        return 0; /* R-local */
     return 1;
 }
 

@@ -9,7 +9,8 @@ import numpy as np
 from scipy.special import logsumexp
 
 
-def visibility(B, Lq, Lkv, *, causal, q_pos=None, kv_pos=None, q_seg=None, kv_seg=None, pad=-1):
+def visibility(B, Lq, Lkv, *, causal, q_pos=None, kv_pos=None, q_seg=None, kv_seg=None, pad=-1,
+               local_mask=None):
     qp = np.broadcast_to(np.arange(Lq), (B, Lq)) if q_pos is None else np.asarray(q_pos)
     kp = np.broadcast_to(np.arange(Lkv), (B, Lkv)) if kv_pos is None else np.asarray(kv_pos)
     qs = np.zeros((B, Lq), np.int64) if q_seg is None else np.asarray(q_seg, np.int64)
@@ -17,11 +18,15 @@ def visibility(B, Lq, Lkv, *, causal, q_pos=None, kv_pos=None, q_seg=None, kv_se
     vis = (qs[:, :, None] == ks[:, None, :]) & (qs[:, :, None] != pad)
     if causal:
         vis &= qp[:, :, None] >= kp[:, None, :]
+    if local_mask is not None:
+        # the per-device mask repeated over every (query shard, kv shard) block
+        lm = np.asarray(local_mask) != 0
+        vis &= np.tile(lm, (Lq // lm.shape[0], Lkv // lm.shape[1]))[None]
     return vis  # [B, Lq, Lkv]
 
 
 def attention(q, k, v, *, scale, soft_cap=None, causal=False, q_pos=None, kv_pos=None,
-              q_seg=None, kv_seg=None, sinks=None, pad=-1):
+              q_seg=None, kv_seg=None, sinks=None, pad=-1, local_mask=None):
     q, k, v = (np.asarray(a, np.float64) for a in (q, k, v))
     B, Lq, Hq, D = q.shape
     Lkv, Hkv = k.shape[1], k.shape[2]
@@ -32,7 +37,7 @@ def attention(q, k, v, *, scale, soft_cap=None, causal=False, q_pos=None, kv_pos
     if soft_cap:
         s = soft_cap * np.tanh(s / soft_cap)
     vis = visibility(B, Lq, Lkv, causal=causal, q_pos=q_pos, kv_pos=kv_pos, q_seg=q_seg,
-                     kv_seg=kv_seg, pad=pad)
+                     kv_seg=kv_seg, pad=pad, local_mask=local_mask)
     s = np.where(vis[:, None], s, -np.inf)
     if sinks is not None:
         col = np.broadcast_to(np.asarray(sinks, np.float64)[None, :, None, None], (B, Hq, Lq, 1))

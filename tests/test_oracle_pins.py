@@ -400,3 +400,99 @@ def test_row_and_head_restriction_equals_full():
              for r in ((0, 50), (50, 96)) for hh in ((0, 1), (1, 4))]
     for t in range(4):
         np.testing.assert_allclose(sum(pp[t] for pp in parts), full[t], atol=1e-12)
+
+
+# ------------------------------------------------- local mask (non-causal ring)
+def _local_mask(seed, ls, lk=None, density=0.5):
+    rng = np.random.default_rng(seed)
+    lk = ls if lk is None else lk
+    return (rng.random((ls, lk)) < density).astype(np.uint8)
+
+
+LOCAL_CASES = [
+    dict(n=2),
+    dict(n=4, segs=True, pad=10),
+    dict(n=2, sinks=True, cap=2.0),
+    dict(n=3, Hq=4, Hkv=1),
+    dict(n=1, segs=True),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(LOCAL_CASES)))
+def test_local_mask_equals_bruteforce_and_ring(ci):
+    case = dict(LOCAL_CASES[ci])
+    n = case.pop("n")
+    case.setdefault("L", 96)
+    q, k, v, kw = _case(500 + ci, causal=False, **case)
+    lm = _local_mask(ci, case["L"] // n)
+    kw["local_mask"] = lm
+    o1, l1 = oracle.attn_fwd(q, k, v, **kw)
+    o2, l2 = brute.attention(q, k, v, **kw)
+    assert np.array_equal(np.isfinite(l1), np.isfinite(l2))
+    f = np.isfinite(l2)
+    np.testing.assert_allclose(l1[f], l2[f], atol=1e-12, rtol=0)
+    np.testing.assert_allclose(o1, o2, atol=1e-12, rtol=0)
+    # the ring over n shards with the mask applied at every step == plain
+    o3, l3 = oracle.attn_fwd_ring(q, k, v, n_shards=n, **kw)
+    np.testing.assert_allclose(l3[f], l1[f], atol=1e-12, rtol=0)
+    np.testing.assert_allclose(o3, o1, atol=1e-12, rtol=0)
+
+
+def test_local_mask_special_cases():
+    q, k, v, kw = _case(601, L=64, causal=False)
+    # an all-ones local mask is no mask at all
+    ones = np.ones((32, 32), np.uint8)
+    o0, l0 = oracle.attn_fwd(q, k, v, **kw)
+    o1, l1 = oracle.attn_fwd(q, k, v, local_mask=ones, **kw)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    # one shard with a lower-triangular local mask is the causal mask
+    tri = np.tril(np.ones((64, 64), np.uint8))
+    o2, l2 = oracle.attn_fwd(q, k, v, local_mask=tri, **kw)
+    kc = dict(kw, causal=True)
+    o3, l3 = oracle.attn_fwd(q, k, v, **kc)
+    assert np.array_equal(o2, o3) and np.array_equal(l2, l3)
+    # with two shards the triangle repeats per block: query row 40 (local
+    # row 8 of shard 1) sees keys 0..8 of shard 0 and 32..40 of shard 1
+    tri2 = np.tril(np.ones((32, 32), np.uint8))
+    vis = brute.visibility(1, 64, 64, causal=False, local_mask=tri2)[0]
+    assert np.nonzero(vis[40])[0].tolist() == list(range(0, 9)) + list(range(32, 41))
+
+
+def test_local_mask_gradients_central_differences():
+    q, k, v, kw = _case(602, B=1, L=24, D=4, causal=False, sinks=True)
+    kw["local_mask"] = _local_mask(7, 12)
+    do = np.random.default_rng(5).normal(size=q.shape)
+    dq, dk, dv, ds, _, _ = oracle.attn_bwd(q, k, v, do, **kw)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attn_fwd(q_, k_, v_, **kw)
+        return float(np.sum(o * do))
+
+    rng = np.random.default_rng(9)
+    h = 1e-5
+    for name, arr, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(10):
+            idx = tuple(rng.integers(0, s) for s in arr.shape)
+            ap, am = arr.copy(), arr.copy()
+            ap[idx] += h
+            am[idx] -= h
+            args_p = {"q": (ap, k, v), "k": (q, ap, v), "v": (q, k, ap)}[name]
+            args_m = {"q": (am, k, v), "k": (q, am, v), "v": (q, k, am)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+@pytest.mark.parametrize("n", [1, 2, 4])
+def test_local_mask_block_map_bruteforce(n):
+    g = torch.Generator().manual_seed(40 + n)
+    B, L = 2, 512
+    seg, pos = random_structure(g, B, L, n_docs_max=3, pad_max=100)
+    ls = L // n
+    # banded local mask (a sliding window) with a random hole pattern
+    i = np.arange(ls)[:, None]
+    j = np.arange(ls)[None, :]
+    lm = ((np.abs(i - j) < 150) & (_local_mask(n, ls, density=0.97) != 0)).astype(np.uint8)
+    kw = dict(causal=False, q_pos=pos.numpy(), kv_pos=pos.numpy(), q_seg=seg.numpy(),
+              kv_seg=seg.numpy(), local_mask=lm)
+    m = oracle.block_mask(B, L, L, **kw)
+    assert np.array_equal(m["tile_class"], _brute_map(B, L, **kw))
