@@ -60,7 +60,7 @@ class RaAttnParams(ctypes.Structure):
         ("pad_segment_id", ctypes.c_int),
         ("q_pos", ctypes.c_void_p), ("kv_pos", ctypes.c_void_p),
         ("q_seg", ctypes.c_void_p), ("kv_seg", ctypes.c_void_p),
-        ("sinks", ctypes.c_void_p),
+        ("sinks", ctypes.c_void_p), ("local_mask", ctypes.c_void_p),
     ]
 
 
@@ -257,9 +257,10 @@ _DT = {torch.bfloat16: RA_BF16, torch.float32: RA_FP32}
 
 def make_params(q, k, *, scale, causal=False, soft_cap=0.0, n_virtual_shards=1, is_mqa=False,
                 pad_segment_id=-1, q_pos=None, kv_pos=None, q_seg=None, kv_seg=None,
-                sinks=None) -> RaAttnParams:
+                sinks=None, local_mask=None) -> RaAttnParams:
     """Params for q (B,Lq,Hq,D) and k (B,Lkv,Hkv,D) tensors; keeps the
-    position / segment / sink tensors referenced by the struct alive."""
+    position / segment / sink / local-mask tensors referenced by the struct
+    alive.  ``local_mask``: (Lq/N, Lkv/N) uint8 device tensor (non-causal only)."""
     B, Lq, Hq, D = q.shape
     Lkv, Hkv = k.shape[1], k.shape[2]
     if q.dtype not in _DT:
@@ -267,8 +268,8 @@ def make_params(q, k, *, scale, causal=False, soft_cap=0.0, n_virtual_shards=1, 
     p = RaAttnParams(B, Lq, Lkv, Hq, Hkv, D, _DT[q.dtype], float(scale),
                      float(soft_cap or 0.0), int(bool(causal)), int(bool(is_mqa)),
                      int(n_virtual_shards), int(pad_segment_id), _ptr(q_pos), _ptr(kv_pos),
-                     _ptr(q_seg), _ptr(kv_seg), _ptr(sinks))
-    p._keep = (q_pos, kv_pos, q_seg, kv_seg, sinks)
+                     _ptr(q_seg), _ptr(kv_seg), _ptr(sinks), _ptr(local_mask))
+    p._keep = (q_pos, kv_pos, q_seg, kv_seg, sinks, local_mask)
     return p
 
 

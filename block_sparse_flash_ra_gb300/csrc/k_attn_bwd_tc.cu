@@ -47,7 +47,7 @@ constexpr int kBwdThreads = 320;
 
 // Visibility bits of query rows q0..q0+63 for one kv row (dkdv: bit c of
 // word c/32 = query row q0+c sees this kv row).
-__device__ __forceinline__ void col_visibility(const Problem &p, int b, int q0, int kv_seg,
+__device__ __forceinline__ void col_visibility(const Problem &p, int b, int q0, int kj, int kv_seg,
                                                int kv_pos, uint32_t vis[2])
 {
     const int4 *qp4 = p.q_pos ? reinterpret_cast<const int4 *>(p.q_pos + (size_t)b * p.Lq + q0) : nullptr;
@@ -71,10 +71,16 @@ __device__ __forceinline__ void col_visibility(const Problem &p, int b, int q0, 
         }
         vis[w] = bits;
     }
+    if (p.local_mask) {
+        uint32_t lb[2];
+        local_col_bits(p, q0, kj, lb);
+        vis[0] &= lb[0];
+        vis[1] &= lb[1];
+    }
 }
 
 // Visibility bits of kv rows k0..k0+63 for one query row (dq).
-__device__ __forceinline__ void row_visibility(const Problem &p, int b, int k0, int q_seg,
+__device__ __forceinline__ void row_visibility(const Problem &p, int b, int k0, int qi, int q_seg,
                                                bool q_pad, int q_pos, uint32_t vis[2])
 {
     const int4 *kp4 = p.kv_pos ? reinterpret_cast<const int4 *>(p.kv_pos + (size_t)b * p.Lkv + k0) : nullptr;
@@ -97,6 +103,12 @@ __device__ __forceinline__ void row_visibility(const Problem &p, int b, int k0, 
             }
         }
         vis[w] = bits;
+    }
+    if (p.local_mask) {
+        uint32_t lb[2];
+        local_row_bits(p, qi, k0, lb);
+        vis[0] &= lb[0];
+        vis[1] &= lb[1];
     }
 }
 
@@ -383,7 +395,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         p.tile_class[((size_t)x.b * p.nq + qt) * p.nk + x.kt] == RA_TILE_PARTIAL;
                     // ---- visibility bits of this half's 64 query columns (partial tiles only)
                     uint32_t vis[2] = {~0u, ~0u};
-                    if (partial) col_visibility(p, x.b, qt * kTile + c0, my_seg, my_pos, vis);
+                    if (partial) col_visibility(p, x.b, qt * kTile + c0, kj, my_seg, my_pos, vis);
                     if (!(ok = wait_all(bars.s_full, n & 1))) break;
                     tc_fence_after();
                     // ---- P^T (bf16 -> TMEM) and Pc = P * (1 - tanh^2) kept packed
@@ -807,7 +819,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int kt = x.list[e];
                     const bool partial = crow[kt] == RA_TILE_PARTIAL;
                     uint32_t vis[2] = {~0u, ~0u};
-                    if (partial) row_visibility(p, x.b, kt * kTile + c0, my_seg, my_pad, my_pos, vis);
+                    if (partial) row_visibility(p, x.b, kt * kTile + c0, qi, my_seg, my_pad, my_pos, vis);
                     if (!(ok = wait_all(bars.s_full, g & 1))) break;
                     tc_fence_after();
                     // ---- phase A: Pc = P * (1 - tanh^2), packed bf16 (P from S)

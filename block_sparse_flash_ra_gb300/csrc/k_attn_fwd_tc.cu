@@ -404,6 +404,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     bits[jj >> 3] |= (vis ? 1u : 0u) << ((4 * jj + z) & 31);
                                 }
                             }
+                            if (p.local_mask) {
+                                uint32_t lb[2];
+                                local_row_bits(p, qi, j0, lb);
+                                bits[0] &= lb[0];
+                                bits[1] &= lb[1];
+                            }
                             vis0 = bits[0];
                             vis1 = bits[1];
                         }

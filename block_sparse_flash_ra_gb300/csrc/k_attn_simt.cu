@@ -85,6 +85,9 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(Problem p, const float *_
                 if (partial) {
                     bool vis = (kseg[j] == my_seg) && !my_pad;
                     if (p.causal) vis = vis && (my_pos >= kpos[j]);
+                    if (p.local_mask)
+                        vis = vis && p.local_mask[(size_t)(i % p.lq_s) * p.lk_s +
+                                                  (kt * kTile + j) % p.lk_s] != 0;
                     if (!vis) continue;
                 }
                 float acc = 0.f;

@@ -11,7 +11,8 @@
 // 2. classify_rows: one block per (b, qt).  Tiles whose class follows
 //    exactly from the summaries (disjoint segment ranges; one common segment,
 //    where the causal predicate reduces to comparing position ranges) are
-//    classified from them; the rest are counted pair by pair.  The block then
+//    classified from them; the rest -- and, with the non-causal ring's local
+//    mask, every tile not already empty -- are counted pair by pair.  The block then
 //    compacts the non-empty kt of its row into fwd_idx and records where the
 //    tiles of each KV shard begin in that list (fwd_shard).
 // 3. columns: one block per (b, kt) compacts the non-empty qt into bwd_idx.
@@ -108,7 +109,10 @@ __global__ void __launch_bounds__(kCls) classify_rows_kernel(Problem p, const Ti
         if (threadIdx.x == 0) nslow = 0;
         __syncthreads();
         for (int kt = k0 + threadIdx.x; kt < kend; kt += kCls) {
-            const int c = classify_fast(qs, ksum[(size_t)b * nk + kt], p.causal);
+            int c = classify_fast(qs, ksum[(size_t)b * nk + kt], p.causal);
+            // a local mask can only remove pairs: tiles not already empty are
+            // counted pair by pair
+            if (p.local_mask && c != RA_TILE_EMPTY) c = -1;
             if (c < 0) {
                 slow[atomicAdd(&nslow, 1)] = kt;
             } else {
@@ -131,6 +135,9 @@ __global__ void __launch_bounds__(kCls) classify_rows_kernel(Problem p, const Ti
                 const int sq = q_seg_s[i];
                 bool vis = (sq == k_seg_s[j]) && !(p.q_seg && sq == p.pad_id);
                 if (p.causal) vis = vis && (q_pos_s[i] >= k_pos_s[j]);
+                if (p.local_mask)
+                    vis = vis && p.local_mask[(size_t)((qt * kTile + i) % p.lq_s) * p.lk_s +
+                                              (kt * kTile + j) % p.lk_s] != 0;
                 cnt += vis ? 1 : 0;
             }
             for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);

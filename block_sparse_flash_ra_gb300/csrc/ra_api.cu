@@ -119,10 +119,14 @@ int check_params(const ra_attn_params *p)
         return fail(RA_ERR_INVALID_ARG, "scale must be positive and finite");
     if ((p->q_seg == nullptr) != (p->kv_seg == nullptr))
         return fail(RA_ERR_INVALID_ARG, "q_seg and kv_seg must both be given or both be NULL");
-    const void *ptrs[5] = {p->q_pos, p->kv_pos, p->q_seg, p->kv_seg, p->sinks};
+    if (p->local_mask && p->causal)
+        return fail(RA_ERR_INVALID_ARG, "local_mask is only defined for causal == 0 (the causal ring "
+                                        "replaces the mask)");
+    const void *ptrs[6] = {p->q_pos, p->kv_pos, p->q_seg, p->kv_seg, p->sinks, p->local_mask};
     for (const void *x : ptrs)
         if (x && !aligned16(x))
-            return fail(RA_ERR_INVALID_ARG, "positions, segment ids and sinks must be 16-byte aligned");
+            return fail(RA_ERR_INVALID_ARG,
+                        "positions, segment ids, sinks and local_mask must be 16-byte aligned");
     return RA_OK;
 }
 
@@ -146,6 +150,7 @@ uint64_t mask_key(const ra_attn_params *p)
     h = mix(h, reinterpret_cast<uintptr_t>(p->kv_pos));
     h = mix(h, reinterpret_cast<uintptr_t>(p->q_seg));
     h = mix(h, reinterpret_cast<uintptr_t>(p->kv_seg));
+    h = mix(h, reinterpret_cast<uintptr_t>(p->local_mask));
     return h;
 }
 
@@ -197,6 +202,9 @@ Problem make_problem(const ra_attn_params *p, const ra_block_mask *m, int *statu
     x.q_seg = p->q_seg;
     x.kv_seg = p->kv_seg;
     x.sinks = p->sinks;
+    x.local_mask = p->local_mask;
+    x.lq_s = p->Lq / p->n_virtual_shards;
+    x.lk_s = p->Lkv / p->n_virtual_shards;
     if (m) {
         x.tile_class = m->tile_class;
         x.fwd_cnt = m->fwd_cnt;

@@ -24,6 +24,8 @@ struct Problem {
     int pad_id;
     const int32_t *q_pos, *kv_pos, *q_seg, *kv_seg;
     const float *sinks;
+    const uint8_t *local_mask; // (lq_s, lk_s) per-shard mask of the non-causal ring, or NULL
+    int lq_s, lk_s;            // Lq / N, Lkv / N
     // block map
     const uint8_t *tile_class;
     const int32_t *fwd_cnt, *fwd_idx, *bwd_cnt, *bwd_idx, *fwd_order, *bwd_order;

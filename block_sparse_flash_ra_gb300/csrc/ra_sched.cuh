@@ -14,6 +14,47 @@ __device__ __forceinline__ int unit_index(int round, int cta, int G)
     return round * G + ((round & 1) ? (G - 1 - cta) : cta);
 }
 
+// The non-causal ring's per-shard mask (Problem::local_mask) on partial
+// tiles.  Row form: bit c of bits[c / 32] is set iff query row qi may see kv
+// column j0 + c, i.e. local_mask[qi mod lq_s][(j0 + c) mod lk_s] != 0; j0 is a
+// multiple of 64 and shards are whole tiles, so the 64 bytes are contiguous
+// and 16-byte aligned.
+__device__ __forceinline__ void local_row_bits(const Problem &p, int qi, int j0, uint32_t bits[2])
+{
+    const uint4 *m4 = reinterpret_cast<const uint4 *>(
+        p.local_mask + (size_t)(qi % p.lq_s) * p.lk_s + (j0 % p.lk_s));
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        uint32_t b = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 v = __ldg(m4 + 2 * w + h);
+            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int z = 0; z < 4; ++z)
+                    b |= (((words[k] >> (8 * z)) & 0xffu) ? 1u : 0u) << (16 * h + 4 * k + z);
+        }
+        bits[w] = b;
+    }
+}
+
+// Column form: bit c set iff query row q0 + c may see kv row kj (q0 a
+// multiple of 64).
+__device__ __forceinline__ void local_col_bits(const Problem &p, int q0, int kj, uint32_t bits[2])
+{
+    const uint8_t *m = p.local_mask + (size_t)(q0 % p.lq_s) * p.lk_s + (kj % p.lk_s);
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        uint32_t b = 0;
+#pragma unroll 8
+        for (int c = 0; c < 32; ++c)
+            b |= (__ldg(m + (size_t)(32 * w + c) * p.lk_s) ? 1u : 0u) << c;
+        bits[w] = b;
+    }
+}
+
 // Wait used only while tearing down after an abort: bounded, ignores the
 // abort flag.
 __device__ __forceinline__ bool wait_drain(uint64_t *bar, uint32_t parity, uint64_t ns)

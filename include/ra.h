@@ -100,6 +100,14 @@ enum { RA_TILE_EMPTY = 0, RA_TILE_PARTIAL = 1, RA_TILE_FULL = 2 };
  *                    without padding.  Both or neither.
  *   sinks            (Hq) fp32 sink logits, counted once per row in the
  *                    denominator only, or NULL.
+ *   local_mask       (Lq/N, Lkv/N) uint8, nonzero = visible, or NULL: the
+ *                    2-D mask of _ring_splash make_ring_attention, which the
+ *                    non-causal ring applies at every ring step, so pair
+ *                    (i, j) also needs local_mask[i mod Lq/N][j mod Lkv/N].
+ *                    Only with causal == 0 (the pages' causal ring replaces
+ *                    the mask; the combination is rejected here).  16-byte
+ *                    aligned; owned by the caller, read by the block-map
+ *                    build and by the attention kernels on partial tiles.
  */
 typedef struct {
     int B, Lq, Lkv, Hq, Hkv, D;
@@ -115,6 +123,7 @@ typedef struct {
     const int32_t *q_seg;
     const int32_t *kv_seg;
     const float *sinks;
+    const uint8_t *local_mask;
 } ra_attn_params;
 
 /*

@@ -50,6 +50,7 @@ def _params(**kw):
 @pytest.mark.parametrize("bad", [
     dict(Hq=3, Hkv=2), dict(is_mqa=1, Hkv=2), dict(Lq=200), dict(Lq=384, n_virtual_shards=2),
     dict(n_virtual_shards=0), dict(B=0), dict(dtype=7), dict(scale=0.0),
+    dict(local_mask=256),  # a local mask needs causal == 0
 ])
 def test_invalid_params_rejected(L, bad):
     p = _params(**bad)

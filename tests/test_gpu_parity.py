@@ -81,14 +81,17 @@ class Case:
                     dev[key] = ra.permute(dev[key], N)
                     host[key] = host_permute(host[key], N)
         self.dev, self.host = dev, host
+        lm = inp.get("local_mask")
         self.params = ra.make_params(
             dev["q"], dev["k"], scale=w.scale, causal=w.causal, soft_cap=w.soft_cap,
             n_virtual_shards=N, is_mqa=w.is_mqa, q_pos=dev["q_pos"], kv_pos=dev["kv_pos"],
-            q_seg=dev["q_seg"], kv_seg=dev["kv_seg"], sinks=dev["sinks"])
+            q_seg=dev["q_seg"], kv_seg=dev["kv_seg"], sinks=dev["sinks"],
+            local_mask=dev.get("local_mask"))
         self.okw = dict(scale=w.scale, soft_cap=w.soft_cap or None, causal=w.causal,
                         q_pos=i32(host["q_pos"]), kv_pos=i32(host["kv_pos"]),
                         q_seg=i32(host["q_seg"]), kv_seg=i32(host["kv_seg"]),
-                        sinks=f64(host["sinks"]))
+                        sinks=f64(host["sinks"]),
+                        local_mask=None if lm is None else lm.numpy())
 
     def mask(self):
         return ra.build_mask(self.params)
@@ -326,3 +329,76 @@ def test_backward_padding_rows_inside_a_tile_without_sinks():
     for g in grads[:3]:
         assert torch.isfinite(g).all()
     _check_bwd(c, grads)
+
+
+# ------------------------------------------- the non-causal ring's local mask
+def _local_mask(seed, ls, window=None, density=0.9):
+    """(ls, ls) uint8: a band |i - j| < window (if given) with random holes."""
+    g = torch.Generator().manual_seed(seed)
+    m = (torch.rand((ls, ls), generator=g) < density)
+    if window is not None:
+        i = torch.arange(ls)[:, None]
+        j = torch.arange(ls)[None, :]
+        m &= (i - j).abs() < window
+    return m.to(torch.uint8)
+
+
+LOCAL_CASES = {
+    "n2_band": (W(causal=False, n_shards=2, seed=51), dict(window=200)),
+    "n4_random_segments": (W(causal=False, n_shards=4, seed=52), dict(density=0.6, segs=True)),
+    "mqa_sinks_cap": (W(causal=False, Hq=4, Hkv=1, is_mqa=True, sinks=True, soft_cap=30.0,
+                        n_shards=2, seed=53), dict(window=300, density=0.95)),
+    "d64": (W(causal=False, D=64, n_shards=2, seed=54), dict(window=64)),
+    "fp32": (W(causal=False, D=64, dtype="fp32", L=512, n_shards=2, seed=55), dict(window=100)),
+}
+
+
+def _local_case(name, dout=False):
+    w, spec = LOCAL_CASES[name]
+    spec = dict(spec)
+    segs = spec.pop("segs", False)
+    lm = _local_mask(w.seed, w.L // w.n_shards, **spec)
+    kw = dict(overrides=dict(local_mask=lm), dout=dout)
+    if segs:
+        kw.update(structure=dict(n_docs_max=3, pad_max=100), seed_struct=w.seed)
+    return Case(w, **kw)
+
+
+@pytest.mark.parametrize("name", list(LOCAL_CASES))
+def test_local_mask_forward_matches_oracle(name):
+    c = _local_case(name)
+    out, lse, _ = c.gpu_fwd()
+    torch.cuda.synchronize()
+    o_ref, l_ref = c.oracle_fwd()
+    check_fwd(out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("name", ["n2_band", "n4_random_segments", "mqa_sinks_cap"])
+def test_local_mask_backward_matches_oracle(name):
+    c = _local_case(name, dout=True)
+    out, lse, m = c.gpu_fwd()
+    d = c.dev
+    grads = ra.backward(c.params, d["q"], d["k"], d["v"], out, lse, d["dout"], m)
+    torch.cuda.synchronize()
+    _check_bwd(c, grads)
+
+
+def test_local_mask_block_map_bit_exact():
+    g = torch.Generator().manual_seed(9)
+    B, L, N = 2, 1024, 4
+    seg, pos = random_structure(g, B, L, n_docs_max=3, pad_max=150)
+    lm = _local_mask(3, L // N, window=180, density=0.97)
+    q = torch.zeros(B, L, 1, 64, dtype=torch.bfloat16, device="cuda")
+    dseg, dlm = seg.cuda(), lm.cuda()
+    p = ra.make_params(q, q, scale=1.0, causal=False, q_seg=dseg, kv_seg=dseg,
+                       n_virtual_shards=N, local_mask=dlm)
+    m = ra.build_mask(p)
+    torch.cuda.synchronize()
+    ref = oracle.block_mask(B, L, L, causal=False, q_seg=seg.numpy(), kv_seg=seg.numpy(),
+                            local_mask=lm.numpy())
+    nq = nk = L // 128
+    buf = m._buf
+    off = m.tile_class - buf.data_ptr()
+    got = buf[off:off + B * nq * nk].cpu().numpy()
+    assert np.array_equal(got, ref["tile_class"].reshape(-1))
+    assert (got == 0).any() and (got == 1).any()  # the band leaves empty and partial tiles
