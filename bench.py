@@ -177,7 +177,7 @@ class Pipeline:
         self.params = ra.make_params(
             d["q"], d["k"], scale=w.scale, causal=w.causal, soft_cap=w.soft_cap, n_virtual_shards=N,
             is_mqa=w.is_mqa, q_pos=src["q_pos"], kv_pos=src["kv_pos"], q_seg=src["q_seg"],
-            kv_seg=src["kv_seg"], sinks=d["sinks"])
+            kv_seg=src["kv_seg"], sinks=d["sinks"], local_mask=d["local_mask"])
         self.mask_buf = torch.empty(ra.ra_block_mask_bytes(self.params), dtype=torch.uint8, device="cuda")
         self.ws = torch.empty(ra.ra_attn_bwd_workspace_size(self.params), dtype=torch.uint8, device="cuda")
         self.mask = ra.RaBlockMask()
@@ -428,12 +428,13 @@ def _oracle_sample(w, rows):
     sl = lambda t: None if t is None else t[:, :, ::G].contiguous()  # noqa: E731
     kw = dict(scale=w.scale, soft_cap=w.soft_cap or None, causal=w.causal, q_pos=i(inp["q_pos"]),
               kv_pos=i(inp["kv_pos"]), q_seg=i(inp["q_seg"]), kv_seg=i(inp["kv_seg"]),
-              sinks=None if inp["sinks"] is None else f(inp["sinks"][::G]))
+              sinks=None if inp["sinks"] is None else f(inp["sinks"][::G]),
+              local_mask=i(inp["local_mask"]))
     q, do = f(sl(inp["q"])), f(sl(inp["dout"]))
     k, v = f(inp["k"]), f(inp["v"])
     r0 = w.L - rows
     m = oracle.block_mask(w.B, w.L, w.L, causal=w.causal, q_pos=kw["q_pos"], kv_pos=kw["kv_pos"],
-                          q_seg=kw["q_seg"], kv_seg=kw["kv_seg"])
+                          q_seg=kw["q_seg"], kv_seg=kw["kv_seg"], local_mask=kw["local_mask"])
     nq = w.L // 128
     tiles = int(sum(m["fwd_cnt"][b * nq + qt] for b in range(w.B) for qt in range(r0 // 128, nq)))
     flops = 3.5 * tiles * w.Hkv * 4 * 128 * 128 * w.D

@@ -11,8 +11,11 @@
 // 2. classify_rows: one block per (b, qt).  Tiles whose class follows
 //    exactly from the summaries (disjoint segment ranges; one common segment,
 //    where the causal predicate reduces to comparing position ranges) are
-//    classified from them; the rest -- and, with the non-causal ring's local
-//    mask, every tile not already empty -- are counted pair by pair.  The block then
+//    classified from them, the rest pair by pair.  With the non-causal ring's
+//    local mask, each 128 x 128 block of the mask is classified once first;
+//    a tile is then empty if either class is, takes the mask's class where
+//    every pair passes the other rules, and is counted pair by pair only
+//    where both are partial.  The block then
 //    compacts the non-empty kt of its row into fwd_idx and records where the
 //    tiles of each KV shard begin in that list (fwd_shard).
 // 3. columns: one block per (b, kt) compacts the non-empty qt into bwd_idx.
@@ -85,9 +88,39 @@ __device__ __forceinline__ int classify_fast(const TileSum &q, const TileSum &k,
 
 constexpr int kCls = 256; // threads of classify / column kernels
 
+// grid (tq, tk): class of one 128 x 128 block of the non-causal ring's local
+// mask (lq_s x lk_s bytes, nonzero = visible); the mask repeats over every
+// shard pair, so tile (qt, kt) sees local block (qt mod tq, kt mod tk).
+__global__ void __launch_bounds__(kCls) local_tile_kernel(const uint8_t *__restrict__ m, int lk_s,
+                                                          int tk, uint8_t *__restrict__ lcls)
+{
+    const int lt = blockIdx.x, kt = blockIdx.y;
+    int cnt = 0;
+    // 128 rows of 128 bytes = 8 uint4 per row
+    for (int e = threadIdx.x; e < kTile * 8; e += kCls) {
+        const int i = e >> 3, c16 = e & 7;
+        const uint4 v = *reinterpret_cast<const uint4 *>(
+            m + (size_t)(lt * kTile + i) * lk_s + (size_t)kt * kTile + c16 * 16);
+        // __vcmpne4 gives 0xff in every nonzero byte
+        cnt += (__popc(__vcmpne4(v.x, 0u)) + __popc(__vcmpne4(v.y, 0u)) +
+                __popc(__vcmpne4(v.z, 0u)) + __popc(__vcmpne4(v.w, 0u))) >> 3;
+    }
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    __shared__ int red[kCls / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cnt;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int t = 0;
+        for (int w = 0; w < kCls / 32; ++w) t += red[w];
+        lcls[(size_t)lt * tk + kt] =
+            (uint8_t)(t == 0 ? RA_TILE_EMPTY : (t == kTile * kTile ? RA_TILE_FULL : RA_TILE_PARTIAL));
+    }
+}
+
 // grid (nq, B)
 __global__ void __launch_bounds__(kCls) classify_rows_kernel(Problem p, const TileSum *qsum,
-                                                             const TileSum *ksum, uint8_t *cls,
+                                                             const TileSum *ksum,
+                                                             const uint8_t *lcls, uint8_t *cls,
                                                              int32_t *fwd_cnt, int32_t *fwd_idx,
                                                              int32_t *fwd_shard)
 {
@@ -110,9 +143,13 @@ __global__ void __launch_bounds__(kCls) classify_rows_kernel(Problem p, const Ti
         __syncthreads();
         for (int kt = k0 + threadIdx.x; kt < kend; kt += kCls) {
             int c = classify_fast(qs, ksum[(size_t)b * nk + kt], p.causal);
-            // a local mask can only remove pairs: tiles not already empty are
-            // counted pair by pair
-            if (p.local_mask && c != RA_TILE_EMPTY) c = -1;
+            if (p.local_mask && c != RA_TILE_EMPTY) {
+                // the local mask can only remove pairs
+                const int lc = lcls[(size_t)(qt % p.tq) * p.tk + (kt % p.tk)];
+                if (lc == RA_TILE_EMPTY) c = RA_TILE_EMPTY;
+                else if (c == RA_TILE_FULL) c = lc; // every pair passes the other rules
+                else if (lc != RA_TILE_FULL) c = -1; // both partial (or unknown): count pairs
+            }
             if (c < 0) {
                 slow[atomicAdd(&nslow, 1)] = kt;
             } else {
@@ -282,9 +319,10 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t *cnt, int R, 
 
 } // namespace
 
-size_t mask_scratch_ints(int B, int nq, int nk)
+size_t mask_scratch_ints(int B, int nq, int nk, int N)
 {
-    return (size_t)B * (nq + nk) * (sizeof(TileSum) / sizeof(int32_t));
+    const size_t local_tiles = (size_t)(nq / N) * (nk / N); // one byte each
+    return (size_t)B * (nq + nk) * (sizeof(TileSum) / sizeof(int32_t)) + (local_tiles + 3) / 4;
 }
 
 cudaError_t launch_mask_build(const Problem &p, uint8_t *cls, int32_t *fwd_cnt, int32_t *fwd_idx,
@@ -294,10 +332,13 @@ cudaError_t launch_mask_build(const Problem &p, uint8_t *cls, int32_t *fwd_cnt, 
 {
     TileSum *qsum = reinterpret_cast<TileSum *>(scratch);
     TileSum *ksum = qsum + (size_t)p.B * p.nq;
+    uint8_t *lcls = reinterpret_cast<uint8_t *>(ksum + (size_t)p.B * p.nk);
     tile_summary_kernel<<<dim3(p.nq, p.B), 128, 0, s>>>(p.q_seg, p.q_pos, p.Lq, p.pad_id, qsum);
     tile_summary_kernel<<<dim3(p.nk, p.B), 128, 0, s>>>(p.kv_seg, p.kv_pos, p.Lkv, p.pad_id, ksum);
-    classify_rows_kernel<<<dim3(p.nq, p.B), kCls, 0, s>>>(p, qsum, ksum, cls, fwd_cnt, fwd_idx,
-                                                          fwd_shard);
+    if (p.local_mask)
+        local_tile_kernel<<<dim3(p.tq, p.tk), kCls, 0, s>>>(p.local_mask, p.lk_s, p.tk, lcls);
+    classify_rows_kernel<<<dim3(p.nq, p.B), kCls, 0, s>>>(p, qsum, ksum, lcls, cls, fwd_cnt,
+                                                          fwd_idx, fwd_shard);
     columns_kernel<<<dim3(p.nk, p.B), kCls, 0, s>>>(cls, p.nq, p.nk, bwd_cnt, bwd_idx);
     const size_t sm_f = sizeof(int) * ((size_t)p.nk + 1 + 1024);
     const size_t sm_b = sizeof(int) * ((size_t)p.nq + 1 + 1024);

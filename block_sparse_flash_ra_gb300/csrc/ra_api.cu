@@ -173,7 +173,7 @@ MaskLayout mask_layout(const ra_attn_params *p)
     m.fwd_order = o; o += up256(4 * B * nq);
     m.bwd_order = o; o += up256(4 * B * nk);
     m.fwd_shard = o; o += up256(4 * B * nq * ((size_t)p->n_virtual_shards + 1));
-    m.scratch = o;   o += up256(4 * mask_scratch_ints((int)B, (int)nq, (int)nk));
+    m.scratch = o;   o += up256(4 * mask_scratch_ints((int)B, (int)nq, (int)nk, p->n_virtual_shards));
     m.total = o;
     return m;
 }
@@ -309,7 +309,7 @@ RA_API int ra_build_block_mask(const ra_attn_params *p, void *buf, size_t buf_by
                                       reinterpret_cast<int32_t *>(b + L.scratch),
                                       reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "mask build launch");
-    count(6);
+    count(p->local_mask ? 7 : 6);
     *out = m;
     return RA_OK;
 }

@@ -42,7 +42,7 @@ cudaError_t launch_mask_build(const Problem &p, uint8_t *cls, int32_t *fwd_cnt, 
                               int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order,
                               int32_t *bwd_order, int32_t *fwd_shard, int32_t *scratch,
                               cudaStream_t s);
-size_t mask_scratch_ints(int B, int nq, int nk);
+size_t mask_scratch_ints(int B, int nq, int nk, int N);
 cudaError_t launch_merge(float *out, float *lse, const float *bout, const float *blse, int B,
                          int L, int H, int D, cudaStream_t s);
 cudaError_t launch_fwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,

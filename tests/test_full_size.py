@@ -55,7 +55,8 @@ def run_gpu(w, inp):
     p = ra.make_params(d["q"], d["k"], scale=w.scale, causal=w.causal, soft_cap=w.soft_cap,
                        n_virtual_shards=N, is_mqa=w.is_mqa, q_pos=d["q_pos"],
                        kv_pos=d["kv_pos"], q_seg=d["q_seg"], kv_seg=d["kv_seg"],
-                       sinks=d["sinks"], pad_segment_id=PAD_SEGMENT_ID)
+                       sinks=d["sinks"], pad_segment_id=PAD_SEGMENT_ID,
+                       local_mask=d["local_mask"])
     m = ra.build_mask(p)
     out, lse = ra.forward(p, d["q"], d["k"], d["v"], m)
     grads = None
@@ -79,7 +80,8 @@ def oracle_kw(w, inp):
     return dict(scale=w.scale, soft_cap=w.soft_cap or None, causal=w.causal,
                 q_pos=i32(inp["q_pos"]), kv_pos=i32(inp["kv_pos"]),
                 q_seg=i32(inp["q_seg"]), kv_seg=i32(inp["kv_seg"]),
-                sinks=f64(inp["sinks"]), pad_segment_id=PAD_SEGMENT_ID)
+                sinks=f64(inp["sinks"]), pad_segment_id=PAD_SEGMENT_ID,
+                local_mask=None if inp["local_mask"] is None else inp["local_mask"].numpy())
 
 
 def check_rows(got, w, q, k, v, kw, heads, rows):
@@ -94,7 +96,7 @@ def check_rows(got, w, q, k, v, kw, heads, rows):
     assert np.max(np.abs(o - o_r)) <= O_TOL, (w.name, heads, rows)
 
 
-FWD = ["gqa8k", "mqa32k", "packed16k", "long64k", "gqa32k"]
+FWD = ["gqa8k", "mqa32k", "packed16k", "long64k", "gqa32k", "local8k"]
 
 
 @pytest.mark.parametrize("name", FWD)
@@ -128,7 +130,7 @@ def _grad_rows(w, inp):
     return (w.L - 128, w.L), None
 
 
-BWD = ["packed16k", "long64k", "gqa32k"]
+BWD = ["packed16k", "long64k", "gqa32k", "local8k"]
 
 
 @pytest.mark.parametrize("name", BWD)
@@ -138,11 +140,30 @@ def test_full_size_backward_sampled_rows(name):
     got = run_gpu(w, inp)
     q, k, v, do = f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["dout"])
     kw = oracle_kw(w, inp)
-    rows, batch = _grad_rows(w, inp)
     G = w.Hq // w.Hkv
     heads = (0, G)  # every query head of kv head 0
+    hs = slice(*heads)
+    if w.local_window:
+        # keys at local index < 128 of every shard are seen only by query rows
+        # at local index < 128 + window, in every shard: sum the oracle over
+        # those row ranges (each restricted call adds its rows' contributions)
+        ls = w.L // w.n_shards
+        span = 128 + w.local_window
+        dk = dv = 0.0
+        for s in range(w.n_shards):
+            rows = (s * ls, s * ls + span)
+            dq_s, dk_s, dv_s, _, _, _ = oracle.attn_bwd(q, k, v, do, heads=heads, rows=rows, **kw)
+            rs = slice(*rows)
+            assert rel_l2(got["dq"][:, rs, hs], dq_s[:, rs, hs]) <= GRAD_TOL
+            dk = dk + dk_s
+            dv = dv + dv_s
+        keys = np.concatenate([np.arange(s * ls, s * ls + 128) for s in range(w.n_shards)])
+        assert rel_l2(got["dk"][:, keys, 0:1], dk[:, keys, 0:1]) <= GRAD_TOL
+        assert rel_l2(got["dv"][:, keys, 0:1], dv[:, keys, 0:1]) <= GRAD_TOL
+        return
+    rows, batch = _grad_rows(w, inp)
     dq, dk, dv, _, _, _ = oracle.attn_bwd(q, k, v, do, heads=heads, rows=rows, **kw)
-    rs, hs = slice(*rows), slice(*heads)
+    rs = slice(*rows)
     bs = slice(None) if batch is None else slice(batch, batch + 1)
     assert rel_l2(got["dq"][:, rs, hs], dq[:, rs, hs]) <= GRAD_TOL
     assert rel_l2(got["dk"][bs, rs, 0:1], dk[bs, rs, 0:1]) <= GRAD_TOL

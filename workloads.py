@@ -20,6 +20,9 @@ q, k, v, dO, sinks, document lengths, then cast to the workload dtype):
 * ``long64k``   B1 Hq8 Hkv2 L65536 D128 bf16, causal, 8 shards, zigzag, dO.
 * ``gqa32k``    B1 Hq32 Hkv8 L32768 D128 bf16, causal, 8 shards, zigzag, dO --
   the 32K causal GQA workload the throughput target is quoted on.
+* ``local8k``   B1 Hq32 Hkv8 L8192 D128 bf16, non-causal, 4 shards, dO, with
+  the per-shard local mask of the non-causal ring: a band |i - j| < 512 in
+  local (within-shard) coordinates, applied to every shard pair.
 
 The seed of a named workload is its index in the list above.  Positions are
 always produced in the original token order; a permuted run permutes them
@@ -54,6 +57,7 @@ class Workload:
     doc_len: tuple = (128, 4096)
     pad_frac_den: int = 20       # last L // pad_frac_den tokens are padding
     backward: bool = False
+    local_window: int = 0        # > 0: per-shard local band mask |i - j| < window (non-causal)
     seed: int = 0
     extra: dict = field(default_factory=dict)
 
@@ -82,6 +86,8 @@ WORKLOADS = {
                  seed=4),
         Workload("gqa32k", 1, 32768, 32, 8, 128, n_shards=8, zigzag=True, backward=True,
                  seed=5),
+        Workload("local8k", 1, 8192, 32, 8, 128, causal=False, n_shards=4, local_window=512,
+                 backward=True, seed=6),
     ]
 }
 
@@ -131,9 +137,16 @@ def make_inputs(w: Workload, *, device="cpu", with_dout=None):
         # explicit positions so that they can travel with the permuted tokens
         ar = torch.arange(w.L, dtype=torch.int32).unsqueeze(0).repeat(w.B, 1)
         q_pos, kv_pos = ar, ar.clone()
+    local_mask = None
+    if w.local_window:
+        # the non-causal ring's per-shard mask: a band in local coordinates
+        ls = w.L // w.n_shards
+        i = torch.arange(ls).unsqueeze(1)
+        j = torch.arange(ls).unsqueeze(0)
+        local_mask = ((i - j).abs() < w.local_window).to(torch.uint8)
     out = dict(q=q.to(dt), k=k.to(dt), v=v.to(dt),
                dout=None if dout is None else dout.to(dt), sinks=sinks,
-               q_pos=q_pos, kv_pos=kv_pos, q_seg=q_seg, kv_seg=kv_seg)
+               q_pos=q_pos, kv_pos=kv_pos, q_seg=q_seg, kv_seg=kv_seg, local_mask=local_mask)
     if device != "cpu":
         out = {n: (t.to(device) if isinstance(t, torch.Tensor) else t) for n, t in out.items()}
     return out
