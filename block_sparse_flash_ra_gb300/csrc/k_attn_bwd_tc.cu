@@ -408,25 +408,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const float4 *l4 = reinterpret_cast<const float4 *>(lse_s);
                         uint32_t pk[32];
                         if (cap > 0.f) {
+                            float xa = 0.f;
 #pragma unroll
-                            for (int j = 0; j < 64; j += 4) {
-                                const float4 lv = l4[j >> 2];
-                                const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-                                float pr[4], cr[4];
+                            for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
+                            // one loop per tanh form, chosen once per tile (warp-uniform)
+                            auto capped = [&](auto tanh_fn) {
 #pragma unroll
-                                for (int z = 0; z < 4; ++z) {
-                                    const int c = j + z;
-                                    const float t = tanh_fast(s[c] * scale_over_cap);
-                                    float e = ex2_approx(fmaf(cap2, t, la[z]));
-                                    e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
-                                    pr[z] = e;
-                                    cr[z] = e * (1.f - t * t);
+                                for (int j = 0; j < 64; j += 4) {
+                                    const float4 lv = l4[j >> 2];
+                                    const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+                                    float pr[4], cr[4];
+#pragma unroll
+                                    for (int z = 0; z < 4; ++z) {
+                                        const int c = j + z;
+                                        const float t = tanh_fn(s[c] * scale_over_cap);
+                                        float e = ex2_approx(fmaf(cap2, t, la[z]));
+                                        e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
+                                        pr[z] = e;
+                                        cr[z] = e * (1.f - t * t);
+                                    }
+                                    pk[j >> 1] = pack_bf16x2(pr[0], pr[1]);
+                                    pk[(j >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
+                                    pc[j >> 1] = pack_bf16x2(cr[0], cr[1]);
+                                    pc[(j >> 1) + 1] = pack_bf16x2(cr[2], cr[3]);
                                 }
-                                pk[j >> 1] = pack_bf16x2(pr[0], pr[1]);
-                                pk[(j >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
-                                pc[j >> 1] = pack_bf16x2(cr[0], cr[1]);
-                                pc[(j >> 1) + 1] = pack_bf16x2(cr[2], cr[3]);
-                            }
+                            };
+                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall))
+                                capped([](float x) { return tanh_small(x); });
+                            else
+                                capped([](float x) { return tanh_fast(x); });
                         } else {
                             // masked logits -> -inf, so that 2^(...) = 0 below
                             if (partial) {
@@ -830,19 +840,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tmem_ld32(lane_base + c0 + 32, s + 32);
                         tmem_ld_wait();
                         if (cap > 0.f) {
+                            float xa = 0.f;
 #pragma unroll
-                            for (int j = 0; j < 64; j += 2) {
-                                float cv[2];
+                            for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
+                            // one loop per tanh form, chosen once per tile (warp-uniform)
+                            auto capped = [&](auto tanh_fn) {
 #pragma unroll
-                                for (int z = 0; z < 2; ++z) {
-                                    const int c = j + z;
-                                    const float t = tanh_fast(s[c] * scale_over_cap);
-                                    float e = ex2_approx(fmaf(cap2, t, nl2));
-                                    e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
-                                    cv[z] = e * (1.f - t * t);
+                                for (int j = 0; j < 64; j += 2) {
+                                    float cv[2];
+#pragma unroll
+                                    for (int z = 0; z < 2; ++z) {
+                                        const int c = j + z;
+                                        const float t = tanh_fn(s[c] * scale_over_cap);
+                                        float e = ex2_approx(fmaf(cap2, t, nl2));
+                                        e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
+                                        cv[z] = e * (1.f - t * t);
+                                    }
+                                    pc[j >> 1] = pack_bf16x2(cv[0], cv[1]);
                                 }
-                                pc[j >> 1] = pack_bf16x2(cv[0], cv[1]);
-                            }
+                            };
+                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall))
+                                capped([](float x) { return tanh_small(x); });
+                            else
+                                capped([](float x) { return tanh_fast(x); });
                         } else {
                             // masked logits -> -inf, so that 2^(...) = 0 below
                             if (partial) {

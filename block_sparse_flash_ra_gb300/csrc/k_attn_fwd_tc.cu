@@ -422,8 +422,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         // with a soft cap the logits are formed here in log2 units;
                         // without one s stays raw and the scale rides in the exponent
                         if (cap > 0.f) {
+                            float xa = 0.f;
 #pragma unroll
-                            for (int j = 0; j < 64; ++j) s[j] = cap2 * tanh_fast(s[j] * scale_over_cap);
+                            for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
+                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
+                                // cap * log2 e * tanh(x), x = s / cap * scale, on the FMA pipe:
+                                // x * (d1 + x^2 (d3 + x^2 (d5 + x^2 d7))), d = cap2 * c
+                                const float2 k2 = make_float2(scale_over_cap, scale_over_cap);
+                                const float2 d7 = make_float2(cap2 * kTanhC7, cap2 * kTanhC7);
+                                const float2 d5 = make_float2(cap2 * kTanhC5, cap2 * kTanhC5);
+                                const float2 d3 = make_float2(cap2 * kTanhC3, cap2 * kTanhC3);
+                                const float2 d1 = make_float2(cap2, cap2);
+#pragma unroll
+                                for (int j = 0; j < 64; j += 2) {
+                                    const float2 x = fmul2(make_float2(s[j], s[j + 1]), k2);
+                                    const float2 x2 = fmul2(x, x);
+                                    float2 pp = ffma2(x2, d7, d5);
+                                    pp = ffma2(x2, pp, d3);
+                                    pp = ffma2(x2, pp, d1);
+                                    const float2 r = fmul2(x, pp);
+                                    s[j] = r.x;
+                                    s[j + 1] = r.y;
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 64; ++j) s[j] = cap2 * tanh_fast(s[j] * scale_over_cap);
+                            }
                         }
                         if (partial) {
 #pragma unroll
