@@ -832,8 +832,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (partial) row_visibility(p, x.b, kt * kTile + c0, qi, my_seg, my_pad, my_pos, vis);
                     if (!(ok = wait_all(bars.s_full, g & 1))) break;
                     tc_fence_after();
-                    // ---- phase A: Pc = P * (1 - tanh^2), packed bf16 (P from S)
-                    uint32_t pc[32];
+                    // ---- phase A: Pc = P * (1 - tanh^2) in fp32 registers (P from S)
+                    float pf[64];
                     {
                         float s[64];
                         tmem_ld32(lane_base + c0, s);
@@ -856,7 +856,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                         e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
                                         cv[z] = e * (1.f - t * t);
                                     }
-                                    pc[j >> 1] = pack_bf16x2(cv[0], cv[1]);
+                                    pf[j] = cv[0];
+                                    pf[j + 1] = cv[1];
                                 }
                             };
                             if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall))
@@ -875,7 +876,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                             for (int j = 0; j < 64; j += 2) {
                                 const float2 x2 = ffma2(make_float2(s[j], s[j + 1]), sc2, nl22);
-                                pc[j >> 1] = pack_bf16x2(ex2_approx(x2.x), ex2_approx(x2.y));
+                                pf[j] = ex2_approx(x2.x);
+                                pf[j + 1] = ex2_approx(x2.y);
                             }
                         }
                     }
@@ -894,7 +896,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const float2 dl2 = make_float2(dl, dl);
 #pragma unroll
                         for (int j = 0; j < 64; j += 2) {
-                            const float2 r = fmul2(unpack_bf16x2(pc[j >> 1]),
+                            const float2 r = fmul2(make_float2(pf[j], pf[j + 1]),
                                                    fsub2(make_float2(dpv[j], dpv[j + 1]), dl2));
                             pk[j >> 1] = pack_bf16x2(r.x, r.y);
                         }
