@@ -9,6 +9,8 @@ every query row that can see that key lies inside the set (the last rows of a
 causal sequence, or the rows of one whole document).  Bars as in the small
 parity tests: O max-abs 2e-2, lse max-abs 1e-3, gradients relative L2 1e-2.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -201,3 +203,27 @@ def test_full_size_block_map_and_permutation_bit_exact():
                bwd_order=dev_arr(m.bwd_order, nk, torch.int32))
     for key, val in got.items():
         assert np.array_equal(val.reshape(-1), np.asarray(ref[key]).reshape(-1)), key
+
+
+def test_maximum_sequence_length_forward_sampled_rows():
+    # the longest sequence the library accepts (2^20 tokens), one head, D = 64
+    L = 1 << 20
+    g = torch.Generator().manual_seed(71)
+    q, k, v = (torch.randn((1, L, 1, 64), generator=g).to(torch.bfloat16) for _ in range(3))
+    dq_, dk_, dv_ = q.cuda(), k.cuda(), v.cuda()
+    scale = 0.125
+    p = ra.make_params(dq_, dk_, scale=scale, causal=True, n_virtual_shards=2)
+    m = ra.build_mask(p)
+    out, lse = ra.forward(p, dq_, dk_, dv_, m)
+    torch.cuda.synchronize()
+    assert ra.ra_get_device_status() == ra.RA_OK
+    o, l = f64(out), f64(lse)
+    q64, k64, v64 = f64(q), f64(k), f64(v)
+    for rows in ((0, 16), (L // 2 - 8, L // 2 + 8), (L - 16, L)):
+        o_ref, l_ref = oracle.attn_fwd(q64, k64, v64, scale=scale, causal=True, rows=rows)
+        rs = slice(*rows)
+        assert np.max(np.abs(l[:, :, rs] - l_ref[:, :, rs])) <= LSE_TOL, rows
+        assert np.max(np.abs(o[:, rs] - o_ref[:, rs])) <= O_TOL, rows
+    # the next admissible length above the limit is refused
+    p2 = ra.RaAttnParams(1, L + 256, L + 256, 1, 1, 64, ra.RA_BF16, scale, 0.0, 1, 0, 2, -1)
+    assert ra.lib().ra_block_mask_bytes(ctypes.byref(p2)) == 0

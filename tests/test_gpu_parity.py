@@ -277,6 +277,8 @@ BWD_CASES = {
     "mqa_sinks_cap": W(Hq=4, Hkv=1, is_mqa=True, sinks=True, soft_cap=5.0, L=512, seed=32),
     "noncausal": W(causal=False, L=512, seed=33),
     "d64_zigzag": W(D=64, L=512, zigzag=True, n_shards=2, seed=34),
+    "mqa_sinks_cap50": W(Hq=4, Hkv=1, is_mqa=True, sinks=True, soft_cap=50.0, L=512, seed=37),
+    "ragged_n5_b2": W(B=2, Hq=6, Hkv=2, L=640, n_shards=5, seed=38),
 }
 
 
