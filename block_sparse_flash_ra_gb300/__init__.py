@@ -69,8 +69,11 @@ class RaBlockMask(ctypes.Structure):
         ("tile_class", ctypes.c_void_p), ("fwd_cnt", ctypes.c_void_p),
         ("fwd_idx", ctypes.c_void_p), ("bwd_cnt", ctypes.c_void_p),
         ("bwd_idx", ctypes.c_void_p), ("fwd_order", ctypes.c_void_p),
-        ("bwd_order", ctypes.c_void_p), ("fwd_shard", ctypes.c_void_p), ("B", ctypes.c_int),
-        ("nq", ctypes.c_int), ("nk", ctypes.c_int), ("n_shards", ctypes.c_int),
+        ("bwd_order", ctypes.c_void_p), ("fwd_shard", ctypes.c_void_p),
+        ("part_fwd", ctypes.c_void_p), ("part_bwd", ctypes.c_void_p),
+        ("part_rows", ctypes.c_void_p), ("part_cols", ctypes.c_void_p),
+        ("n_part", ctypes.c_void_p), ("B", ctypes.c_int), ("nq", ctypes.c_int),
+        ("nk", ctypes.c_int), ("n_shards", ctypes.c_int), ("part_cap", ctypes.c_int),
         ("key", ctypes.c_uint64),
     ]
 

@@ -45,73 +45,6 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kBwdThreads = 320;
 
-// Visibility bits of query rows q0..q0+63 for one kv row (dkdv: bit c of
-// word c/32 = query row q0+c sees this kv row).
-__device__ __forceinline__ void col_visibility(const Problem &p, int b, int q0, int kj, int kv_seg,
-                                               int kv_pos, uint32_t vis[2])
-{
-    const int4 *qp4 = p.q_pos ? reinterpret_cast<const int4 *>(p.q_pos + (size_t)b * p.Lq + q0) : nullptr;
-    const int4 *qs4 = p.q_seg ? reinterpret_cast<const int4 *>(p.q_seg + (size_t)b * p.Lq + q0) : nullptr;
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-        uint32_t bits = 0;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            const int c = w * 32 + jj * 4;
-            const int4 pv = qp4 ? __ldg(qp4 + (c >> 2)) : make_int4(q0 + c, q0 + c + 1, q0 + c + 2, q0 + c + 3);
-            const int4 sv = qs4 ? __ldg(qs4 + (c >> 2)) : make_int4(0, 0, 0, 0);
-            const int pa[4] = {pv.x, pv.y, pv.z, pv.w};
-            const int sa[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                bool v = (sa[z] == kv_seg) && !(p.q_seg && sa[z] == p.pad_id);
-                if (p.causal) v = v && (pa[z] >= kv_pos);
-                bits |= (v ? 1u : 0u) << (jj * 4 + z);
-            }
-        }
-        vis[w] = bits;
-    }
-    if (p.local_mask) {
-        uint32_t lb[2];
-        local_col_bits(p, q0, kj, lb);
-        vis[0] &= lb[0];
-        vis[1] &= lb[1];
-    }
-}
-
-// Visibility bits of kv rows k0..k0+63 for one query row (dq).
-__device__ __forceinline__ void row_visibility(const Problem &p, int b, int k0, int qi, int q_seg,
-                                               bool q_pad, int q_pos, uint32_t vis[2])
-{
-    const int4 *kp4 = p.kv_pos ? reinterpret_cast<const int4 *>(p.kv_pos + (size_t)b * p.Lkv + k0) : nullptr;
-    const int4 *ks4 = p.kv_seg ? reinterpret_cast<const int4 *>(p.kv_seg + (size_t)b * p.Lkv + k0) : nullptr;
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-        uint32_t bits = 0;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            const int c = w * 32 + jj * 4;
-            const int4 pv = kp4 ? __ldg(kp4 + (c >> 2)) : make_int4(k0 + c, k0 + c + 1, k0 + c + 2, k0 + c + 3);
-            const int4 sv = ks4 ? __ldg(ks4 + (c >> 2)) : make_int4(0, 0, 0, 0);
-            const int pa[4] = {pv.x, pv.y, pv.z, pv.w};
-            const int sa[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                bool v = (sa[z] == q_seg) && !q_pad;
-                if (p.causal) v = v && (q_pos >= pa[z]);
-                bits |= (v ? 1u : 0u) << (jj * 4 + z);
-            }
-        }
-        vis[w] = bits;
-    }
-    if (p.local_mask) {
-        uint32_t lb[2];
-        local_row_bits(p, qi, k0, lb);
-        vis[0] &= lb[0];
-        vis[1] &= lb[1];
-    }
-}
-
 // ====================================================================== dkdv
 template <int D>
 struct DkdvCfg {
@@ -385,8 +318,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int my_pos = p.kv_pos ? p.kv_pos[(size_t)x.b * p.Lkv + kj] : kj;
                 const int my_seg = p.kv_seg ? p.kv_seg[(size_t)x.b * p.Lkv + kj] : 0;
                 const int steps = p.G * x.cnt;
+                // column-order number of the next partial tile (restarts with each head)
+                const int pbase = p.part_bwd[x.col];
+                int pslot = pbase;
                 for (int i = 0; i < steps; ++i, ++n) {
-                    const int qt = x.list[i % x.cnt];
+                    const int e = i % x.cnt;
+                    if (e == 0) pslot = pbase;
+                    const int qt = x.list[e];
                     const int st = n % C::kStages;
                     const float *lse_s = reinterpret_cast<const float *>(
                         smem + C::kStageOff + st * C::kStageBytes + 2 * C::kTileBytes) + c0;
@@ -395,7 +333,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         p.tile_class[((size_t)x.b * p.nq + qt) * p.nk + x.kt] == RA_TILE_PARTIAL;
                     // ---- visibility bits of this half's 64 query columns (partial tiles only)
                     uint32_t vis[2] = {~0u, ~0u};
-                    if (partial) col_visibility(p, x.b, qt * kTile + c0, kj, my_seg, my_pos, vis);
+                    if (partial) {
+                        const uint2 vb = col_bits(p, pslot++, row, wg, x.b, qt * kTile + c0, kj, my_seg,
+                                                  my_pos);
+                        vis[0] = vb.x;
+                        vis[1] = vb.y;
+                    }
                     if (!(ok = wait_all(bars.s_full, n & 1))) break;
                     tc_fence_after();
                     // ---- P^T (bf16 -> TMEM) and Pc = P * (1 - tanh^2) kept packed
@@ -825,11 +768,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int my_seg = p.q_seg ? p.q_seg[(size_t)x.b * p.Lq + qi] : 0;
                 const bool my_pad = p.q_seg && my_seg == p.pad_id;
                 const uint8_t *crow = p.tile_class + (size_t)x.row * p.nk;
+                // row-order number of the next partial tile
+                int pslot = p.part_fwd[(size_t)x.row * (p.N + 1)];
                 for (int e = 0; e < x.cnt; ++e, ++g) {
                     const int kt = x.list[e];
                     const bool partial = crow[kt] == RA_TILE_PARTIAL;
                     uint32_t vis[2] = {~0u, ~0u};
-                    if (partial) row_visibility(p, x.b, kt * kTile + c0, qi, my_seg, my_pad, my_pos, vis);
+                    if (partial) {
+                        const uint2 vb = row_bits(p, pslot++, row, wg, x.b, kt * kTile + c0, qi, my_seg,
+                                                  my_pad, my_pos);
+                        vis[0] = vb.x;
+                        vis[1] = vb.y;
+                    }
                     if (!(ok = wait_all(bars.s_full, g & 1))) break;
                     tc_fence_after();
                     // ---- phase A: Pc = P * (1 - tanh^2) in fp32 registers (P from S)

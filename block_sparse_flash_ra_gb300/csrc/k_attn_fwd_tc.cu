@@ -93,6 +93,7 @@ struct Unit {
     int b, qt, h, row, cnt, dev;
     const int32_t *list;
     const int32_t *shard; // N+1 offsets into list: where each KV shard's tiles begin
+    const int32_t *pfwd;  // N+1 row-order numbers of the first partial tile of each shard
 };
 
 __device__ __forceinline__ Unit unit_of(const Problem &p, int u)
@@ -106,6 +107,7 @@ __device__ __forceinline__ Unit unit_of(const Problem &p, int u)
     x.dev = x.qt / p.tq;
     x.list = p.fwd_idx + (size_t)x.row * p.nk;
     x.shard = p.fwd_shard + (size_t)x.row * (p.N + 1);
+    x.pfwd = p.part_fwd + (size_t)x.row * (p.N + 1);
     return x;
 }
 
@@ -357,8 +359,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const bool my_pad = p.q_seg && my_seg == p.pad_id;
                 const uint8_t *crow = p.tile_class + (size_t)x.row * p.nk;
                 for (int t = 0; ok && t < p.N; ++t) {
+                    const int src = (x.dev - t + p.N) % p.N;
                     int lo, hi;
-                    shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
+                    shard_range(p, x, src, lo, hi);
+                    int pslot = x.pfwd[src]; // number of the shard's first partial tile
                     const bool sink_here = has_sink && t == 0;
                     if (lo == hi) {
                         // empty shard: partial is (0, -inf), or (0, sink) at t = 0
@@ -383,35 +387,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         uint32_t vis0 = ~0u, vis1 = ~0u;
                         if (partial) {
                             // visibility of kv columns kt*128 + c0 .. +63 for this row
-                            const int j0 = kt * kTile + c0;
-                            const int4 *kp4 = p.kv_pos
-                                ? reinterpret_cast<const int4 *>(p.kv_pos + (size_t)x.b * p.Lkv + j0) : nullptr;
-                            const int4 *ks4 = p.kv_seg
-                                ? reinterpret_cast<const int4 *>(p.kv_seg + (size_t)x.b * p.Lkv + j0) : nullptr;
-                            uint32_t bits[2] = {0u, 0u};
-#pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) {
-                                const int4 pv = kp4 ? __ldg(kp4 + jj)
-                                                    : make_int4(j0 + 4 * jj, j0 + 4 * jj + 1,
-                                                                j0 + 4 * jj + 2, j0 + 4 * jj + 3);
-                                const int4 sv = ks4 ? __ldg(ks4 + jj) : make_int4(0, 0, 0, 0);
-                                const int pa[4] = {pv.x, pv.y, pv.z, pv.w};
-                                const int sa[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-                                for (int z = 0; z < 4; ++z) {
-                                    bool vis = (sa[z] == my_seg) && !my_pad;
-                                    if (p.causal) vis = vis && (my_pos >= pa[z]);
-                                    bits[jj >> 3] |= (vis ? 1u : 0u) << ((4 * jj + z) & 31);
-                                }
-                            }
-                            if (p.local_mask) {
-                                uint32_t lb[2];
-                                local_row_bits(p, qi, j0, lb);
-                                bits[0] &= lb[0];
-                                bits[1] &= lb[1];
-                            }
-                            vis0 = bits[0];
-                            vis1 = bits[1];
+                            const uint2 vb = row_bits(p, pslot++, row, wg, x.b, kt * kTile + c0, qi,
+                                                      my_seg, my_pad, my_pos);
+                            vis0 = vb.x;
+                            vis1 = vb.y;
                         }
                         if (!(ok = wait_all(bars.s_full + sb, (g >> 1) & 1))) break;
                         tc_fence_after();

@@ -155,7 +155,8 @@ uint64_t mask_key(const ra_attn_params *p)
 }
 
 struct MaskLayout {
-    size_t cls, fwd_cnt, fwd_idx, bwd_cnt, bwd_idx, fwd_order, bwd_order, fwd_shard, scratch, total;
+    size_t cls, fwd_cnt, fwd_idx, bwd_cnt, bwd_idx, fwd_order, bwd_order, fwd_shard, part_fwd,
+        part_bwd, part_rows, part_cols, n_part, scratch, total;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -173,6 +174,12 @@ MaskLayout mask_layout(const ra_attn_params *p)
     m.fwd_order = o; o += up256(4 * B * nq);
     m.bwd_order = o; o += up256(4 * B * nk);
     m.fwd_shard = o; o += up256(4 * B * nq * ((size_t)p->n_virtual_shards + 1));
+    m.part_fwd = o;  o += up256(4 * B * nq * ((size_t)p->n_virtual_shards + 1));
+    m.part_bwd = o;  o += up256(4 * B * nk);
+    const size_t cap = (size_t)mask_part_cap((int)B, (int)nq, (int)nk);
+    m.part_rows = o; o += up256(cap * RA_TILE * 16);
+    m.part_cols = o; o += up256(cap * RA_TILE * 16);
+    m.n_part = o;    o += 256;
     m.scratch = o;   o += up256(4 * mask_scratch_ints((int)B, (int)nq, (int)nk, p->n_virtual_shards));
     m.total = o;
     return m;
@@ -214,6 +221,11 @@ Problem make_problem(const ra_attn_params *p, const ra_block_mask *m, int *statu
         x.fwd_order = m->fwd_order;
         x.bwd_order = m->bwd_order;
         x.fwd_shard = m->fwd_shard;
+        x.part_fwd = m->part_fwd;
+        x.part_bwd = m->part_bwd;
+        x.part_rows = m->part_rows;
+        x.part_cols = m->part_cols;
+        x.part_cap = m->part_cap;
     }
     x.status = status;
     x.timeout_ns = g_timeout_ns.load();
@@ -224,10 +236,12 @@ int check_mask(const ra_attn_params *p, const ra_block_mask *m)
 {
     if (!m) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
     if (!m->tile_class || !m->fwd_cnt || !m->fwd_idx || !m->bwd_cnt || !m->bwd_idx ||
-        !m->fwd_order || !m->bwd_order || !m->fwd_shard)
+        !m->fwd_order || !m->bwd_order || !m->fwd_shard || !m->part_fwd || !m->part_bwd ||
+        !m->part_rows || !m->part_cols || !m->n_part)
         return fail(RA_ERR_INVALID_ARG, "mask has NULL arrays (not built?)");
     if (m->B != p->B || m->nq != p->Lq / RA_TILE || m->nk != p->Lkv / RA_TILE ||
-        m->n_shards != p->n_virtual_shards || m->key != mask_key(p))
+        m->n_shards != p->n_virtual_shards || m->key != mask_key(p) ||
+        m->part_cap != mask_part_cap(p->B, p->Lq / RA_TILE, p->Lkv / RA_TILE))
         return fail(RA_ERR_INVALID_ARG, "mask was built for other params (sizes, causal, shards, "
                                         "padding id or pos/seg arrays)");
     return RA_OK;
@@ -298,18 +312,22 @@ RA_API int ra_build_block_mask(const ra_attn_params *p, void *buf, size_t buf_by
     m.fwd_order = reinterpret_cast<int32_t *>(b + L.fwd_order);
     m.bwd_order = reinterpret_cast<int32_t *>(b + L.bwd_order);
     m.fwd_shard = reinterpret_cast<int32_t *>(b + L.fwd_shard);
+    m.part_fwd = reinterpret_cast<int32_t *>(b + L.part_fwd);
+    m.part_bwd = reinterpret_cast<int32_t *>(b + L.part_bwd);
+    m.part_rows = reinterpret_cast<uint32_t *>(b + L.part_rows);
+    m.part_cols = reinterpret_cast<uint32_t *>(b + L.part_cols);
+    m.n_part = reinterpret_cast<int32_t *>(b + L.n_part);
     m.B = p->B;
     m.nq = p->Lq / RA_TILE;
     m.nk = p->Lkv / RA_TILE;
     m.n_shards = p->n_virtual_shards;
+    m.part_cap = mask_part_cap(m.B, m.nq, m.nk);
     m.key = mask_key(p);
     const Problem pr = make_problem(p, nullptr, dc->status);
-    cudaError_t e = launch_mask_build(pr, m.tile_class, m.fwd_cnt, m.fwd_idx, m.bwd_cnt, m.bwd_idx,
-                                      m.fwd_order, m.bwd_order, m.fwd_shard,
-                                      reinterpret_cast<int32_t *>(b + L.scratch),
+    cudaError_t e = launch_mask_build(pr, m, reinterpret_cast<int32_t *>(b + L.scratch),
                                       reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "mask build launch");
-    count(p->local_mask ? 7 : 6);
+    count(kMaskBuildKernels + (p->local_mask ? 1 : 0));
     *out = m;
     return RA_OK;
 }

@@ -30,6 +30,13 @@ struct Problem {
     const uint8_t *tile_class;
     const int32_t *fwd_cnt, *fwd_idx, *bwd_cnt, *bwd_idx, *fwd_order, *bwd_order;
     const int32_t *fwd_shard; // (B*nq, N+1) first fwd_idx position of each KV shard
+    // partial mask blocks: bits of PARTIAL tiles, numbered in row order
+    // (part_fwd: first number at each shard start of a row) and in column
+    // order (part_bwd: first number of each column); numbers >= part_cap have
+    // no block and are masked from positions and segments
+    const int32_t *part_fwd, *part_bwd;
+    const uint32_t *part_rows, *part_cols; // (part_cap, 128, 4) words each
+    int part_cap;
     // failure reporting
     int *status;
     uint64_t timeout_ns;
@@ -38,11 +45,15 @@ struct Problem {
 // ---- launchers (each returns cudaError_t of its launch) -------------------
 cudaError_t launch_permute(const void *in, void *out, int B, int L, size_t row_bytes, int n,
                            int inverse, cudaStream_t s);
-cudaError_t launch_mask_build(const Problem &p, uint8_t *cls, int32_t *fwd_cnt, int32_t *fwd_idx,
-                              int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order,
-                              int32_t *bwd_order, int32_t *fwd_shard, int32_t *scratch,
+// Builds every array of `m` (device pointers) from the problem's positions,
+// segments and local mask; `scratch` holds mask_scratch_ints() ints.
+// Launches kMaskBuildKernels kernels, one more with a local mask.
+cudaError_t launch_mask_build(const Problem &p, const ra_block_mask &m, int32_t *scratch,
                               cudaStream_t s);
+constexpr int kMaskBuildKernels = 9;
 size_t mask_scratch_ints(int B, int nq, int nk, int N);
+// slots of partial mask blocks in a map of B x nq x nk tiles
+int mask_part_cap(int B, int nq, int nk);
 cudaError_t launch_merge(float *out, float *lse, const float *bout, const float *blse, int B,
                          int L, int H, int D, cudaStream_t s);
 cudaError_t launch_fwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,

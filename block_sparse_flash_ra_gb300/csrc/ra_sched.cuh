@@ -55,6 +55,79 @@ __device__ __forceinline__ void local_col_bits(const Problem &p, int q0, int kj,
     }
 }
 
+// Visibility bits of one 64-column half of a PARTIAL tile, in the two forms
+// the kernels need.  A tile numbered below Problem::part_cap reads the block
+// the block map stored (one 8-byte load); a tile past it re-derives the bits
+// from positions, segments and the local mask, in a call kept out of line so
+// that the rarely taken path does not crowd the instruction cache of the hot
+// loops.
+//
+// Row form: bit c of word c / 32 is set iff query row qi sees kv row k0 + c
+// (k0 = kt * 128 + 64 * half).
+static __device__ __noinline__ uint2 row_bits_derived(const Problem p, int b, int k0, int qi, int q_seg,
+                                               int q_pad, int q_pos)
+{
+    const int32_t *kp = p.kv_pos ? p.kv_pos + (size_t)b * p.Lkv + k0 : nullptr;
+    const int32_t *ks = p.kv_seg ? p.kv_seg + (size_t)b * p.Lkv + k0 : nullptr;
+    uint32_t bits[2] = {0u, 0u};
+    for (int c = 0; c < 64; ++c) {
+        const int pos = kp ? __ldg(kp + c) : k0 + c;
+        const int seg = ks ? __ldg(ks + c) : 0;
+        bool v = seg == q_seg && !q_pad;
+        if (p.causal) v = v && q_pos >= pos;
+        if (v) bits[c >> 5] |= 1u << (c & 31);
+    }
+    if (p.local_mask) {
+        uint32_t lb[2];
+        local_row_bits(p, qi, k0, lb);
+        bits[0] &= lb[0];
+        bits[1] &= lb[1];
+    }
+    return make_uint2(bits[0], bits[1]);
+}
+
+__device__ __forceinline__ uint2 row_bits(const Problem &p, int slot, int row, int half, int b,
+                                          int k0, int qi, int q_seg, bool q_pad, int q_pos)
+{
+    if (slot < p.part_cap)
+        return __ldg(reinterpret_cast<const uint2 *>(p.part_rows + ((size_t)slot * kTile + row) * 4) +
+                     half);
+    return row_bits_derived(p, b, k0, qi, q_seg, q_pad ? 1 : 0, q_pos);
+}
+
+// Column form: bit c of word c / 32 is set iff query row q0 + c sees kv row
+// kj (q0 = qt * 128 + 64 * half).
+static __device__ __noinline__ uint2 col_bits_derived(const Problem p, int b, int q0, int kj, int kv_seg,
+                                               int kv_pos)
+{
+    const int32_t *qp = p.q_pos ? p.q_pos + (size_t)b * p.Lq + q0 : nullptr;
+    const int32_t *qs = p.q_seg ? p.q_seg + (size_t)b * p.Lq + q0 : nullptr;
+    uint32_t bits[2] = {0u, 0u};
+    for (int c = 0; c < 64; ++c) {
+        const int pos = qp ? __ldg(qp + c) : q0 + c;
+        const int seg = qs ? __ldg(qs + c) : 0;
+        bool v = seg == kv_seg && !(qs && seg == p.pad_id);
+        if (p.causal) v = v && pos >= kv_pos;
+        if (v) bits[c >> 5] |= 1u << (c & 31);
+    }
+    if (p.local_mask) {
+        uint32_t lb[2];
+        local_col_bits(p, q0, kj, lb);
+        bits[0] &= lb[0];
+        bits[1] &= lb[1];
+    }
+    return make_uint2(bits[0], bits[1]);
+}
+
+__device__ __forceinline__ uint2 col_bits(const Problem &p, int slot, int row, int half, int b,
+                                          int q0, int kj, int kv_seg, int kv_pos)
+{
+    if (slot < p.part_cap)
+        return __ldg(reinterpret_cast<const uint2 *>(p.part_cols + ((size_t)slot * kTile + row) * 4) +
+                     half);
+    return col_bits_derived(p, b, q0, kj, kv_seg, kv_pos);
+}
+
 // Wait used only while tearing down after an abort: bounded, ignores the
 // abort flag.
 __device__ __forceinline__ bool wait_drain(uint64_t *bar, uint32_t parity, uint64_t ns)

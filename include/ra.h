@@ -143,6 +143,26 @@ typedef struct {
  *               kt >= s*nk/N, so KV shard s owns fwd_idx[fwd_shard[s] ..
  *               fwd_shard[s+1]) (entry N = fwd_cnt).  The forward walks a
  *               row's shards in ring order through these offsets.
+ * Partial mask blocks (the pages' MaskInfo partial_mask_blocks): the
+ * visibility bits of PARTIAL tiles, stored once per tile and shared by every
+ * head, so the attention kernels mask a partial tile with one 8-byte load per
+ * thread instead of re-deriving it from positions and segments.  PARTIAL
+ * tiles are numbered twice: in row order (by b*nq+qt, then kt ascending) and
+ * in column order (by b*nk+kt, then qt ascending); the first part_cap of each
+ * numbering have a block, the rest are masked from positions and segments.
+ *   part_fwd    (B*nq, N+1): entry s of a row is the row-order number of the
+ *               first PARTIAL tile at or after fwd_idx position fwd_shard[s]
+ *               of that row (entry 0: the row's first, entry N: one past its
+ *               last).
+ *   part_bwd    (B*nk): column-order number of each column's first PARTIAL
+ *               tile.
+ *   part_rows   (part_cap, 128, 4) uint32, row-order: bit z of word w of row i
+ *               is set iff query row qt*128+i sees kv row kt*128+32w+z.
+ *   part_cols   (part_cap, 128, 4) uint32, column-order: bit z of word w of
+ *               row j is set iff query row qt*128+32w+z sees kv row kt*128+j.
+ *   n_part      (1) int32: PARTIAL tiles in the map (blocks stored:
+ *               min(n_part, part_cap)).
+ *   part_cap    4 * B * (nq + nk).
  *   key         fingerprint of the ra_attn_params fields the map depends on;
  *               attention calls reject a map built for other params.
  */
@@ -155,7 +175,12 @@ typedef struct {
     int32_t *fwd_order;
     int32_t *bwd_order;
     int32_t *fwd_shard;
-    int B, nq, nk, n_shards;
+    int32_t *part_fwd;
+    int32_t *part_bwd;
+    uint32_t *part_rows;
+    uint32_t *part_cols;
+    int32_t *n_part;
+    int B, nq, nk, n_shards, part_cap;
     uint64_t key;
 } ra_block_mask;
 
@@ -176,7 +201,8 @@ RA_API size_t ra_block_mask_bytes(const ra_attn_params *p);
  * the tile lists and schedules (make_ring_attention's forward and dkv
  * MaskInfo; Kvax create_attention_mask with padding-only tiles skipped).
  * Result is bit-exact: a tile is EMPTY iff no pair is visible, FULL iff all
- * 128*128 pairs are, PARTIAL otherwise.
+ * 128*128 pairs are, PARTIAL otherwise; the partial mask blocks hold the
+ * exact visibility bits of the PARTIAL tiles they cover.
  *   buf, buf_bytes  device buffer of at least ra_block_mask_bytes(p) bytes,
  *                   256-byte aligned; owned by the caller and must outlive
  *                   every call that uses `out`.

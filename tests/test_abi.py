@@ -69,7 +69,7 @@ def test_segments_must_come_in_pairs(L):
 
 def test_mask_from_other_params_rejected(L):
     p = _params()
-    m = ra.RaBlockMask(16, 16, 16, 16, 16, 16, 16, 16, 1, 2, 2, 2, 12345)
+    m = ra.RaBlockMask(16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 2, 2, 2, 48, 12345)
     rc = L.ra_attn_fwd(ctypes.byref(p), 16, 16, 16, ctypes.byref(m), 16, 16, None, 0, None)
     assert rc == ra.RA_ERR_INVALID_ARG
     assert "mask" in ra.ra_last_error()
@@ -86,8 +86,10 @@ def test_mask_bytes_cover_every_array(L):
     p = _params(B=2, Lq=512, Lkv=1024, n_virtual_shards=1)
     n = L.ra_block_mask_bytes(ctypes.byref(p))
     nq, nk = 4, 8
+    cap = 4 * 2 * (nq + nk)  # partial mask blocks: 4 B (nq + nk) slots of 2 KB, twice
     need = 2 * nq * nk + 4 * (2 * nq + 2 * nq * nk + 2 * nk + 2 * nk * nq + 2 * nq + 2 * nk
-                              + 2 * nq * 2)  # fwd_shard: N + 1 = 2 offsets per row
+                              + 2 * nq * 2  # fwd_shard: N + 1 = 2 offsets per row
+                              + 2 * nq * 2 + 2 * nk + 1) + 2 * cap * 128 * 16
     assert n >= need
 
 

@@ -12,6 +12,7 @@ import torch
 
 import block_sparse_flash_ra_gb300 as ra
 import oracle
+from tests.brute import visibility
 from workloads import WORKLOADS, Workload, make_inputs, random_structure
 
 pytestmark = pytest.mark.gpu
@@ -144,6 +145,10 @@ STRUCT_CASES = {
     "packed_docs_pad": (W(B=2, seed=21), dict(n_docs_max=5, pad_max=300)),
     "packed_docs_pad_sinks": (W(B=2, seed=22, sinks=True), dict(n_docs_max=4, pad_max=400)),
     "shuffled_positions": (W(seed=23, L=512, n_shards=1), dict(n_docs_max=1, shuffle_positions=True)),
+    # more partial tiles than stored blocks: tiles past the capacity are
+    # masked from positions and segments
+    "shuffled_positions_past_block_capacity": (W(seed=26, L=2048, Hq=2, Hkv=1, n_shards=2),
+                                               dict(n_docs_max=2, shuffle_positions=True)),
     "noncausal_segments": (W(causal=False, seed=24), dict(n_docs_max=6, pad_max=50)),
 }
 
@@ -174,6 +179,51 @@ def test_forward_all_padding_rows_and_empty_tiles():
 
 
 # ------------------------------------------------------------ block map
+def _dev_arr(m, ptr, n, dtype):
+    buf = m._buf
+    off = ptr - buf.data_ptr()
+    nbytes = n * torch.tensor([], dtype=dtype).element_size()
+    return buf[off:off + nbytes].view(dtype).cpu().numpy()
+
+
+def _pack_rows(block):
+    """(128, 128) bool -> (128, 4) uint32, bit z of word w = column 32w + z."""
+    return np.packbits(block, axis=1, bitorder="little").view("<u4")
+
+
+def check_partial_blocks(m, cls, vis, n_shards):
+    """The partial mask blocks against the dense visibility (bit-exact):
+    numbering in row and column order, per-shard first numbers, and the bits
+    of every numbered tile below the capacity."""
+    B, nq, nk = cls.shape
+    cap = m.part_cap
+    assert cap == 4 * B * (nq + nk)
+    part = [(b, qt, kt) for b in range(B) for qt in range(nq) for kt in range(nk)
+            if cls[b, qt, kt] == 1]
+    assert int(_dev_arr(m, m.n_part, 1, torch.int32)[0]) == len(part)
+    tk = nk // n_shards
+    pf = _dev_arr(m, m.part_fwd, B * nq * (n_shards + 1), torch.int32).reshape(B * nq, -1)
+    pb = _dev_arr(m, m.part_bwd, B * nk, torch.int32)
+    want_f = np.zeros_like(pf)
+    for r in range(B * nq):
+        b, qt = divmod(r, nq)
+        before = sum(1 for t in part if (t[0], t[1]) < (b, qt))
+        for s_ in range(n_shards + 1):
+            want_f[r, s_] = before + sum(1 for t in part if (t[0], t[1]) == (b, qt)
+                                         and t[2] < s_ * tk)
+    assert np.array_equal(pf, want_f)
+    colpart = sorted(part, key=lambda t: (t[0], t[2], t[1]))
+    want_b = [sum(1 for t in colpart if (t[0], t[2]) < divmod(c, nk)) for c in range(B * nk)]
+    assert pb.tolist() == want_b
+    rows = _dev_arr(m, m.part_rows, cap * 128 * 4, torch.int32).view("<u4").reshape(cap, 128, 4)
+    cols = _dev_arr(m, m.part_cols, cap * 128 * 4, torch.int32).view("<u4").reshape(cap, 128, 4)
+    for order, got, transpose in ((part, rows, False), (colpart, cols, True)):
+        for slot, (b, qt, kt) in enumerate(order[:cap]):
+            blk = vis[b, qt * 128:(qt + 1) * 128, kt * 128:(kt + 1) * 128]
+            assert np.array_equal(got[slot], _pack_rows(blk.T if transpose else blk)), (slot, b, qt, kt)
+    return len(part)
+
+
 @pytest.mark.parametrize("seed", range(5))
 def test_block_mask_bit_exact(seed):
     g = torch.Generator().manual_seed(seed)
@@ -216,6 +266,29 @@ def test_block_mask_bit_exact(seed):
         listed = idx[r][idx[r] >= 0]
         want = [int(np.sum(listed < s_ * tk)) for s_ in range(n_shards + 1)]
         assert shard[r].tolist() == want, r
+    vis = visibility(B, L, L, causal=causal, q_pos=pos.numpy(), kv_pos=pos.numpy(),
+                     q_seg=seg.numpy(), kv_seg=seg.numpy())
+    check_partial_blocks(m, np.asarray(ref["tile_class"]).reshape(B, nq, nk), vis, n_shards)
+
+
+def test_block_mask_partial_blocks_past_capacity():
+    # shuffled positions: all 256 tiles partial, blocks for the first 128 only
+    g = torch.Generator().manual_seed(4)
+    B, L, N = 1, 2048, 2
+    seg, pos = random_structure(g, B, L, n_docs_max=2, shuffle_positions=True)
+    q = torch.zeros(B, L, 1, 64, dtype=torch.bfloat16, device="cuda")
+    dseg, dpos = seg.cuda(), pos.cuda()
+    p = ra.make_params(q, q, scale=1.0, causal=True, q_pos=dpos, kv_pos=dpos, q_seg=dseg,
+                       kv_seg=dseg, n_virtual_shards=N)
+    m = ra.build_mask(p)
+    torch.cuda.synchronize()
+    ref = oracle.block_mask(B, L, L, causal=True, q_pos=pos.numpy(), kv_pos=pos.numpy(),
+                            q_seg=seg.numpy(), kv_seg=seg.numpy())
+    vis = visibility(B, L, L, causal=True, q_pos=pos.numpy(), kv_pos=pos.numpy(),
+                     q_seg=seg.numpy(), kv_seg=seg.numpy())
+    nq = L // 128
+    n_part = check_partial_blocks(m, np.asarray(ref["tile_class"]).reshape(B, nq, nq), vis, N)
+    assert n_part > m.part_cap
 
 
 def test_block_mask_sequential_positions_bit_exact():
@@ -314,6 +387,18 @@ def test_backward_packed_docs_with_padding():
     _check_bwd(c, grads)
 
 
+def test_backward_past_partial_block_capacity():
+    # shuffled positions make (nearly) every tile partial: 256 tiles, 128 blocks
+    c = Case(W(B=1, L=2048, Hq=2, Hkv=1, seed=39, n_shards=2), dout=True,
+             structure=dict(n_docs_max=2, shuffle_positions=True), seed_struct=4)
+    out, lse, m = c.gpu_fwd()
+    assert int(_dev_arr(m, m.n_part, 1, torch.int32)[0]) > m.part_cap
+    d = c.dev
+    grads = ra.backward(c.params, d["q"], d["k"], d["v"], out, lse, d["dout"], m)
+    torch.cuda.synchronize()
+    _check_bwd(c, grads)
+
+
 def test_backward_padding_rows_inside_a_tile_without_sinks():
     # rows 700..767 are padding: nothing visible, lse = -inf, and they share
     # the last 128-row tile with document rows, so that tile is partial for
@@ -404,3 +489,6 @@ def test_local_mask_block_map_bit_exact():
     got = buf[off:off + B * nq * nk].cpu().numpy()
     assert np.array_equal(got, ref["tile_class"].reshape(-1))
     assert (got == 0).any() and (got == 1).any()  # the band leaves empty and partial tiles
+    vis = visibility(B, L, L, causal=False, q_seg=seg.numpy(), kv_seg=seg.numpy(),
+                     local_mask=lm.numpy())
+    check_partial_blocks(m, got.reshape(B, nq, nk), vis, N)
