@@ -437,6 +437,8 @@ LOCAL_CASES = {
                         n_shards=2, seed=53), dict(window=300, density=0.95)),
     "d64": (W(causal=False, D=64, n_shards=2, seed=54), dict(window=64)),
     "fp32": (W(causal=False, D=64, dtype="fp32", L=512, n_shards=2, seed=55), dict(window=100)),
+    # one shard: the mask covers the whole (Lq, Lkv) grid (a dense 2-D mask)
+    "n1_dense_random": (W(causal=False, n_shards=1, seed=56, L=1536), dict(density=0.3)),
 }
 
 
@@ -460,7 +462,8 @@ def test_local_mask_forward_matches_oracle(name):
     check_fwd(out, lse, o_ref, l_ref)
 
 
-@pytest.mark.parametrize("name", ["n2_band", "n4_random_segments", "mqa_sinks_cap"])
+@pytest.mark.parametrize("name", ["n2_band", "n4_random_segments", "mqa_sinks_cap",
+                                  "n1_dense_random"])
 def test_local_mask_backward_matches_oracle(name):
     c = _local_case(name, dout=True)
     out, lse, m = c.gpu_fwd()
