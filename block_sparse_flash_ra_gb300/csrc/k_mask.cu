@@ -24,10 +24,11 @@
 // 4. order: stable counting sort of rows (columns) by descending count.
 // 5. part_scan: exclusive prefix sums of the partial counts give every
 //    PARTIAL tile a number in row order and one in column order.
-// 6. part_rows / part_cols: the partial mask blocks (the pages' MaskInfo
-//    partial_mask_blocks): the 128 x 128 visibility bits of each numbered
-//    tile below the capacity, row-major by row-order number and transposed by
-//    column-order number.
+// 6. part_list / part_bits: the partial mask blocks (the pages' MaskInfo
+//    partial_mask_blocks): each row and column lists its numbered tiles, then
+//    one block per number writes the 128 x 128 visibility bits of the tile of
+//    that row-order number (row-major) and of that column-order number
+//    (transposed), for the numbers below the capacity.
 #include "ra_internal.h"
 
 namespace ra {
@@ -301,6 +302,80 @@ __global__ void __launch_bounds__(kCls) columns_kernel(const uint8_t *cls, int n
     if (threadIdx.x == 0) part_bwd[(size_t)b * nk + kt] = npart;
 }
 
+// Exclusive prefix sum of one value per thread over a block of 1024 threads
+// (warp shuffles, then the 32 warp totals); `total` gets the block sum.
+// `wsum` is 32 ints of shared memory.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *wsum, int &total)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += t;
+    }
+    if (lane == 31) wsum[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int w = wsum[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        wsum[lane] = w; // inclusive over warps
+    }
+    __syncthreads();
+    total = wsum[31];
+    const int r = (wid > 0 ? wsum[wid - 1] : 0) + x - v;
+    __syncthreads(); // wsum may be reused by the caller
+    return r;
+}
+
+// Stable counting sort of ids 0..R-1 by descending cnt[id] (ties by id).
+// One block of 1024 threads; hist needs (maxc + 1) ints of dynamic smem.
+__global__ void __launch_bounds__(1024) order_kernel(const int32_t *cnt, int R, int maxc,
+                                                     int32_t *order)
+{
+    extern __shared__ int hist[]; // [maxc + 1], then [1024] partials
+    int *part = hist + maxc + 1;
+    const int nb = maxc + 1;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < R; i += blockDim.x) atomicAdd(&hist[maxc - cnt[i]], 1);
+    __syncthreads();
+    // exclusive scan of hist (key = maxc - cnt ascending == cnt descending)
+    const int per = (nb + blockDim.x - 1) / blockDim.x;
+    const int lo = threadIdx.x * per, hi = min(nb, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += hist[i];
+    int total;
+    int run = block_exclusive_scan(sum, part, total);
+    for (int i = lo; i < hi; ++i) {
+        const int v = hist[i];
+        hist[i] = run;
+        run += v;
+    }
+    __syncthreads();
+    // stable scatter by warp 0, 32 ids at a time in id order
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        for (int i0 = 0; i0 < R; i0 += 32) {
+            const int id = i0 + lane;
+            const bool act = id < R;
+            const int key = act ? maxc - cnt[id] : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            const int leader = __ffs(peers) - 1;
+            int start = 0;
+            if (act && lane == leader) {
+                start = hist[key];
+                hist[key] = start + __popc(peers);
+            }
+            start = __shfl_sync(0xffffffffu, start, leader);
+            if (act) order[start + __popc(peers & ((1u << lane) - 1u))] = id;
+            __syncwarp();
+        }
+    }
+}
+
 // Block 0: exclusive prefix over rows of their partial counts, added to
 // every per-shard entry of the row (entry N held the row's own total), and
 // the grand total into n_part.  Block 1: exclusive prefix over columns.
@@ -308,7 +383,7 @@ __global__ void __launch_bounds__(1024) part_scan_kernel(int32_t *part_fwd, int 
                                                          int32_t *part_bwd, int cols,
                                                          int32_t *n_part)
 {
-    __shared__ int part[1024];
+    __shared__ int wsum[32];
     const bool by_rows = blockIdx.x == 0;
     const int R = by_rows ? rows : cols;
     const int per = (R + 1023) / 1024;
@@ -316,19 +391,9 @@ __global__ void __launch_bounds__(1024) part_scan_kernel(int32_t *part_fwd, int 
     int sum = 0;
     for (int r = lo; r < hi; ++r)
         sum += by_rows ? part_fwd[(size_t)r * n1 + n1 - 1] : part_bwd[r];
-    part[threadIdx.x] = sum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int t = 0; t < 1024; ++t) {
-            const int v = part[t];
-            part[t] = run;
-            run += v;
-        }
-        if (by_rows) *n_part = run;
-    }
-    __syncthreads();
-    int run = part[threadIdx.x];
+    int total;
+    int run = block_exclusive_scan(sum, wsum, total);
+    if (by_rows && threadIdx.x == 0) *n_part = total;
     for (int r = lo; r < hi; ++r) {
         if (by_rows) {
             int32_t *e = part_fwd + (size_t)r * n1;
@@ -364,165 +429,124 @@ __device__ __forceinline__ int gather_partial(const int32_t *list, int cnt, int 
     return n;
 }
 
-// grid (nq, B), 128 threads: thread i writes row i of the row-major block of
-// each PARTIAL tile of query-tile row (b, qt) numbered below the capacity.
-__global__ void __launch_bounds__(128) part_rows_kernel(Problem p, const uint8_t *cls,
+// grid (max(nq, nk), B, 2), 128 threads: block (x, b, 0) lists, in row
+// order, the PARTIAL tiles of query-tile row (b, x) numbered below the
+// capacity as (row id, kt); block (x, b, 1) lists those of key-tile column
+// (b, x) in column order as (column id, qt).
+__global__ void __launch_bounds__(128) part_list_kernel(Problem p, const uint8_t *cls,
                                                         const int32_t *fwd_cnt,
                                                         const int32_t *fwd_idx,
-                                                        const int32_t *part_fwd, uint32_t *out)
-{
-    const int b = blockIdx.y, qt = blockIdx.x, i = threadIdx.x;
-    const size_t row = (size_t)b * p.nq + qt;
-    int slot = part_fwd[row * (p.N + 1)];
-    if (slot >= p.part_cap || part_fwd[row * (p.N + 1) + p.N] == slot) return;
-    __shared__ int k_seg_s[kTile], k_pos_s[kTile], plist[kTile], wcnt[4];
-    const int qi = qt * kTile + i;
-    const int my_seg = seg_at(p.q_seg, b, p.Lq, qi);
-    const int my_pos = pos_at(p.q_pos, b, p.Lq, qi);
-    const bool my_pad = p.q_seg && my_seg == p.pad_id;
-    const int cnt = fwd_cnt[row];
-    const int32_t *list = fwd_idx + row * p.nk;
-    for (int e0 = 0; e0 < cnt && slot < p.part_cap; e0 += kTile) {
-        const int n = gather_partial(list, cnt, e0, cls, row * p.nk, 1, plist, wcnt);
-        for (int t = 0; t < n && slot < p.part_cap; ++t, ++slot) {
-            const int kt = plist[t];
-            k_seg_s[i] = seg_at(p.kv_seg, b, p.Lkv, kt * kTile + i);
-            k_pos_s[i] = pos_at(p.kv_pos, b, p.Lkv, kt * kTile + i);
-            __syncthreads();
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t bits = 0;
-#pragma unroll 8
-                for (int z = 0; z < 32; ++z) {
-                    const int j = 32 * k + z;
-                    bool v = k_seg_s[j] == my_seg && !my_pad;
-                    if (p.causal) v = v && my_pos >= k_pos_s[j];
-                    bits |= (v ? 1u : 0u) << z;
-                }
-                w[k] = bits;
-            }
-            if (p.local_mask) {
-                const uint8_t *lm = p.local_mask + (size_t)(qi % p.lq_s) * p.lk_s + (kt * kTile) % p.lk_s;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll 8
-                    for (int z = 0; z < 32; ++z)
-                        if (!lm[32 * k + z]) w[k] &= ~(1u << z);
-            }
-            reinterpret_cast<uint4 *>(out)[(size_t)slot * kTile + i] = make_uint4(w[0], w[1], w[2], w[3]);
-            __syncthreads();
-        }
-    }
-}
-
-// grid (nk, B), 128 threads: thread j writes row j (kv row) of the
-// transposed block of each PARTIAL tile of key-tile column (b, kt) numbered
-// below the capacity.
-__global__ void __launch_bounds__(128) part_cols_kernel(Problem p, const uint8_t *cls,
+                                                        const int32_t *part_fwd,
                                                         const int32_t *bwd_cnt,
                                                         const int32_t *bwd_idx,
-                                                        const int32_t *part_bwd, uint32_t *out)
+                                                        const int32_t *part_bwd, int2 *rows_list,
+                                                        int2 *cols_list)
 {
-    const int b = blockIdx.y, kt = blockIdx.x, j = threadIdx.x;
-    const size_t col = (size_t)b * p.nk + kt;
-    int slot = part_bwd[col];
+    const int b = blockIdx.y, x = blockIdx.x;
+    const bool by_rows = blockIdx.z == 0;
+    if (x >= (by_rows ? p.nq : p.nk)) return;
+    __shared__ int plist[kTile], wcnt[4];
+    const size_t id = (size_t)b * (by_rows ? p.nq : p.nk) + x;
+    int slot = by_rows ? part_fwd[id * (p.N + 1)] : part_bwd[id];
     if (slot >= p.part_cap) return;
-    __shared__ int q_seg_s[kTile], q_pos_s[kTile], plist[kTile], wcnt[4];
-    const int kj = kt * kTile + j;
-    const int my_seg = seg_at(p.kv_seg, b, p.Lkv, kj);
-    const int my_pos = pos_at(p.kv_pos, b, p.Lkv, kj);
-    const int cnt = bwd_cnt[col];
-    const int32_t *list = bwd_idx + col * p.nq;
+    const int cnt = by_rows ? fwd_cnt[id] : bwd_cnt[id];
+    const int32_t *list = by_rows ? fwd_idx + id * p.nk : bwd_idx + id * p.nq;
+    const size_t cls_base = by_rows ? id * p.nk : (size_t)b * p.nq * p.nk + x;
+    const size_t cls_stride = by_rows ? 1 : p.nk;
+    int2 *out = by_rows ? rows_list : cols_list;
     for (int e0 = 0; e0 < cnt && slot < p.part_cap; e0 += kTile) {
-        const int n = gather_partial(list, cnt, e0, cls, (size_t)b * p.nq * p.nk + kt, p.nk, plist,
-                                     wcnt);
-        for (int t = 0; t < n && slot < p.part_cap; ++t, ++slot) {
-            const int qt = plist[t];
-            q_seg_s[j] = seg_at(p.q_seg, b, p.Lq, qt * kTile + j);
-            q_pos_s[j] = pos_at(p.q_pos, b, p.Lq, qt * kTile + j);
-            __syncthreads();
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t bits = 0;
-#pragma unroll 8
-                for (int z = 0; z < 32; ++z) {
-                    const int i = 32 * k + z;
-                    const int sq = q_seg_s[i];
-                    bool v = sq == my_seg && !(p.q_seg && sq == p.pad_id);
-                    if (p.causal) v = v && q_pos_s[i] >= my_pos;
-                    bits |= (v ? 1u : 0u) << z;
-                }
-                w[k] = bits;
-            }
-            if (p.local_mask) {
-                const uint8_t *lm = p.local_mask + (size_t)((qt * kTile) % p.lq_s) * p.lk_s + kj % p.lk_s;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll 8
-                    for (int z = 0; z < 32; ++z)
-                        if (!lm[(size_t)(32 * k + z) * p.lk_s]) w[k] &= ~(1u << z);
-            }
-            reinterpret_cast<uint4 *>(out)[(size_t)slot * kTile + j] = make_uint4(w[0], w[1], w[2], w[3]);
-            __syncthreads();
-        }
+        const int n = gather_partial(list, cnt, e0, cls, cls_base, cls_stride, plist, wcnt);
+        if ((int)threadIdx.x < n && slot + (int)threadIdx.x < p.part_cap)
+            out[slot + threadIdx.x] = make_int2((int)id, plist[threadIdx.x]);
+        slot += n;
+        __syncthreads(); // plist is rewritten by the next chunk
     }
 }
 
-// Stable counting sort of ids 0..R-1 by descending cnt[id] (ties by id).
-// One block of 1024 threads; hist needs (maxc + 1) ints of dynamic smem.
-__global__ void __launch_bounds__(1024) order_kernel(const int32_t *cnt, int R, int maxc,
-                                                     int32_t *order)
+// Visibility word k (columns 32k..32k+31) of one row against 128 staged
+// columns: bit z set iff column 32k + z is visible.
+__device__ __forceinline__ uint32_t vis_word(int k, int seg, bool pad, int pos, const int *seg_s,
+                                             const int *pos_s, bool row_is_query, int causal,
+                                             bool q_seg_present, int pad_id)
 {
-    extern __shared__ int hist[]; // [maxc + 1], then [1024] partials
-    int *part = hist + maxc + 1;
-    const int nb = maxc + 1;
-    for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < R; i += blockDim.x) atomicAdd(&hist[maxc - cnt[i]], 1);
-    __syncthreads();
-    // exclusive scan of hist (key = maxc - cnt ascending == cnt descending)
-    const int per = (nb + blockDim.x - 1) / blockDim.x;
-    const int lo = threadIdx.x * per, hi = min(nb, lo + per);
-    int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += hist[i];
-    part[threadIdx.x] = sum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int t = 0; t < (int)blockDim.x; ++t) {
-            const int v = part[t];
-            part[t] = run;
-            run += v;
+    uint32_t bits = 0;
+#pragma unroll 8
+    for (int z = 0; z < 32; ++z) {
+        const int j = 32 * k + z;
+        bool v;
+        if (row_is_query) {
+            v = seg_s[j] == seg && !pad;
+            if (causal) v = v && pos >= pos_s[j];
+        } else {
+            const int sq = seg_s[j];
+            v = sq == seg && !(q_seg_present && sq == pad_id);
+            if (causal) v = v && pos_s[j] >= pos;
         }
+        bits |= (v ? 1u : 0u) << z;
     }
-    __syncthreads();
-    int run = part[threadIdx.x];
-    for (int i = lo; i < hi; ++i) {
-        const int v = hist[i];
-        hist[i] = run;
-        run += v;
-    }
-    __syncthreads();
-    // stable scatter by warp 0, 32 ids at a time in id order
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        for (int i0 = 0; i0 < R; i0 += 32) {
-            const int id = i0 + lane;
-            const bool act = id < R;
-            const int key = act ? maxc - cnt[id] : -1;
-            const unsigned peers = __match_any_sync(0xffffffffu, key);
-            const int leader = __ffs(peers) - 1;
-            int start = 0;
-            if (act && lane == leader) {
-                start = hist[key];
-                hist[key] = start + __popc(peers);
-            }
-            start = __shfl_sync(0xffffffffu, start, leader);
-            if (act) order[start + __popc(peers & ((1u << lane) - 1u))] = id;
-            __syncwarp();
+    return bits;
+}
+
+// grid (part_cap), 128 threads: block i writes the row-major bits of the
+// i-th tile in row order and the transposed bits of the i-th tile in column
+// order (when they exist).
+__global__ void __launch_bounds__(128) part_bits_kernel(Problem p, const int32_t *n_part,
+                                                        const int2 *rows_list,
+                                                        const int2 *cols_list, uint32_t *rows_out,
+                                                        uint32_t *cols_out)
+{
+    const int i = blockIdx.x, t = threadIdx.x;
+    if (i >= min(*n_part, p.part_cap)) return;
+    __shared__ int seg_s[kTile], pos_s[kTile];
+    // ---- row-major block: thread t = query row t of the tile
+    {
+        const int2 e = rows_list[i];
+        const int b = e.x / p.nq, qt = e.x - b * p.nq, kt = e.y;
+        seg_s[t] = seg_at(p.kv_seg, b, p.Lkv, kt * kTile + t);
+        pos_s[t] = pos_at(p.kv_pos, b, p.Lkv, kt * kTile + t);
+        const int qi = qt * kTile + t;
+        const int seg = seg_at(p.q_seg, b, p.Lq, qi);
+        const int pos = pos_at(p.q_pos, b, p.Lq, qi);
+        const bool pad = p.q_seg && seg == p.pad_id;
+        __syncthreads();
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = vis_word(k, seg, pad, pos, seg_s, pos_s, true, p.causal, p.q_seg != nullptr, p.pad_id);
+        if (p.local_mask) {
+            const uint8_t *lm = p.local_mask + (size_t)(qi % p.lq_s) * p.lk_s + (kt * kTile) % p.lk_s;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll 8
+                for (int z = 0; z < 32; ++z)
+                    if (!lm[32 * k + z]) w[k] &= ~(1u << z);
         }
+        reinterpret_cast<uint4 *>(rows_out)[(size_t)i * kTile + t] = make_uint4(w[0], w[1], w[2], w[3]);
+        __syncthreads(); // seg_s / pos_s are restaged below
+    }
+    // ---- transposed block: thread t = kv row t of the tile
+    {
+        const int2 e = cols_list[i];
+        const int b = e.x / p.nk, kt = e.x - b * p.nk, qt = e.y;
+        seg_s[t] = seg_at(p.q_seg, b, p.Lq, qt * kTile + t);
+        pos_s[t] = pos_at(p.q_pos, b, p.Lq, qt * kTile + t);
+        const int kj = kt * kTile + t;
+        const int seg = seg_at(p.kv_seg, b, p.Lkv, kj);
+        const int pos = pos_at(p.kv_pos, b, p.Lkv, kj);
+        __syncthreads();
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = vis_word(k, seg, false, pos, seg_s, pos_s, false, p.causal, p.q_seg != nullptr, p.pad_id);
+        if (p.local_mask) {
+            const uint8_t *lm = p.local_mask + (size_t)((qt * kTile) % p.lq_s) * p.lk_s + kj % p.lk_s;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll 8
+                for (int z = 0; z < 32; ++z)
+                    if (!lm[(size_t)(32 * k + z) * p.lk_s]) w[k] &= ~(1u << z);
+        }
+        reinterpret_cast<uint4 *>(cols_out)[(size_t)i * kTile + t] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -531,7 +555,10 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t *cnt, int R, 
 size_t mask_scratch_ints(int B, int nq, int nk, int N)
 {
     const size_t local_tiles = (size_t)(nq / N) * (nk / N); // one byte each
-    return (size_t)B * (nq + nk) * (sizeof(TileSum) / sizeof(int32_t)) + (local_tiles + 3) / 4;
+    // tile summaries, local classes, and the two lists of numbered partial
+    // tiles (an int2 per number) -- the lists first, for their alignment
+    return (size_t)4 * mask_part_cap(B, nq, nk) +
+           (size_t)B * (nq + nk) * (sizeof(TileSum) / sizeof(int32_t)) + (local_tiles + 3) / 4;
 }
 
 int mask_part_cap(int B, int nq, int nk)
@@ -545,7 +572,9 @@ cudaError_t launch_mask_build(const Problem &pin, const ra_block_mask &m, int32_
     Problem p = pin;
     p.part_cap = m.part_cap;
     uint8_t *cls = m.tile_class;
-    TileSum *qsum = reinterpret_cast<TileSum *>(scratch);
+    int2 *rows_list = reinterpret_cast<int2 *>(scratch);
+    int2 *cols_list = rows_list + m.part_cap;
+    TileSum *qsum = reinterpret_cast<TileSum *>(cols_list + m.part_cap);
     TileSum *ksum = qsum + (size_t)p.B * p.nq;
     uint8_t *lcls = reinterpret_cast<uint8_t *>(ksum + (size_t)p.B * p.nk);
     tile_summary_kernel<<<dim3(p.nq, p.B), 128, 0, s>>>(p.q_seg, p.q_pos, p.Lq, p.pad_id, qsum);
@@ -562,10 +591,11 @@ cudaError_t launch_mask_build(const Problem &pin, const ra_block_mask &m, int32_
     order_kernel<<<1, 1024, sm_b, s>>>(m.bwd_cnt, p.B * p.nk, p.nq, m.bwd_order);
     part_scan_kernel<<<2, 1024, 0, s>>>(m.part_fwd, p.B * p.nq, p.N + 1, m.part_bwd, p.B * p.nk,
                                         m.n_part);
-    part_rows_kernel<<<dim3(p.nq, p.B), kTile, 0, s>>>(p, cls, m.fwd_cnt, m.fwd_idx, m.part_fwd,
-                                                       m.part_rows);
-    part_cols_kernel<<<dim3(p.nk, p.B), kTile, 0, s>>>(p, cls, m.bwd_cnt, m.bwd_idx, m.part_bwd,
-                                                       m.part_cols);
+    part_list_kernel<<<dim3(max(p.nq, p.nk), p.B, 2), kTile, 0, s>>>(
+        p, cls, m.fwd_cnt, m.fwd_idx, m.part_fwd, m.bwd_cnt, m.bwd_idx, m.part_bwd, rows_list,
+        cols_list);
+    part_bits_kernel<<<m.part_cap, kTile, 0, s>>>(p, m.n_part, rows_list, cols_list, m.part_rows,
+                                                 m.part_cols);
     return cudaGetLastError();
 }
 
