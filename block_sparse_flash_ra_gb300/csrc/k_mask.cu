@@ -6,12 +6,12 @@
 //   class(qt, kt) = EMPTY if no pair is visible, FULL if all are, else PARTIAL
 // with visible(i, j) = same non-padding segment && (!causal || q_pos >= kv_pos).
 //
-// 1. tile_summary: per 128-row tile, min / max segment id and position over
-//    the non-padding rows and the padding count.
+// 1. tile_summary: per 128-row tile, the padding count, the segment id range
+//    and, for up to four distinct segments, each one's position range.
 // 2. classify_rows: one block per (b, qt).  Tiles whose class follows
-//    exactly from the summaries (disjoint segment ranges; one common segment,
-//    where the causal predicate reduces to comparing position ranges) are
-//    classified from them, the rest pair by pair.  With the non-causal ring's
+//    exactly from the summaries (every segment of both tiles summarised, or
+//    disjoint segment ranges) are classified from them, the rest (tiles with
+//    more than four segments) pair by pair.  With the non-causal ring's
 //    local mask, each 128 x 128 block of the mask is classified once first;
 //    a tile is then empty if either class is, takes the mask's class where
 //    every pair passes the other rules, and is counted pair by pair only
@@ -34,8 +34,13 @@
 namespace ra {
 namespace {
 
+// Per 128-row tile: the padding count, the range of segment ids, and for up
+// to kMaxSeg distinct non-padding segments the id and the position range of
+// the tile's tokens in it (nseg = kMaxSeg + 1: more segments than that).
+constexpr int kMaxSeg = 4;
 struct TileSum {
-    int seg_min, seg_max, pos_min, pos_max, npad;
+    int nseg, npad, seg_min, seg_max;
+    int seg[kMaxSeg], pmin[kMaxSeg], pmax[kMaxSeg];
 };
 
 __device__ __forceinline__ int seg_at(const int32_t *seg, int b, int L, int i)
@@ -52,46 +57,86 @@ __global__ void __launch_bounds__(128) tile_summary_kernel(const int32_t *seg, c
                                                            int L, int pad_id, TileSum *out)
 {
     const int b = blockIdx.y, t = blockIdx.x, i = t * kTile + threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int s = seg_at(seg, b, L, i);
     const int p = pos_at(pos, b, L, i);
     const bool pad = seg && (s == pad_id);
-    int smin = pad ? INT_MAX : s, smax = pad ? INT_MIN : s;
-    int pmin = pad ? INT_MAX : p, pmax = pad ? INT_MIN : p;
-    int npad = pad ? 1 : 0;
-    for (int o = 16; o > 0; o >>= 1) {
-        smin = min(smin, __shfl_xor_sync(0xffffffffu, smin, o));
-        smax = max(smax, __shfl_xor_sync(0xffffffffu, smax, o));
-        pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
-        pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
-        npad += __shfl_xor_sync(0xffffffffu, npad, o);
-    }
-    __shared__ TileSum w[4];
-    if ((threadIdx.x & 31) == 0) w[threadIdx.x >> 5] = TileSum{smin, smax, pmin, pmax, npad};
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        TileSum r = w[0];
-        for (int k = 1; k < 4; ++k) {
-            r.seg_min = min(r.seg_min, w[k].seg_min);
-            r.seg_max = max(r.seg_max, w[k].seg_max);
-            r.pos_min = min(r.pos_min, w[k].pos_min);
-            r.pos_max = max(r.pos_max, w[k].pos_max);
-            r.npad += w[k].npad;
+    // lanes of one segment (padding is a group of its own)
+    const unsigned long long key = pad ? (1ull << 32) : (unsigned long long)(uint32_t)s;
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    int mn = p, mx = p;
+    for (int l = 0; l < 32; ++l) {
+        const int v = __shfl_sync(0xffffffffu, p, l);
+        if ((grp >> l) & 1u) {
+            mn = min(mn, v);
+            mx = max(mx, v);
         }
-        out[(size_t)b * gridDim.x + t] = r;
     }
+    const bool leader = lane == __ffs(grp) - 1;
+    __shared__ TileSum ts;
+    if (threadIdx.x == 0) {
+        ts.nseg = 0;
+        ts.npad = 0;
+        ts.seg_min = INT_MAX;
+        ts.seg_max = INT_MIN;
+    }
+    __syncthreads();
+    if (pad && leader) atomicAdd(&ts.npad, __popc(grp));
+    if (!pad && leader) {
+        atomicMin(&ts.seg_min, s);
+        atomicMax(&ts.seg_max, s);
+    }
+    // group leaders merge their segment into the table one at a time
+    for (int w = 0; w < 4; ++w) {
+        if (warp == w) {
+            for (int l = 0; l < 32; ++l) {
+                if (lane == l && leader && !pad) {
+                    const int n = ts.nseg;
+                    const int m = min(n, kMaxSeg);
+                    int k = 0;
+                    while (k < m && ts.seg[k] != s) ++k;
+                    if (k < m) {
+                        ts.pmin[k] = min(ts.pmin[k], mn);
+                        ts.pmax[k] = max(ts.pmax[k], mx);
+                    } else if (n < kMaxSeg) {
+                        ts.seg[n] = s;
+                        ts.pmin[n] = mn;
+                        ts.pmax[n] = mx;
+                        ts.nseg = n + 1;
+                    } else {
+                        ts.nseg = kMaxSeg + 1;
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[(size_t)b * gridDim.x + t] = ts;
 }
 
-// Class from the summaries when it is exact, else -1 (count pairs).
+// Class from the summaries when it is exact, else -1 (count pairs).  With
+// every segment of both tiles summarised the class is exact: some pair is
+// visible iff a common segment has a query position >= a key position
+// (always, without causal); all pairs are iff both tiles hold one and the
+// same segment, no padding, and (causal) the smallest query position is >=
+// the largest key position.
 __device__ __forceinline__ int classify_fast(const TileSum &q, const TileSum &k, int causal)
 {
-    if (q.npad == kTile || k.npad == kTile) return RA_TILE_EMPTY;
+    if (q.nseg == 0 || k.nseg == 0) return RA_TILE_EMPTY; // all padding
     if (q.seg_max < k.seg_min || k.seg_max < q.seg_min) return RA_TILE_EMPTY;
-    const bool one = q.seg_min == q.seg_max && k.seg_min == k.seg_max && q.seg_min == k.seg_min;
-    if (!one) return -1;
-    const bool nopad = (q.npad == 0 && k.npad == 0);
-    if (!causal) return nopad ? RA_TILE_FULL : RA_TILE_PARTIAL;
-    if (q.pos_max < k.pos_min) return RA_TILE_EMPTY;
-    if (q.pos_min >= k.pos_max) return nopad ? RA_TILE_FULL : RA_TILE_PARTIAL;
+    if (q.nseg > kMaxSeg || k.nseg > kMaxSeg) return -1;
+    bool vis = false;
+#pragma unroll
+    for (int a = 0; a < kMaxSeg; ++a)
+#pragma unroll
+        for (int c = 0; c < kMaxSeg; ++c)
+            if (a < q.nseg && c < k.nseg && q.seg[a] == k.seg[c] && (!causal || q.pmax[a] >= k.pmin[c]))
+                vis = true;
+    if (!vis) return RA_TILE_EMPTY;
+    if (q.nseg == 1 && k.nseg == 1 && q.npad == 0 && k.npad == 0 &&
+        (!causal || q.pmin[0] >= k.pmax[0]))
+        return RA_TILE_FULL;
     return RA_TILE_PARTIAL;
 }
 
@@ -170,8 +215,43 @@ __global__ void __launch_bounds__(kCls) classify_rows_kernel(Problem p, const Ti
         }
         __syncthreads();
         const int ns = nslow;
+        // Quick pass: thread t tests kv column t mod 128 of a slow tile against
+        // query rows t/128 + 16k (k < 8), one pair in eight; a visible and a
+        // hidden pair among them make the tile PARTIAL without counting (the
+        // usual case: tiles cut by a document boundary).  The next tile's kv
+        // entries are fetched one tile ahead.
+        const int cj = threadIdx.x & (kTile - 1), r0 = threadIdx.x >> 7;
+        int ks_next = 0, kp_next = 0;
+        if (ns > 0) {
+            ks_next = seg_at(p.kv_seg, b, p.Lkv, slow[0] * kTile + cj);
+            kp_next = pos_at(p.kv_pos, b, p.Lkv, slow[0] * kTile + cj);
+        }
         for (int si = 0; si < ns; ++si) {
             const int kt = slow[si];
+            const int ksg = ks_next, kps = kp_next;
+            if (si + 1 < ns) {
+                ks_next = seg_at(p.kv_seg, b, p.Lkv, slow[si + 1] * kTile + cj);
+                kp_next = pos_at(p.kv_pos, b, p.Lkv, slow[si + 1] * kTile + cj);
+            }
+            bool seen_vis = false, seen_hid = false;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = r0 + 16 * k;
+                const int sq = q_seg_s[i];
+                bool vis = (sq == ksg) && !(p.q_seg && sq == p.pad_id);
+                if (p.causal) vis = vis && (q_pos_s[i] >= kps);
+                if (p.local_mask)
+                    vis = vis && p.local_mask[(size_t)((qt * kTile + i) % p.lq_s) * p.lk_s +
+                                              (kt * kTile + cj) % p.lk_s] != 0;
+                seen_vis |= vis;
+                seen_hid |= !vis;
+            }
+            const int any_vis = __syncthreads_or(seen_vis ? 1 : 0);
+            const int any_hid = __syncthreads_or(seen_hid ? 1 : 0);
+            if (any_vis && any_hid) {
+                if (threadIdx.x == 0) crow[kt] = (uint8_t)RA_TILE_PARTIAL;
+                continue;
+            }
             if (threadIdx.x < kTile) {
                 const int j = kt * kTile + threadIdx.x;
                 k_seg_s[threadIdx.x] = seg_at(p.kv_seg, b, p.Lkv, j);
