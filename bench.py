@@ -41,13 +41,13 @@ METRIC = "masked-attention TFLOP/s fwd and fwd+bwd (unmasked tiles) and % BF16 t
 UNIT = "TFLOP/s"
 
 # DRAM traffic per launch of each kernel from an ncu capture (bytes), keyed by
-# (workload, kernel), with the sha256 of the kernel source it was taken on; a
-# changed source, or another workload, reports null.
+# (workload, kernel), with the hash of the sources the kernel is compiled from
+# (_src_hash); a changed source, or another workload, reports null.
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch, ncu on the gqa32k bench step
-    ("gqa32k", "fwd_tc_kernel"): (3.076e9 + 0.290e9, "032abeea48f38633"),
-    ("gqa32k", "bwd_dkdv_kernel"): (4.065e9 + 0.121e9, "fa5bbf99321fa07d"),
-    ("gqa32k", "bwd_dq_kernel"): (4.135e9 + 0.241e9, "fa5bbf99321fa07d"),
+    ("gqa32k", "fwd_tc_kernel"): (3.129e9 + 0.290e9, "36b130360c06befa"),
+    ("gqa32k", "bwd_dkdv_kernel"): (4.081e9 + 0.130e9, "4b80553840e43957"),
+    ("gqa32k", "bwd_dq_kernel"): (3.623e9 + 0.252e9, "4b80553840e43957"),
 }
 
 
@@ -61,11 +61,18 @@ def _peaks():
 
 
 def _src_hash(name):
-    p = os.path.join(ROOT, "block_sparse_flash_ra_gb300", "csrc", name)
+    """sha256 (first 16 hex) of a kernel source and the headers it includes."""
+    csrc = os.path.join(ROOT, "block_sparse_flash_ra_gb300", "csrc")
+    files = [os.path.join(csrc, f) for f in (name, "ra_sched.cuh", "ra_device.cuh", "ra_internal.h")]
+    files.append(os.path.join(ROOT, "include", "ra.h"))
+    h = hashlib.sha256()
     try:
-        return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+        for f in files:
+            with open(f, "rb") as fh:
+                h.update(fh.read())
     except OSError:
         return None
+    return h.hexdigest()[:16]
 
 
 def _dist():
