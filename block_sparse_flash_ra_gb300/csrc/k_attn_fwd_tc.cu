@@ -353,6 +353,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const float sink2 = has_sink ? p.sinks[x.h] * kLog2e : 0.f;
             float lse_run = -INFINITY;
             bool orun_set = false; // uniform: O_run columns hold this unit's data
+            bool out_written = false; // uniform: the last merge stored the output itself
+            int tiles_done = 0;
             if (x.cnt > 0) {
                 const int my_pos = p.q_pos ? p.q_pos[(size_t)x.b * p.Lq + qi] : qi;
                 const int my_seg = p.q_seg ? p.q_seg[(size_t)x.b * p.Lq + qi] : 0;
@@ -501,6 +503,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     }
                     if (!ok) break;
                     // ---- shard end: normalise, add the sink (t == 0), merge
+                    tiles_done += hi - lo;
+                    // the unit's last non-empty shard merges straight into the bf16 output
+                    const bool last = tiles_done == x.cnt;
                     if (!(ok = wait_pv_upto(g))) break;
                     tc_fence_after();
                     float *xs = xsum + (nshard & 1) * 256;
@@ -530,16 +535,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         tmem_ld32(lane_base + C::kColO + o_col + c * 32, a);
                         if (orun_set) tmem_ld32(lane_base + C::kColRun + o_col + c * 32, cur);
                         tmem_ld_wait();
-                        uint32_t nv[32];
+                        float nv[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const float os = a[j] * inv;
                             const float cv = orun_set ? cur[j] : 0.f;
-                            nv[j] = __float_as_uint(first ? os : cv - w * (cv - os));
+                            nv[j] = first ? os : cv - w * (cv - os);
                         }
-                        tmem_st32(lane_base + C::kColRun + o_col + c * 32, nv);
+                        if (last) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                uint4 v;
+                                v.x = pack_bf16x2(nv[8 * k + 0], nv[8 * k + 1]);
+                                v.y = pack_bf16x2(nv[8 * k + 2], nv[8 * k + 3]);
+                                v.z = pack_bf16x2(nv[8 * k + 4], nv[8 * k + 5]);
+                                v.w = pack_bf16x2(nv[8 * k + 6], nv[8 * k + 7]);
+                                dst[k] = v;
+                            }
+                        } else {
+                            uint32_t nw[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) nw[j] = __float_as_uint(nv[j]);
+                            tmem_st32(lane_base + C::kColRun + o_col + c * 32, nw);
+                        }
                     }
-                    tmem_st_wait();
+                    if (!last) tmem_st_wait();
+                    out_written = last;
                     lse_run = first ? lse_s : lse_run + softplus_f(lse_s - lse_run);
                     orun_set = true;
                 }
@@ -547,8 +569,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             } else if (has_sink) {
                 lse_run = sink2 * kLn2;
             }
-            // ---- epilogue: this half of O_run -> bf16, lse
-            if (orun_set) {
+            // ---- epilogue: this half of O_run -> bf16 (unless the last merge
+            // stored it), lse
+            if (out_written) {
+            } else if (orun_set) {
 #pragma unroll
                 for (int c = 0; c < kOH / 32; ++c) {
                     float a[32];
