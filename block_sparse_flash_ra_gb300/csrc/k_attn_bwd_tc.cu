@@ -106,7 +106,9 @@ __device__ __forceinline__ ColUnit col_unit(const Problem &p, int u)
     return x;
 }
 
-template <int D>
+// CAP: soft cap on (compiled per choice, so that neither form carries the
+// other's code)
+template <int D, bool CAP>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         constexpr int kOH = D / 2;
         const uint32_t o_col = wg * kOH;
         const float scale2 = p.scale * kLog2e;
-        const float cap = p.soft_cap;
+        const float cap = CAP ? p.soft_cap : 0.f;
         const float cap2 = cap * kLog2e;
         const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
         uint32_t n = 0, ua = 0;
@@ -350,12 +352,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tmem_ld_wait();
                         const float4 *l4 = reinterpret_cast<const float4 *>(lse_s);
                         uint32_t pk[32];
-                        if (cap > 0.f) {
+                        if (CAP) {
                             float xa = 0.f;
 #pragma unroll
                             for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
-                            // one loop per tanh form, chosen once per tile (warp-uniform)
-                            auto capped = [&](auto tanh_fn) {
+                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
+                                // tanh by its odd Taylor series on the FMA pipe, two lanes
+                                // per instruction: t = x (1 + x^2 (c3 + x^2 (c5 + x^2 c7)))
+                                const float2 k2 = make_float2(scale_over_cap, scale_over_cap);
+                                const float2 c7 = make_float2(kTanhC7, kTanhC7);
+                                const float2 c5 = make_float2(kTanhC5, kTanhC5);
+                                const float2 c3 = make_float2(kTanhC3, kTanhC3);
+                                const float2 one = make_float2(1.f, 1.f);
+                                const float2 cc = make_float2(cap2, cap2);
+#pragma unroll
+                                for (int j = 0; j < 64; j += 4) {
+                                    const float4 lv = l4[j >> 2];
+                                    const float2 la[2] = {make_float2(lv.x, lv.y), make_float2(lv.z, lv.w)};
+#pragma unroll
+                                    for (int h = 0; h < 2; ++h) {
+                                        const int c = j + 2 * h;
+                                        const float2 x = fmul2(make_float2(s[c], s[c + 1]), k2);
+                                        const float2 x2 = fmul2(x, x);
+                                        float2 pp = ffma2(x2, c7, c5);
+                                        pp = ffma2(x2, pp, c3);
+                                        pp = ffma2(x2, pp, one);
+                                        const float2 t = fmul2(x, pp);
+                                        const float2 a = ffma2(cc, t, la[h]);
+                                        float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                                        if (partial) {
+                                            e.x = ((vis[c >> 5] >> (c & 31)) & 1u) ? e.x : 0.f;
+                                            e.y = ((vis[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e.y : 0.f;
+                                        }
+                                        const float2 cr = fmul2(e, fsub2(one, fmul2(t, t)));
+                                        pk[c >> 1] = pack_bf16x2(e.x, e.y);
+                                        pc[c >> 1] = pack_bf16x2(cr.x, cr.y);
+                                    }
+                                }
+                            } else {
 #pragma unroll
                                 for (int j = 0; j < 64; j += 4) {
                                     const float4 lv = l4[j >> 2];
@@ -364,7 +398,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                                     for (int z = 0; z < 4; ++z) {
                                         const int c = j + z;
-                                        const float t = tanh_fn(s[c] * scale_over_cap);
+                                        const float t = tanh_fast(s[c] * scale_over_cap);
                                         float e = ex2_approx(fmaf(cap2, t, la[z]));
                                         e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
                                         pr[z] = e;
@@ -375,11 +409,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                     pc[j >> 1] = pack_bf16x2(cr[0], cr[1]);
                                     pc[(j >> 1) + 1] = pack_bf16x2(cr[2], cr[3]);
                                 }
-                            };
-                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall))
-                                capped([](float x) { return tanh_small(x); });
-                            else
-                                capped([](float x) { return tanh_fast(x); });
+                            }
                         } else {
                             // masked logits -> -inf, so that 2^(...) = 0 below
                             if (partial) {
@@ -545,7 +575,7 @@ __device__ __forceinline__ RowUnit row_unit(const Problem &p, int u)
     return x;
 }
 
-template <int D>
+template <int D, bool CAP>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -744,7 +774,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         constexpr int kOH = D / 2;
         const uint32_t o_col = wg * kOH;
         const float scale2 = p.scale * kLog2e;
-        const float cap = p.soft_cap;
+        const float cap = CAP ? p.soft_cap : 0.f;
         const float cap2 = cap * kLog2e;
         const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
         uint32_t g = 0, ua = 0;
@@ -789,19 +819,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tmem_ld32(lane_base + c0, s);
                         tmem_ld32(lane_base + c0 + 32, s + 32);
                         tmem_ld_wait();
-                        if (cap > 0.f) {
+                        if (CAP) {
                             float xa = 0.f;
 #pragma unroll
                             for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
-                            // one loop per tanh form, chosen once per tile (warp-uniform)
-                            auto capped = [&](auto tanh_fn) {
+                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
+                                // tanh by its odd Taylor series on the FMA pipe, two lanes
+                                // per instruction: t = x (1 + x^2 (c3 + x^2 (c5 + x^2 c7)))
+                                const float2 k2 = make_float2(scale_over_cap, scale_over_cap);
+                                const float2 c7 = make_float2(kTanhC7, kTanhC7);
+                                const float2 c5 = make_float2(kTanhC5, kTanhC5);
+                                const float2 c3 = make_float2(kTanhC3, kTanhC3);
+                                const float2 one = make_float2(1.f, 1.f);
+                                const float2 cc = make_float2(cap2, cap2);
+                                const float2 nl22 = make_float2(nl2, nl2);
+#pragma unroll
+                                for (int c = 0; c < 64; c += 2) {
+                                    const float2 x = fmul2(make_float2(s[c], s[c + 1]), k2);
+                                    const float2 x2 = fmul2(x, x);
+                                    float2 pp = ffma2(x2, c7, c5);
+                                    pp = ffma2(x2, pp, c3);
+                                    pp = ffma2(x2, pp, one);
+                                    const float2 t = fmul2(x, pp);
+                                    const float2 a = ffma2(cc, t, nl22);
+                                    float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                                    if (partial) {
+                                        e.x = ((vis[c >> 5] >> (c & 31)) & 1u) ? e.x : 0.f;
+                                        e.y = ((vis[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e.y : 0.f;
+                                    }
+                                    const float2 cv = fmul2(e, fsub2(one, fmul2(t, t)));
+                                    pf[c] = cv.x;
+                                    pf[c + 1] = cv.y;
+                                }
+                            } else {
 #pragma unroll
                                 for (int j = 0; j < 64; j += 2) {
                                     float cv[2];
 #pragma unroll
                                     for (int z = 0; z < 2; ++z) {
                                         const int c = j + z;
-                                        const float t = tanh_fn(s[c] * scale_over_cap);
+                                        const float t = tanh_fast(s[c] * scale_over_cap);
                                         float e = ex2_approx(fmaf(cap2, t, nl2));
                                         e = ((vis[c >> 5] >> (c & 31)) & 1u) ? e : 0.f;
                                         cv[z] = e * (1.f - t * t);
@@ -809,11 +866,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                     pf[j] = cv[0];
                                     pf[j + 1] = cv[1];
                                 }
-                            };
-                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall))
-                                capped([](float x) { return tanh_small(x); });
-                            else
-                                capped([](float x) { return tanh_fast(x); });
+                            }
                         } else {
                             // masked logits -> -inf, so that 2^(...) = 0 below
                             if (partial) {
@@ -897,21 +950,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 int bwd_dkdv_smem_bytes(int D) { return D == 64 ? DkdvCfg<64>::kSmem : DkdvCfg<128>::kSmem; }
 int bwd_dq_smem_bytes(int D) { return D == 64 ? DqCfg<64>::kSmem : DqCfg<128>::kSmem; }
 
+template <int D>
+cudaError_t bwd_set_attributes_d()
+{
+    const void *fns[4] = {(const void *)bwd_dkdv_kernel<D, false>, (const void *)bwd_dkdv_kernel<D, true>,
+                          (const void *)bwd_dq_kernel<D, false>, (const void *)bwd_dq_kernel<D, true>};
+    const int smem[4] = {DkdvCfg<D>::kSmem, DkdvCfg<D>::kSmem, DqCfg<D>::kSmem, DqCfg<D>::kSmem};
+    for (int i = 0; i < 4; ++i) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t bwd_tc_set_attributes(int D)
 {
-    cudaError_t e;
-    if (D == 64) {
-        e = cudaFuncSetAttribute(bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 DkdvCfg<64>::kSmem);
-        if (e != cudaSuccess) return e;
-        return cudaFuncSetAttribute(bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    DqCfg<64>::kSmem);
-    }
-    e = cudaFuncSetAttribute(bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkdvCfg<128>::kSmem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                DqCfg<128>::kSmem);
+    return D == 64 ? bwd_set_attributes_d<64>() : bwd_set_attributes_d<128>();
+}
+
+template <int D>
+void launch_dkdv_d(const Problem &p, int grid, const CUtensorMap &q, const CUtensorMap &k,
+                   const CUtensorMap &v, const CUtensorMap &d, const float *nlse2,
+                   const float *delta, __nv_bfloat16 *gk, __nv_bfloat16 *gv, cudaStream_t s)
+{
+    if (p.soft_cap > 0.f)
+        bwd_dkdv_kernel<D, true><<<grid, kBwdThreads, DkdvCfg<D>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gk, gv);
+    else
+        bwd_dkdv_kernel<D, false><<<grid, kBwdThreads, DkdvCfg<D>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gk, gv);
+}
+
+template <int D>
+void launch_dq_d(const Problem &p, int grid, const CUtensorMap &q, const CUtensorMap &k,
+                 const CUtensorMap &v, const CUtensorMap &d, const float *nlse2, const float *delta,
+                 __nv_bfloat16 *gq, cudaStream_t s)
+{
+    if (p.soft_cap > 0.f)
+        bwd_dq_kernel<D, true><<<grid, kBwdThreads, DqCfg<D>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gq);
+    else
+        bwd_dq_kernel<D, false><<<grid, kBwdThreads, DqCfg<D>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gq);
 }
 
 cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *tm_k,
@@ -927,9 +1004,9 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *t
     const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
     __nv_bfloat16 *gk = static_cast<__nv_bfloat16 *>(dk), *gv = static_cast<__nv_bfloat16 *>(dv);
     if (p.D == 64)
-        bwd_dkdv_kernel<64><<<grid, kBwdThreads, DkdvCfg<64>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gk, gv);
+        launch_dkdv_d<64>(p, grid, q, k, v, d, nlse2, delta, gk, gv, s);
     else
-        bwd_dkdv_kernel<128><<<grid, kBwdThreads, DkdvCfg<128>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gk, gv);
+        launch_dkdv_d<128>(p, grid, q, k, v, d, nlse2, delta, gk, gv, s);
     return cudaGetLastError();
 }
 
@@ -945,9 +1022,9 @@ cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_
     const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
     __nv_bfloat16 *gq = static_cast<__nv_bfloat16 *>(dq);
     if (p.D == 64)
-        bwd_dq_kernel<64><<<grid, kBwdThreads, DqCfg<64>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gq);
+        launch_dq_d<64>(p, grid, q, k, v, d, nlse2, delta, gq, s);
     else
-        bwd_dq_kernel<128><<<grid, kBwdThreads, DqCfg<128>::kSmem, s>>>(q, k, v, d, p, nlse2, delta, gq);
+        launch_dq_d<128>(p, grid, q, k, v, d, nlse2, delta, gq, s);
     return cudaGetLastError();
 }
 

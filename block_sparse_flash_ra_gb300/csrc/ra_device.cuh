@@ -308,22 +308,14 @@ __device__ __forceinline__ float tanh_fast(float y)
 }
 
 // tanh on the FMA pipe for |x| <= kTanhSmall: the odd Taylor series of tanh,
-// x - x^3/3 + 2x^5/15 - 17x^7/315.  The series alternates with shrinking
+// x - x^3/3 + 2x^5/15 - 17x^7/315, which the soft-cap paths evaluate two
+// lanes per instruction (fma.rn.f32x2).  The series alternates with shrinking
 // terms there, so the error is below the first omitted term 62x^9/2835,
-// i.e. below 3.4e-7 * |tanh x| at |x| = 0.25.  Callers use it when every |x|
-// of a tile is that small (soft caps are large against typical logits) and
-// tanh_fast otherwise.
+// i.e. below 3.4e-7 * |tanh x| at |x| = 0.25.  The kernels use it when every
+// |x| of a tile is that small (soft caps are large against typical logits)
+// and tanh_fast otherwise.
 constexpr float kTanhSmall = 0.25f;
 constexpr float kTanhC3 = -1.f / 3.f, kTanhC5 = 2.f / 15.f, kTanhC7 = -17.f / 315.f;
-
-__device__ __forceinline__ float tanh_small(float x)
-{
-    const float x2 = x * x;
-    float p = fmaf(x2, kTanhC7, kTanhC5);
-    p = fmaf(x2, p, kTanhC3);
-    p = fmaf(x2, p, 1.f);
-    return x * p;
-}
 
 // max(a, b, c) in one instruction (sm_100 and later).
 __device__ __forceinline__ float max3(float a, float b, float c)
