@@ -89,16 +89,23 @@ __device__ __forceinline__ DkdvBars dkdv_bars(uint8_t *smem)
     return r;
 }
 
+// dK/dV work unit: (kv tile column, kv head, chunk of its query heads); the
+// gc query heads h0 .. h0+gc-1 of the chunk are walked over the column.
 struct ColUnit {
-    int b, kt, hkv, col, cnt;
+    int b, kt, hkv, col, cnt, chunk, h0, gc;
     const int32_t *list; // q tiles of the column
 };
 
 __device__ __forceinline__ ColUnit col_unit(const Problem &p, int u)
 {
     ColUnit x;
-    x.col = p.bwd_order[u / p.Hkv];
-    x.hkv = u % p.Hkv;
+    const int per = p.Hkv * p.hsplit;
+    x.col = p.bwd_order[u / per];
+    const int r = u - (u / per) * per;
+    x.hkv = r / p.hsplit;
+    x.chunk = r - x.hkv * p.hsplit;
+    x.gc = p.G / p.hsplit;
+    x.h0 = x.hkv * p.G + x.chunk * x.gc;
     x.b = x.col / p.nk;
     x.kt = x.col - x.b * p.nk;
     x.cnt = p.bwd_cnt[x.col];
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
     const WaitCtx ctx{abort_flag, p.status, p.timeout_ns};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int U = p.B * p.nk * p.Hkv;
+    const int U = p.B * p.nk * p.Hkv * p.hsplit;
     const int Gd = gridDim.x;
 
     if (threadIdx.x == 0) {
@@ -178,8 +185,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 x.kt * kTile, x.b);
                 }
                 ++uk;
-                for (int gi = 0; ok && gi < p.G; ++gi) {
-                    const int h = x.hkv * p.G + gi;
+                for (int gi = 0; ok && gi < x.gc; ++gi) {
+                    const int h = x.h0 + gi;
                     for (int e = 0; e < x.cnt; ++e) {
                         const int qt = x.list[e];
                         const int st = n % C::kStages;
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!(ok = mbar_wait(bars.kv_full, uk & 1, ctx))) break;
                 tc_fence_after();
                 ++uk;
-                const int steps = p.G * x.cnt;
+                const int steps = x.gc * x.cnt;
                 if (!(ok = wait_stage(n))) break;
                 issue_s(stage_base(n));
                 for (int i = 0; i < steps; ++i, ++n) {
@@ -299,6 +306,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int row = quarter * 32 + lane; // kv row within the tile
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const int c0 = wg * 64;
+        // head split: the chunk's scaled dK and dV go to fp32 partials
+        const bool split = p.hsplit > 1;
+        float *part_k = p.dkv_part;
+        float *part_v = split ? p.dkv_part + (size_t)p.hsplit * p.B * p.Lkv * p.Hkv * D : nullptr;
         constexpr int kOH = D / 2;
         const uint32_t o_col = wg * kOH;
         const float scale2 = p.scale * kLog2e;
@@ -316,10 +327,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const ColUnit x = col_unit(p, u);
             const int kj = x.kt * kTile + row;
             const size_t orow = (((size_t)x.b * p.Lkv + kj) * p.Hkv + x.hkv) * D + o_col;
+            // this chunk's slice of the partials: (hsplit, B, Lkv, Hkv, D)
+            const size_t prow = (size_t)x.chunk * p.B * p.Lkv * p.Hkv * D + orow;
             if (x.cnt > 0) {
                 const int my_pos = p.kv_pos ? p.kv_pos[(size_t)x.b * p.Lkv + kj] : kj;
                 const int my_seg = p.kv_seg ? p.kv_seg[(size_t)x.b * p.Lkv + kj] : 0;
-                const int steps = p.G * x.cnt;
+                const int steps = x.gc * x.cnt;
                 // column-order number of the next partial tile (restarts with each head)
                 const int pbase = p.part_bwd[x.col];
                 int pslot = pbase;
@@ -463,7 +476,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mbar_arrive(bars.ds_ready);
                 }
                 if (!ok) break;
-                // ---- epilogue: this half of dV and scale * dK -> bf16
+                // ---- epilogue: this half of dV and scale * dK -> bf16 (or, with
+                // a head split, the chunk's fp32 partials)
                 if (!(ok = wait_all(bars.acc_ready, ua & 1))) break;
                 ++ua;
                 tc_fence_after();
@@ -473,6 +487,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_ld32(lane_base + C::kColDV + o_col + c * 32, a);
                     tmem_ld32(lane_base + C::kColDK + o_col + c * 32, bk);
                     tmem_ld_wait();
+                    if (split) {
+                        float4 *pk4 = reinterpret_cast<float4 *>(part_k + prow + c * 32);
+                        float4 *pv4 = reinterpret_cast<float4 *>(part_v + prow + c * 32);
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4) {
+                            pv4[k4] = make_float4(a[4 * k4], a[4 * k4 + 1], a[4 * k4 + 2], a[4 * k4 + 3]);
+                            pk4[k4] = make_float4(p.scale * bk[4 * k4], p.scale * bk[4 * k4 + 1],
+                                                  p.scale * bk[4 * k4 + 2], p.scale * bk[4 * k4 + 3]);
+                        }
+                        continue;
+                    }
                     uint4 *dvp = reinterpret_cast<uint4 *>(dv + orow + c * 32);
                     uint4 *dkp = reinterpret_cast<uint4 *>(dk + orow + c * 32);
 #pragma unroll
@@ -489,6 +514,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         dvp[k4] = v;
                         dkp[k4] = w;
                     }
+                }
+            } else if (split) {
+                float4 *pk4 = reinterpret_cast<float4 *>(part_k + prow);
+                float4 *pv4 = reinterpret_cast<float4 *>(part_v + prow);
+                for (int k4 = 0; k4 < kOH / 4; ++k4) {
+                    pk4[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    pv4[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             } else {
                 uint4 *dvp = reinterpret_cast<uint4 *>(dv + orow);
@@ -945,6 +977,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// dk, dv = sum over the hsplit chunks of the fp32 partials, as bf16; one
+// thread per 4 elements (n = B*Lkv*Hkv*D).
+__global__ void __launch_bounds__(256) dkv_reduce_kernel(const float *__restrict__ part, int hsplit,
+                                                         size_t n, __nv_bfloat16 *__restrict__ dk,
+                                                         __nv_bfloat16 *__restrict__ dv)
+{
+    const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= n) return;
+    float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
+    for (int c = 0; c < hsplit; ++c) {
+        const float4 a = *reinterpret_cast<const float4 *>(part + (size_t)c * n + i);
+        const float4 b = *reinterpret_cast<const float4 *>(part + (size_t)(hsplit + c) * n + i);
+        sk = make_float4(sk.x + a.x, sk.y + a.y, sk.z + a.z, sk.w + a.w);
+        sv = make_float4(sv.x + b.x, sv.y + b.y, sv.z + b.z, sv.w + b.w);
+    }
+    *reinterpret_cast<uint2 *>(dk + i) = make_uint2(pack_bf16x2(sk.x, sk.y), pack_bf16x2(sk.z, sk.w));
+    *reinterpret_cast<uint2 *>(dv + i) = make_uint2(pack_bf16x2(sv.x, sv.y), pack_bf16x2(sv.z, sv.w));
+}
+
 } // namespace
 
 int bwd_dkdv_smem_bytes(int D) { return D == 64 ? DkdvCfg<64>::kSmem : DkdvCfg<128>::kSmem; }
@@ -996,7 +1047,7 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *t
                                const float *delta, void *dk, void *dv, int num_sms,
                                cudaStream_t s)
 {
-    const int U = p.B * p.nk * p.Hkv;
+    const int U = p.B * p.nk * p.Hkv * p.hsplit;
     const int grid = U < num_sms ? U : num_sms;
     const CUtensorMap &q = *static_cast<const CUtensorMap *>(tm_q);
     const CUtensorMap &k = *static_cast<const CUtensorMap *>(tm_k);
@@ -1007,6 +1058,11 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *t
         launch_dkdv_d<64>(p, grid, q, k, v, d, nlse2, delta, gk, gv, s);
     else
         launch_dkdv_d<128>(p, grid, q, k, v, d, nlse2, delta, gk, gv, s);
+    if (p.hsplit > 1) {
+        const size_t n = (size_t)p.B * p.Lkv * p.Hkv * p.D;
+        const unsigned blocks = (unsigned)((n / 4 + 255) / 256);
+        dkv_reduce_kernel<<<blocks, 256, 0, s>>>(p.dkv_part, p.hsplit, n, gk, gv);
+    }
     return cudaGetLastError();
 }
 

@@ -161,6 +161,34 @@ struct MaskLayout {
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Query-head chunks of each dK/dV work unit: halved until the units number
+// at least kDkdvTargetUnits (four per SM of a 152-SM GPU; a fixed figure, so
+// that the workspace size does not depend on the device) or the group cannot
+// be split further.  Few kv tiles and kv heads (MQA) otherwise leave too few
+// units, each long, for an even spread over the SMs.
+constexpr long kDkdvTargetUnits = 608;
+
+int dkdv_head_split(const ra_attn_params *p)
+{
+    const long units = (long)p->B * (p->Lkv / RA_TILE) * p->Hkv;
+    const int G = p->Hq / p->Hkv;
+    int hs = 1;
+    while (units * hs < kDkdvTargetUnits && G % (2 * hs) == 0) hs *= 2;
+    return hs;
+}
+
+// Backward workspace: Delta and -lse*log2 e per row, dsinks partials per
+// (b, head, q tile), and with a head split the fp32 dK / dV partials.
+size_t bwd_ws_bytes(const ra_attn_params *p, bool allow_split)
+{
+    const size_t rows = (size_t)p->B * p->Hq * p->Lq;
+    const size_t part = (size_t)p->Hq * p->B * (p->Lq / RA_TILE);
+    size_t n = 2 * up256(rows * 4) + up256(part * 4);
+    const int hs = allow_split ? dkdv_head_split(p) : 1;
+    if (hs > 1) n += up256(2 * (size_t)hs * p->B * p->Lkv * p->Hkv * p->D * 4);
+    return n;
+}
+
 MaskLayout mask_layout(const ra_attn_params *p)
 {
     const size_t B = p->B, nq = p->Lq / RA_TILE, nk = p->Lkv / RA_TILE;
@@ -227,6 +255,8 @@ Problem make_problem(const ra_attn_params *p, const ra_block_mask *m, int *statu
         x.part_cols = m->part_cols;
         x.part_cap = m->part_cap;
     }
+    x.hsplit = 1;
+    x.dkv_part = nullptr;
     x.status = status;
     x.timeout_ns = g_timeout_ns.load();
     return x;
@@ -404,9 +434,7 @@ RA_API int ra_merge_out_lse(float *out, float *lse, const float *block_out, cons
 RA_API size_t ra_attn_bwd_workspace_size(const ra_attn_params *p)
 {
     if (check_params(p) != RA_OK) return 0;
-    const size_t rows = (size_t)p->B * p->Hq * p->Lq;
-    const size_t part = (size_t)p->Hq * p->B * (p->Lq / RA_TILE);
-    return 2 * up256(rows * 4) + up256(part * 4);
+    return bwd_ws_bytes(p, true);
 }
 
 } // extern "C"
@@ -416,15 +444,18 @@ namespace {
 
 enum BwdStage { kPrep = 1, kDkdv = 2, kDq = 4 };
 
-// Backward workspace: Delta rows, the rows' -lse * log2 e, dsinks partials.
+// Backward workspace: Delta rows, the rows' -lse * log2 e, dsinks partials,
+// and the dK / dV partials of a head split (hsplit > 1).
 struct BwdWs {
-    float *delta, *nlse2, *part;
+    float *delta, *nlse2, *part, *dkv_part;
+    int hsplit;
 };
 
 // Shared checks of the backward entry points; on success fills the device
 // cache and the workspace split.
 int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
-               const ra_block_mask *mask, void *ws, size_t ws_bytes, DevCache **dc, BwdWs *w)
+               const ra_block_mask *mask, void *ws, size_t ws_bytes, DevCache **dc, BwdWs *w,
+               bool allow_split = true)
 {
     int rc = check_params(p);
     if (rc) return rc;
@@ -436,7 +467,7 @@ int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
     if (p->D != 64 && p->D != 128) return fail(RA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", p->D);
     if (p->dtype != RA_BF16)
         return fail(RA_ERR_UNSUPPORTED, "the backward is implemented for bf16 inputs");
-    const size_t need = ra_attn_bwd_workspace_size(p);
+    const size_t need = bwd_ws_bytes(p, allow_split);
     if (!ws || ws_bytes < need)
         return fail(RA_ERR_WORKSPACE, "backward workspace has %zu bytes, needs %zu", ws_bytes, need);
     if (reinterpret_cast<uintptr_t>(ws) & 255u)
@@ -447,6 +478,9 @@ int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
     w->delta = reinterpret_cast<float *>(b);
     w->nlse2 = reinterpret_cast<float *>(b + rows_bytes);
     w->part = reinterpret_cast<float *>(b + 2 * rows_bytes);
+    w->hsplit = allow_split ? dkdv_head_split(p) : 1;
+    const size_t part_bytes = up256((size_t)p->Hq * p->B * (p->Lq / RA_TILE) * 4);
+    w->dkv_part = w->hsplit > 1 ? reinterpret_cast<float *>(b + 2 * rows_bytes + part_bytes) : nullptr;
     return RA_OK;
 }
 
@@ -467,9 +501,12 @@ int bwd_tc_kernels(const ra_attn_params *p, DevCache *dc, const Problem &pr, int
     if ((rc = encode_rows(&tv, v, p->B, p->Lkv, p->Hkv, p->D))) return rc;
     if ((rc = encode_rows(&tdo, dout, p->B, p->Lq, p->Hq, p->D))) return rc;
     if (stages & kDkdv) {
-        e = launch_bwd_dkdv_tc(pr, &tq, &tk, &tv, &tdo, w.nlse2, w.delta, dk, dv, dc->num_sms, s);
+        Problem ps = pr;
+        ps.hsplit = w.hsplit;
+        ps.dkv_part = w.dkv_part;
+        e = launch_bwd_dkdv_tc(ps, &tq, &tk, &tv, &tdo, w.nlse2, w.delta, dk, dv, dc->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
-        count(1);
+        count(w.hsplit > 1 ? 2 : 1);
     }
     if (stages & kDq) {
         e = launch_bwd_dq_tc(pr, &tq, &tk, &tv, &tdo, w.nlse2, w.delta, dq, dc->num_sms, s);
@@ -537,12 +574,25 @@ RA_API int ra_attn_bwd(const ra_attn_params *p, const void *q, const void *k, co
                        const ra_block_mask *mask, void *dq, void *dk, void *dv, float *dsinks,
                        void *ws, size_t ws_bytes, ra_stream_t stream)
 {
+    return ra::bwd_all(p, q, k, v, out, lse, dout, mask, dq, dk, dv, dsinks, ws, ws_bytes, stream,
+                       true);
+}
+
+} // extern "C"
+
+namespace ra {
+
+int bwd_all(const ra_attn_params *p, const void *q, const void *k, const void *v,
+            const void *out, const float *lse, const void *dout, const ra_block_mask *mask,
+            void *dq, void *dk, void *dv, float *dsinks, void *ws, size_t ws_bytes,
+            ra_stream_t stream, bool allow_split)
+{
     if (!mask) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
     if (p && p->sinks && !dsinks) return fail(RA_ERR_INVALID_ARG, "dsinks is NULL but sinks are given");
     const void *ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
     DevCache *dc = nullptr;
     BwdWs w{};
-    int rc = bwd_common(p, ptrs, 9, mask, ws, ws_bytes, &dc, &w);
+    int rc = bwd_common(p, ptrs, 9, mask, ws, ws_bytes, &dc, &w, allow_split);
     if (rc) return rc;
     const Problem pr = make_problem(p, mask, dc->status);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -551,6 +601,12 @@ RA_API int ra_attn_bwd(const ra_attn_params *p, const void *q, const void *k, co
     count(p->sinks ? 2 : 1);
     return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, dout, w, dq, dk, dv, s);
 }
+
+size_t bwd_ws_min_bytes(const ra_attn_params *p) { return bwd_ws_bytes(p, false); }
+
+} // namespace ra
+
+extern "C" {
 
 RA_API int ra_permute_tokens(const void *in, void *out, int B, int L, size_t row_bytes,
                              int n_shards, ra_stream_t stream)

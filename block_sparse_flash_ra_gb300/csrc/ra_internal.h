@@ -37,6 +37,12 @@ struct Problem {
     const int32_t *part_fwd, *part_bwd;
     const uint32_t *part_rows, *part_cols; // (part_cap, 128, 4) words each
     int part_cap;
+    // dK/dV schedule: each kv head's G query heads are split into hsplit
+    // chunks of units; with hsplit > 1 each chunk stores its scaled dK and
+    // dV as fp32 partials (dkv_part: dK then dV, each (hsplit, B, Lkv, Hkv, D))
+    // that a reduction sums into dk, dv
+    int hsplit;
+    float *dkv_part;
     // failure reporting
     int *status;
     uint64_t timeout_ns;
@@ -83,6 +89,14 @@ int bwd_dq_smem_bytes(int D);
 cudaError_t fwd_tc_set_attributes(int D);
 cudaError_t bwd_tc_set_attributes(int D);
 cudaError_t simt_set_attributes(int D);
+
+// ra_attn_bwd with the dK/dV head split allowed or not (without it the
+// workspace needs only bwd_ws_min_bytes).
+int bwd_all(const ra_attn_params *p, const void *q, const void *k, const void *v,
+            const void *out, const float *lse, const void *dout, const ra_block_mask *mask,
+            void *dq, void *dk, void *dv, float *dsinks, void *ws, size_t ws_bytes,
+            ra_stream_t stream, bool allow_split);
+size_t bwd_ws_min_bytes(const ra_attn_params *p);
 
 // Records `msg` as this thread's last error message and returns `code`.
 int set_last_error(int code, const char *msg);

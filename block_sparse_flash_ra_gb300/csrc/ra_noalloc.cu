@@ -64,8 +64,9 @@ RA_API int ra_attn_bwd_noalloc(const ra_attn_params *p, const void *q, const voi
                                void *dv, float *dsinks, ra_stream_t stream)
 {
     if (!p) return ra::set_last_error(RA_ERR_INVALID_ARG, "params is NULL");
-    const size_t need = ra_attn_bwd_workspace_size(p);
-    if (need == 0) return RA_ERR_INVALID_ARG; // the size query recorded why
+    if (ra_attn_bwd_workspace_size(p) == 0) return RA_ERR_INVALID_ARG; // the size query recorded why
+    // the built-in scratch serves the schedule without a dK/dV head split
+    const size_t need = ra::bwd_ws_min_bytes(p);
     if (need > ra::kScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof(msg),
@@ -79,8 +80,8 @@ RA_API int ra_attn_bwd_noalloc(const ra_attn_params *p, const void *q, const voi
     if (rc) return rc;
     // Every value the backward reads from its workspace is written earlier in
     // the same call, so nothing in the scratch has to start at zero.
-    return ra_attn_bwd(p, q, k, v, out, lse, dout, mask, dq, dk, dv, dsinks, scratch,
-                       ra::kScratchBytes, stream);
+    return ra::bwd_all(p, q, k, v, out, lse, dout, mask, dq, dk, dv, dsinks, scratch,
+                       ra::kScratchBytes, stream, false);
 }
 
 } // extern "C"

@@ -247,7 +247,13 @@ RA_API int ra_merge_out_lse(float *out, float *lse, const float *block_out,
                             ra_stream_t stream);
 
 /* Workspace bytes of ra_attn_bwd: per-row Delta = <dO, O> and per-row
- * -lse * log2(e) (fp32, B*Hq*Lq each) and per-tile partial sums of dsinks. */
+ * -lse * log2(e) (fp32, B*Hq*Lq each), per-tile partial sums of dsinks, and,
+ * when the kv tiles times kv heads are few (B * Lkv/128 * Hkv < 608, e.g.
+ * MQA), fp32 partial dK and dV of each chunk of query heads (2 * hs * B * Lkv
+ * * Hkv * D floats, hs = the number of chunks, a power of two dividing
+ * Hq/Hkv): the dK/dV stage then splits each kv head's query heads over hs
+ * work units, so that the units spread evenly over the SMs, and sums the
+ * partials afterwards. */
 RA_API size_t ra_attn_bwd_workspace_size(const ra_attn_params *p);
 
 /*
@@ -297,8 +303,9 @@ RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k,
  *   The workspace comes from a fixed array of ra_attn_bwd_noalloc_max_workspace()
  *   bytes (8 MiB) in the library's device memory, held by every GPU that loads
  *   the library until the process exits.  Problems whose
- *   ra_attn_bwd_workspace_size() exceeds it fail with RA_ERR_WORKSPACE
- *   (roughly B * Hq * Lq above one million query rows); use ra_attn_bwd then.
+ *   workspace exceeds it fail with RA_ERR_WORKSPACE (roughly B * Hq * Lq
+ *   above one million query rows; this call never splits the query heads of
+ *   the dK/dV stage, so it needs no dK/dV partials); use ra_attn_bwd then.
  *   Nothing is allocated: no cudaMalloc / cudaFree is ever called.
  *   The first call on a device looks up the array's device address on that
  *   device (a synchronous runtime query); make that first call before any
