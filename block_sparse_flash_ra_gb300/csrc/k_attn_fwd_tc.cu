@@ -506,12 +506,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     tiles_done += hi - lo;
                     // the unit's last non-empty shard merges straight into the bf16 output
                     const bool last = tiles_done == x.cnt;
-                    if (!(ok = wait_pv_upto(g))) break;
-                    tc_fence_after();
+                    // this half's row sum is posted before the wait for the shard's
+                    // last PV product, so that the two waits overlap
                     float *xs = xsum + (nshard & 1) * 256;
                     ++nshard;
                     xs[wg * 128 + row] = l;
-                    if (!(ok = pair_sync())) break;
+                    mbar_arrive(bars.xsync + quarter);
+                    if (!(ok = wait_pv_upto(g))) break;
+                    tc_fence_after();
+                    if (!(ok = wait_all(bars.xsync + quarter, (xph++) & 1))) break;
                     l += xs[(wg ^ 1) * 128 + row];
                     float m_fin = m_ref, fac = 1.f;
                     if (sink_here) {
