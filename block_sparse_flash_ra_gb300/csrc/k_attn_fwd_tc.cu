@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         // empty shard: partial is (0, -inf), or (0, sink) at t = 0
                         if (sink_here) {
                             const float ls = sink2 * kLn2;
-                            lse_run = (lse_run == -INFINITY) ? ls : lse_run + softplus_f(ls - lse_run);
+                            lse_run = (lse_run == -INFINITY) ? ls : lse_run + softplus_fast(ls - lse_run);
                         }
                         continue;
                     }
@@ -524,14 +524,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     }
                     float lse_s, inv;
                     if (l > 0.f) {
-                        lse_s = (m_fin + log2f(l)) * kLn2;
-                        inv = fac / l;
+                        lse_s = (m_fin + lg2_approx(l)) * kLn2;
+                        inv = fac * rcp_approx(l);
                     } else {
                         lse_s = -INFINITY;
                         inv = 0.f;
                     }
                     const bool first = (lse_run == -INFINITY);
-                    const float w = first ? 1.f : sigmoid_f(lse_s - lse_run);
+                    const float w = first ? 1.f : sigmoid_fast(lse_s - lse_run);
 #pragma unroll
                     for (int c = 0; c < kOH / 32; ++c) {
                         float a[32], cur[32];
@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     }
                     if (!last) tmem_st_wait();
                     out_written = last;
-                    lse_run = first ? lse_s : lse_run + softplus_f(lse_s - lse_run);
+                    lse_run = first ? lse_s : lse_run + softplus_fast(lse_s - lse_run);
                     orun_set = true;
                 }
                 if (!ok) break;

@@ -140,16 +140,19 @@ __device__ __forceinline__ bool wait_drain(uint64_t *bar, uint32_t parity, uint6
     return true;
 }
 
-__device__ __forceinline__ float sigmoid_f(float x)
+// sigmoid and softplus of the ring merge (_update_out_and_lse) from the
+// approximate base-2 exponent, logarithm and reciprocal instructions
+// (relative errors near 2^-22): sigmoid(x) = 1 / (1 + 2^(-x log2 e)),
+// softplus(x) = max(x, 0) + ln 2 * log2(1 + 2^(-|x| log2 e)).  Both give 0
+// at x = -inf and no NaN at +-inf.
+__device__ __forceinline__ float sigmoid_fast(float x)
 {
-    if (x >= 0.f) return 1.f / (1.f + expf(-x));
-    const float e = expf(x);
-    return e / (1.f + e);
+    return rcp_approx(1.f + ex2_approx(-x * kLog2e));
 }
 
-__device__ __forceinline__ float softplus_f(float x)
+__device__ __forceinline__ float softplus_fast(float x)
 {
-    return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+    return fmaxf(x, 0.f) + kLn2 * lg2_approx(1.f + ex2_approx(-fabsf(x) * kLog2e));
 }
 
 constexpr uint64_t kDrainNs = 100000000ull; // 100 ms
