@@ -27,6 +27,7 @@
 // The dkdv kernel recomputes S and dP per tile and the dq kernel recomputes
 // them again: 7 tile products instead of 5, in exchange for no fp32 atomics.
 #include <math.h>
+#include <type_traits>
 
 #include "ra_sched.cuh"
 
@@ -369,39 +370,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             float xa = 0.f;
 #pragma unroll
                             for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
-                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
+                            const bool tiny = __all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny) != 0;
+                            if (tiny || __all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
                                 // tanh by its odd Taylor series on the FMA pipe, two lanes
-                                // per instruction: t = x (1 + x^2 (c3 + x^2 (c5 + x^2 c7)))
+                                // per instruction: t = x (1 + x^2 (c3 + x^2 (c5 + x^2 c7))),
+                                // or t = x (1 + c3 x^2) when every |x| < 1/8
                                 const float2 k2 = make_float2(scale_over_cap, scale_over_cap);
                                 const float2 c7 = make_float2(kTanhC7, kTanhC7);
                                 const float2 c5 = make_float2(kTanhC5, kTanhC5);
                                 const float2 c3 = make_float2(kTanhC3, kTanhC3);
                                 const float2 one = make_float2(1.f, 1.f);
                                 const float2 cc = make_float2(cap2, cap2);
+                                auto run = [&](auto tiny_c) {
+                                    constexpr bool kTiny = decltype(tiny_c)::value;
 #pragma unroll
-                                for (int j = 0; j < 64; j += 4) {
-                                    const float4 lv = l4[j >> 2];
-                                    const float2 la[2] = {make_float2(lv.x, lv.y), make_float2(lv.z, lv.w)};
+                                    for (int j = 0; j < 64; j += 4) {
+                                        const float4 lv = l4[j >> 2];
+                                        const float2 la[2] = {make_float2(lv.x, lv.y), make_float2(lv.z, lv.w)};
 #pragma unroll
-                                    for (int h = 0; h < 2; ++h) {
-                                        const int c = j + 2 * h;
-                                        const float2 x = fmul2(make_float2(s[c], s[c + 1]), k2);
-                                        const float2 x2 = fmul2(x, x);
-                                        float2 pp = ffma2(x2, c7, c5);
-                                        pp = ffma2(x2, pp, c3);
-                                        pp = ffma2(x2, pp, one);
-                                        const float2 t = fmul2(x, pp);
-                                        const float2 a = ffma2(cc, t, la[h]);
-                                        float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-                                        if (partial) {
-                                            e.x = ((vis[c >> 5] >> (c & 31)) & 1u) ? e.x : 0.f;
-                                            e.y = ((vis[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e.y : 0.f;
+                                        for (int h = 0; h < 2; ++h) {
+                                            const int c = j + 2 * h;
+                                            const float2 x = fmul2(make_float2(s[c], s[c + 1]), k2);
+                                            const float2 x2 = fmul2(x, x);
+                                            float2 pp;
+                                            if (kTiny) {
+                                                pp = ffma2(x2, c3, one);
+                                            } else {
+                                                pp = ffma2(x2, c7, c5);
+                                                pp = ffma2(x2, pp, c3);
+                                                pp = ffma2(x2, pp, one);
+                                            }
+                                            const float2 t = fmul2(x, pp);
+                                            const float2 a = ffma2(cc, t, la[h]);
+                                            float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                                            if (partial) {
+                                                e.x = ((vis[c >> 5] >> (c & 31)) & 1u) ? e.x : 0.f;
+                                                e.y = ((vis[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e.y : 0.f;
+                                            }
+                                            const float2 cr = fmul2(e, fsub2(one, fmul2(t, t)));
+                                            pk[c >> 1] = pack_bf16x2(e.x, e.y);
+                                            pc[c >> 1] = pack_bf16x2(cr.x, cr.y);
                                         }
-                                        const float2 cr = fmul2(e, fsub2(one, fmul2(t, t)));
-                                        pk[c >> 1] = pack_bf16x2(e.x, e.y);
-                                        pc[c >> 1] = pack_bf16x2(cr.x, cr.y);
                                     }
-                                }
+                                };
+                                if (tiny) run(std::true_type{});
+                                else run(std::false_type{});
                             } else {
 #pragma unroll
                                 for (int j = 0; j < 64; j += 4) {
@@ -855,9 +868,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             float xa = 0.f;
 #pragma unroll
                             for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
-                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
+                            const bool tiny = __all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny) != 0;
+                            if (tiny || __all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
                                 // tanh by its odd Taylor series on the FMA pipe, two lanes
-                                // per instruction: t = x (1 + x^2 (c3 + x^2 (c5 + x^2 c7)))
+                                // per instruction: t = x (1 + x^2 (c3 + x^2 (c5 + x^2 c7))),
+                                // or t = x (1 + c3 x^2) when every |x| < 1/8
                                 const float2 k2 = make_float2(scale_over_cap, scale_over_cap);
                                 const float2 c7 = make_float2(kTanhC7, kTanhC7);
                                 const float2 c5 = make_float2(kTanhC5, kTanhC5);
@@ -865,24 +880,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 const float2 one = make_float2(1.f, 1.f);
                                 const float2 cc = make_float2(cap2, cap2);
                                 const float2 nl22 = make_float2(nl2, nl2);
+                                auto run = [&](auto tiny_c) {
+                                    constexpr bool kTiny = decltype(tiny_c)::value;
 #pragma unroll
-                                for (int c = 0; c < 64; c += 2) {
-                                    const float2 x = fmul2(make_float2(s[c], s[c + 1]), k2);
-                                    const float2 x2 = fmul2(x, x);
-                                    float2 pp = ffma2(x2, c7, c5);
-                                    pp = ffma2(x2, pp, c3);
-                                    pp = ffma2(x2, pp, one);
-                                    const float2 t = fmul2(x, pp);
-                                    const float2 a = ffma2(cc, t, nl22);
-                                    float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-                                    if (partial) {
-                                        e.x = ((vis[c >> 5] >> (c & 31)) & 1u) ? e.x : 0.f;
-                                        e.y = ((vis[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e.y : 0.f;
+                                    for (int c = 0; c < 64; c += 2) {
+                                        const float2 x = fmul2(make_float2(s[c], s[c + 1]), k2);
+                                        const float2 x2 = fmul2(x, x);
+                                        float2 pp;
+                                        if (kTiny) {
+                                            pp = ffma2(x2, c3, one);
+                                        } else {
+                                            pp = ffma2(x2, c7, c5);
+                                            pp = ffma2(x2, pp, c3);
+                                            pp = ffma2(x2, pp, one);
+                                        }
+                                        const float2 t = fmul2(x, pp);
+                                        const float2 a = ffma2(cc, t, nl22);
+                                        float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                                        if (partial) {
+                                            e.x = ((vis[c >> 5] >> (c & 31)) & 1u) ? e.x : 0.f;
+                                            e.y = ((vis[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e.y : 0.f;
+                                        }
+                                        const float2 cv = fmul2(e, fsub2(one, fmul2(t, t)));
+                                        pf[c] = cv.x;
+                                        pf[c + 1] = cv.y;
                                     }
-                                    const float2 cv = fmul2(e, fsub2(one, fmul2(t, t)));
-                                    pf[c] = cv.x;
-                                    pf[c + 1] = cv.y;
-                                }
+                                };
+                                if (tiny) run(std::true_type{});
+                                else run(std::false_type{});
                             } else {
 #pragma unroll
                                 for (int j = 0; j < 64; j += 2) {

@@ -406,7 +406,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             float xa = 0.f;
 #pragma unroll
                             for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
-                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
+                            if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny)) {
+                                // cap * log2 e * (x - x^3/3), x = s * scale / cap, as
+                                // s * (A + B s^2): three instructions per pair of logits
+                                const float kk = scale_over_cap;
+                                const float2 A = make_float2(cap2 * kk, cap2 * kk);
+                                const float2 B = make_float2(cap2 * kTanhC3 * kk * kk * kk,
+                                                             cap2 * kTanhC3 * kk * kk * kk);
+#pragma unroll
+                                for (int j = 0; j < 64; j += 2) {
+                                    const float2 v = make_float2(s[j], s[j + 1]);
+                                    const float2 r = fmul2(v, ffma2(fmul2(v, v), B, A));
+                                    s[j] = r.x;
+                                    s[j + 1] = r.y;
+                                }
+                            } else if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
                                 // cap * log2 e * tanh(x), x = s / cap * scale, on the FMA pipe:
                                 // x * (d1 + x^2 (d3 + x^2 (d5 + x^2 d7))), d = cap2 * c
                                 const float2 k2 = make_float2(scale_over_cap, scale_over_cap);

@@ -322,6 +322,11 @@ __device__ __forceinline__ float tanh_fast(float y)
 // |x| of a tile is that small (soft caps are large against typical logits)
 // and tanh_fast otherwise.
 constexpr float kTanhSmall = 0.25f;
+// Below |x| = 1/8 the kernels keep only x - x^3/3: the first omitted term,
+// 2x^5/15, is below 4.1e-6 there (3.3e-5 of tanh x), which a soft cap of up to
+// ~100 turns into less than 6e-4 in the base-2 logit -- under the bf16
+// rounding of P (2^-9 relative).
+constexpr float kTanhTiny = 0.125f;
 constexpr float kTanhC3 = -1.f / 3.f, kTanhC5 = 2.f / 15.f, kTanhC7 = -17.f / 315.f;
 
 // max(a, b, c) in one instruction (sm_100 and later).
