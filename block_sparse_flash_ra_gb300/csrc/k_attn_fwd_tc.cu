@@ -21,6 +21,8 @@
 //   warp 8     TMA producer: Q once per work unit, K and V tiles into a
 //              rings of shared-memory stages (2 for K, 3 for V at D = 128)
 //   warp 9     TMEM allocator and single-thread MMA issuer
+//   warps 10-11 no role: with warps 8-9 they form the warpgroup that hands
+//              registers to the softmax warpgroups (setmaxnreg)
 // TMEM (512 columns x 128 lanes, fp32):
 //   [0,128)   S buffer 0   (P of the tile, bf16, overwrites columns [0,32)
 //                           and [64,96): each half over columns it has read)
@@ -122,7 +124,15 @@ __device__ __forceinline__ void shard_range(const Problem &p, const Unit &x, int
 constexpr int kSoftmaxThreads = 256; // warps 0-7
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;
+// setmaxnreg split: 256 x 224 + 128 x 56 = 64512 = 384 x 168, the block's
+// registers at launch (the kernel is built for 168 per thread; the launcher
+// checks that count before the first launch)
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kSoftmaxRegs = 224;
+constexpr uint32_t kSideRegs = 56;
+static_assert(256 * kSoftmaxRegs + 128 * kSideRegs <= kFwdThreads * kLaunchRegs,
+              "register split exceeds the block's launch registers");
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -179,127 +189,131 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            uint32_t g = 0, uq = 0;
-            uint32_t k_issued[C::kMaxStages] = {}, v_issued[C::kMaxStages] = {};
-            bool ok = true;
-            for (int r = 0; ok && r * G < U; ++r) {
-                const int u = unit_index(r, blockIdx.x, G);
-                if (u >= U) continue;
-                const Unit x = unit_of(p, u);
-                if (x.cnt == 0) continue;
-                if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
-                mbar_expect_tx(bars.q_full, C::kTileBytes);
-                for (int hb = 0; hb < D / 64; ++hb)
-                    tma_load_4d(smem + C::kQOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h,
-                                x.qt * kTile, x.b);
-                ++uq;
-                const int g_kv = x.h / p.G;
-                for (int t = 0; ok && t < p.N; ++t) {
-                    int lo, hi;
-                    shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
-                    for (int e = lo; e < hi; ++e) {
-                        const int kt = x.list[e];
-                        const int sk = g % C::kKStages;
-                        if (!(ok = mbar_wait(bars.k_empty + sk, ((g / C::kKStages) & 1) ^ 1, ctx))) break;
-                        mbar_expect_tx(bars.k_full + sk, C::kTileBytes);
-                        for (int hb = 0; hb < D / 64; ++hb)
-                            tma_load_4d(smem + C::kKOff + sk * C::kTileBytes + hb * 16384, &tm_k,
-                                        bars.k_full + sk, hb * 64, g_kv, kt * kTile, x.b);
-                        ++k_issued[sk];
-                        const int sv = g % C::kVStages;
-                        if (!(ok = mbar_wait(bars.v_empty + sv, ((g / C::kVStages) & 1) ^ 1, ctx))) break;
-                        mbar_expect_tx(bars.v_full + sv, C::kTileBytes);
-                        for (int hb = 0; hb < D / 64; ++hb)
-                            tma_load_4d(smem + C::kVOff + sv * C::kTileBytes + hb * 16384, &tm_v,
-                                        bars.v_full + sv, hb * 64, g_kv, kt * kTile, x.b);
-                        ++v_issued[sv];
-                        ++g;
-                    }
-                }
-            }
-            if (!ok) {
-                // let the copies already issued land before the CTA exits
-                for (int s = 0; s < C::kKStages; ++s)
-                    if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
-                for (int s = 0; s < C::kVStages; ++s)
-                    if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
-                if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t q_base = smem_u32(smem + C::kQOff);
-            const uint32_t k_base = smem_u32(smem + C::kKOff);
-            const uint32_t v_base = smem_u32(smem + C::kVOff);
-            uint32_t g = 0, uq = 0;
-            bool have_prev = false, prev_first = false;
-            uint32_t prev_g = 0;
-            bool ok = true;
-            auto issue_pv = [&](uint32_t pg, bool first) -> bool {
-                const int sb = pg & 1;
-                if (!mbar_wait(bars.p_full + sb, (pg >> 1) & 1, ctx)) return false;
-                const int st = pg % C::kVStages;
-                if (!mbar_wait(bars.v_full + st, (pg / C::kVStages) & 1, ctx)) return false;
-                tc_fence_after();
-                const uint32_t vb = v_base + st * C::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, 16384, 1024);
-                    // P of kv rows 16kk..16kk+15: the half of warps 0-3 (kk < 4) sits
-                    // in columns [0,32) of the S buffer, the other half in [64,96)
-                    const uint32_t acol = sb * 128 + kk * 8 + (kk >= 4 ? 32 : 0);
-                    mma_ts(tmem + C::kColO, tmem + acol, bdesc, C::kIdescPV,
-                           (kk > 0 || !first) ? 1u : 0u);
-                }
-                tc_commit(bars.v_empty + st);
-                tc_commit(bars.pv_done);
-                return true;
-            };
-            for (int r = 0; ok && r * G < U; ++r) {
-                const int u = unit_index(r, blockIdx.x, G);
-                if (u >= U) continue;
-                const Unit x = unit_of(p, u);
-                if (x.cnt == 0) continue;
-                if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
-                tc_fence_after();
-                ++uq;
-                int done = 0;
-                for (int t = 0; ok && t < p.N; ++t) {
-                    int lo, hi;
-                    shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
-                    for (int e = lo; e < hi; ++e) {
-                        const int st = g % C::kKStages;
-                        if (!(ok = mbar_wait(bars.k_full + st, (g / C::kKStages) & 1, ctx))) break;
-                        tc_fence_after();
-                        const int sb = g & 1;
-                        const uint32_t kb = k_base + st * C::kTileBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tmem + sb * 128, sdesc_sw128(q_base + off, 16, 1024),
-                                   sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+    if (warp >= kProducerWarp) {
+        regs_shrink<kSideRegs>();
+        if (warp == kProducerWarp) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                uint32_t g = 0, uq = 0;
+                uint32_t k_issued[C::kMaxStages] = {}, v_issued[C::kMaxStages] = {};
+                bool ok = true;
+                for (int r = 0; ok && r * G < U; ++r) {
+                    const int u = unit_index(r, blockIdx.x, G);
+                    if (u >= U) continue;
+                    const Unit x = unit_of(p, u);
+                    if (x.cnt == 0) continue;
+                    if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
+                    mbar_expect_tx(bars.q_full, C::kTileBytes);
+                    for (int hb = 0; hb < D / 64; ++hb)
+                        tma_load_4d(smem + C::kQOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h,
+                                    x.qt * kTile, x.b);
+                    ++uq;
+                    const int g_kv = x.h / p.G;
+                    for (int t = 0; ok && t < p.N; ++t) {
+                        int lo, hi;
+                        shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
+                        for (int e = lo; e < hi; ++e) {
+                            const int kt = x.list[e];
+                            const int sk = g % C::kKStages;
+                            if (!(ok = mbar_wait(bars.k_empty + sk, ((g / C::kKStages) & 1) ^ 1, ctx))) break;
+                            mbar_expect_tx(bars.k_full + sk, C::kTileBytes);
+                            for (int hb = 0; hb < D / 64; ++hb)
+                                tma_load_4d(smem + C::kKOff + sk * C::kTileBytes + hb * 16384, &tm_k,
+                                            bars.k_full + sk, hb * 64, g_kv, kt * kTile, x.b);
+                            ++k_issued[sk];
+                            const int sv = g % C::kVStages;
+                            if (!(ok = mbar_wait(bars.v_empty + sv, ((g / C::kVStages) & 1) ^ 1, ctx))) break;
+                            mbar_expect_tx(bars.v_full + sv, C::kTileBytes);
+                            for (int hb = 0; hb < D / 64; ++hb)
+                                tma_load_4d(smem + C::kVOff + sv * C::kTileBytes + hb * 16384, &tm_v,
+                                            bars.v_full + sv, hb * 64, g_kv, kt * kTile, x.b);
+                            ++v_issued[sv];
+                            ++g;
                         }
-                        tc_commit(bars.k_empty + st);
-                        tc_commit(bars.s_full + sb);
-                        if (++done == x.cnt) tc_commit(bars.q_empty);
-                        if (have_prev && !(ok = issue_pv(prev_g, prev_first))) break;
-                        have_prev = true;
-                        prev_g = g;
-                        prev_first = (e == lo);
-                        ++g;
                     }
                 }
+                if (!ok) {
+                    // let the copies already issued land before the CTA exits
+                    for (int s = 0; s < C::kKStages; ++s)
+                        if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
+                    for (int s = 0; s < C::kVStages; ++s)
+                        if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
+                    if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
+                }
             }
-            if (ok && have_prev) ok = issue_pv(prev_g, prev_first);
-            // all issued MMAs must finish before TMEM is released
-            tc_commit(bars.drain);
-            wait_drain(bars.drain, 0, kDrainNs);
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                const uint32_t q_base = smem_u32(smem + C::kQOff);
+                const uint32_t k_base = smem_u32(smem + C::kKOff);
+                const uint32_t v_base = smem_u32(smem + C::kVOff);
+                uint32_t g = 0, uq = 0;
+                bool have_prev = false, prev_first = false;
+                uint32_t prev_g = 0;
+                bool ok = true;
+                auto issue_pv = [&](uint32_t pg, bool first) -> bool {
+                    const int sb = pg & 1;
+                    if (!mbar_wait(bars.p_full + sb, (pg >> 1) & 1, ctx)) return false;
+                    const int st = pg % C::kVStages;
+                    if (!mbar_wait(bars.v_full + st, (pg / C::kVStages) & 1, ctx)) return false;
+                    tc_fence_after();
+                    const uint32_t vb = v_base + st * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, 16384, 1024);
+                        // P of kv rows 16kk..16kk+15: the half of warps 0-3 (kk < 4) sits
+                        // in columns [0,32) of the S buffer, the other half in [64,96)
+                        const uint32_t acol = sb * 128 + kk * 8 + (kk >= 4 ? 32 : 0);
+                        mma_ts(tmem + C::kColO, tmem + acol, bdesc, C::kIdescPV,
+                               (kk > 0 || !first) ? 1u : 0u);
+                    }
+                    tc_commit(bars.v_empty + st);
+                    tc_commit(bars.pv_done);
+                    return true;
+                };
+                for (int r = 0; ok && r * G < U; ++r) {
+                    const int u = unit_index(r, blockIdx.x, G);
+                    if (u >= U) continue;
+                    const Unit x = unit_of(p, u);
+                    if (x.cnt == 0) continue;
+                    if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                    tc_fence_after();
+                    ++uq;
+                    int done = 0;
+                    for (int t = 0; ok && t < p.N; ++t) {
+                        int lo, hi;
+                        shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
+                        for (int e = lo; e < hi; ++e) {
+                            const int st = g % C::kKStages;
+                            if (!(ok = mbar_wait(bars.k_full + st, (g / C::kKStages) & 1, ctx))) break;
+                            tc_fence_after();
+                            const int sb = g & 1;
+                            const uint32_t kb = k_base + st * C::kTileBytes;
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                mma_ss(tmem + sb * 128, sdesc_sw128(q_base + off, 16, 1024),
+                                       sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+                            }
+                            tc_commit(bars.k_empty + st);
+                            tc_commit(bars.s_full + sb);
+                            if (++done == x.cnt) tc_commit(bars.q_empty);
+                            if (have_prev && !(ok = issue_pv(prev_g, prev_first))) break;
+                            have_prev = true;
+                            prev_g = g;
+                            prev_first = (e == lo);
+                            ++g;
+                        }
+                    }
+                }
+                if (ok && have_prev) ok = issue_pv(prev_g, prev_first);
+                // all issued MMAs must finish before TMEM is released
+                tc_commit(bars.drain);
+                wait_drain(bars.drain, 0, kDrainNs);
+            }
         }
     } else {
+        regs_grow<kSoftmaxRegs>();
         // ------------------------------------------------------------ softmax
         // Two warpgroups split the 128 S columns of every query row: warps
         // 0-3 take columns 0-63, warps 4-7 columns 64-127.  Warp w may only
@@ -633,11 +647,16 @@ int fwd_tc_smem_bytes(int D)
 
 cudaError_t fwd_tc_set_attributes(int D)
 {
-    if (D == 64)
-        return cudaFuncSetAttribute(fwd_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    FwdCfg<64>::kSmem);
-    return cudaFuncSetAttribute(fwd_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FwdCfg<128>::kSmem);
+    const void *fn = D == 64 ? reinterpret_cast<const void *>(fwd_tc_kernel<64>)
+                             : reinterpret_cast<const void *>(fwd_tc_kernel<128>);
+    // the setmaxnreg split draws on the registers the block is launched with:
+    // refuse to run a build that gives each thread fewer than it assumes
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                D == 64 ? FwdCfg<64>::kSmem : FwdCfg<128>::kSmem);
 }
 
 cudaError_t launch_fwd_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,

@@ -283,6 +283,21 @@ __device__ __forceinline__ void tmem_st_wait()
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Register reallocation between warpgroups (setmaxnreg): every warp of the
+// warpgroup executes the same instruction.  The increases of all warpgroups
+// must fit in the registers the block was launched with (threads x the
+// kernel's per-thread count); the launcher checks that before launching.
+template <uint32_t N>
+__device__ __forceinline__ void regs_grow()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_shrink()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ----------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x)
 {
