@@ -472,15 +472,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tmem_ld_wait();
                         const float4 *d4 = reinterpret_cast<const float4 *>(dl_s);
                         uint32_t dk2[32];
+                        // (dP - Delta) rounded to bf16, times the bf16 Pc, two lanes per
+                        // instruction
 #pragma unroll
                         for (int j = 0; j < 64; j += 4) {
                             const float4 dl = d4[j >> 2];
-                            const float2 r0 = fmul2(unpack_bf16x2(pc[j >> 1]),
-                                                    fsub2(make_float2(dpv[j], dpv[j + 1]), make_float2(dl.x, dl.y)));
-                            const float2 r1 = fmul2(unpack_bf16x2(pc[(j >> 1) + 1]),
-                                                    fsub2(make_float2(dpv[j + 2], dpv[j + 3]), make_float2(dl.z, dl.w)));
-                            dk2[j >> 1] = pack_bf16x2(r0.x, r0.y);
-                            dk2[(j >> 1) + 1] = pack_bf16x2(r1.x, r1.y);
+                            const float2 r0 = fsub2(make_float2(dpv[j], dpv[j + 1]), make_float2(dl.x, dl.y));
+                            const float2 r1 = fsub2(make_float2(dpv[j + 2], dpv[j + 3]), make_float2(dl.z, dl.w));
+                            dk2[j >> 1] = mul_bf16x2(pc[j >> 1], pack_bf16x2(r0.x, r0.y));
+                            dk2[(j >> 1) + 1] = mul_bf16x2(pc[(j >> 1) + 1], pack_bf16x2(r1.x, r1.y));
                         }
                         tmem_st32(lane_base + C::kColDP + c0, dk2);
                     }

@@ -398,6 +398,14 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b)
     return d;
 }
 
+// Product of two packed bf16 pairs, each lane rounded to bf16.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // The two bf16 halves of a packed pair, widened to fp32 (exact).
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w)
 {
