@@ -128,6 +128,7 @@ FWD_CASES = {
     # |s * scale| / cap mostly in [1/8, 1/4): the degree-7 tanh series
     "cap20": W(soft_cap=20.0, seed=21),
     "d64": W(D=64, seed=17),
+    "d64_cap50_sinks": W(D=64, soft_cap=50.0, sinks=True, seed=22),
     "d64_fp32": W(D=64, dtype="fp32", seed=18, L=512),
     "zigzag_n4": W(zigzag=True, n_shards=4, seed=19),
     "b2_gqa": W(B=2, Hq=6, Hkv=3, seed=20, L=768, n_shards=3),
@@ -354,6 +355,7 @@ BWD_CASES = {
     "d64_zigzag": W(D=64, L=512, zigzag=True, n_shards=2, seed=34),
     "mqa_sinks_cap50": W(Hq=4, Hkv=1, is_mqa=True, sinks=True, soft_cap=50.0, L=512, seed=37),
     "cap20": W(Hq=4, Hkv=2, soft_cap=20.0, L=512, seed=39),
+    "d64_cap20_sinks": W(D=64, Hq=4, Hkv=2, soft_cap=20.0, sinks=True, L=512, seed=40),
     "ragged_n5_b2": W(B=2, Hq=6, Hkv=2, L=640, n_shards=5, seed=38),
 }
 
