@@ -259,6 +259,63 @@ class Pipeline:
 
 
 
+def time_merge(w, reps=10):
+    """Mean time of one standalone ra_merge_out_lse over the workload's (B, L,
+    Hq, D) fp32 output and (B, Hq, L) lse -- the ring update as its own call --
+    with inputs larger than L2, after 3 untimed calls."""
+    import block_sparse_flash_ra_gb300 as ra
+    B, L, H, D = w.B, w.L, w.Hq, w.D
+    g = torch.Generator(device="cuda").manual_seed(7)
+    out = torch.randn((B, L, H, D), device="cuda", generator=g)
+    bout = torch.randn((B, L, H, D), device="cuda", generator=g)
+    lse = torch.randn((B, H, L), device="cuda", generator=g)
+    blse = torch.randn((B, H, L), device="cuda", generator=g)
+    for _ in range(3):
+        ra.ra_merge_out_lse(out, lse, bout, blse, B, L, H, D)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(reps):
+        ra.ra_merge_out_lse(out, lse, bout, blse, B, L, H, D)
+    e.record()
+    torch.cuda.synchronize()
+    nbytes = 3 * out.numel() * 4 + 3 * lse.numel() * 4  # out read + written, block_out read; same for lse
+    return s.elapsed_time(e) / reps, nbytes
+
+
+def hbm_kernels(pipe, per, peaks, peak_kind):
+    """Achieved bandwidth of the memory-bound stages of the step (algorithmic
+    bytes over their CUDA-event time) and of the standalone merge call,
+    against the measured HBM copy bandwidth."""
+    w, d = pipe.w, pipe.dev
+    tb = lambda t: 0 if t is None else t.numel() * t.element_size()  # noqa: E731
+    pos = sum(tb(d[k]) for k in ("q_pos", "kv_pos", "q_seg", "kv_seg"))
+    stages = {
+        # every token row of q, k, v, dO (and positions / segments) read and written once
+        "permute": (per["permute"], 2 * (sum(tb(d[k]) for k in ("q", "k", "v", "dout")) + pos))
+        if w.zigzag else None,
+        "unpermute_fwd": (per["unpermute_fwd"], 2 * (tb(pipe.out) + tb(pipe.lse))) if w.zigzag else None,
+        "unpermute_bwd": (per["unpermute_bwd"], 2 * (tb(pipe.dq) + tb(pipe.dk) + tb(pipe.dv)))
+        if w.zigzag else None,
+        # O and dO read, lse read, Delta and -lse*log2 e written
+        "bwd_prep": (per["bwd_prep"], tb(pipe.out) + tb(pipe.dev["dout"]) + 3 * tb(pipe.lse)),
+        # positions and segments read, one class byte per tile written (lists and
+        # orders add a few MB): kilobytes to megabytes, so the stage is launch-bound
+        "mask": (per["mask"], pos + w.B * (w.L // 128) ** 2),
+    }
+    mm, mb = time_merge(w)
+    stages["merge_out_lse"] = (mm, mb)
+    hbm = peaks["hbm_gbs"]
+    r = {"peak_gbs": hbm, "peak_kind": f"hbm_gbs ({peak_kind})"}
+    for k, v in stages.items():
+        if v is None:
+            continue
+        ms, nb = v
+        gbs = nb / (ms * 1e-3) / 1e9
+        r[k] = {"ms": round(ms, 4), "bytes": int(nb), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+    return r
+
+
 def run_ours(args, w, ws_, rank, local):
     import block_sparse_flash_ra_gb300 as ra
     torch.cuda.set_device(local)
@@ -345,6 +402,7 @@ def run_ours(args, w, ws_, rank, local):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    line["hbm_kernels"] = hbm_kernels(pipe, per, peaks, peak_kind)
     return line, pipe
 
 
