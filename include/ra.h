@@ -239,8 +239,9 @@ RA_API int ra_attn_fwd(const ra_attn_params *p, const void *q, const void *k, co
  *   Where lse == -inf the block is taken as is; otherwise
  *   w = sigmoid(block_lse - lse), out -= w * (out - block_out),
  *   lse += softplus(block_lse - lse).
- *   out / block_out must not overlap; D % 4 == 0.
- * Errors: RA_ERR_INVALID_ARG, RA_ERR_CUDA.
+ *   out / block_out must not overlap and must be 16-byte aligned;
+ *   D % 4 == 0.
+ * Errors: RA_ERR_INVALID_ARG (NULL, sizes, alignment, overlap), RA_ERR_CUDA.
  */
 RA_API int ra_merge_out_lse(float *out, float *lse, const float *block_out,
                             const float *block_lse, int B, int L, int H, int D,

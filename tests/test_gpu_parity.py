@@ -325,9 +325,10 @@ def test_permute_bit_exact(dtype, inner, n):
 
 
 # ------------------------------------------------------------ merge
-def test_merge_matches_oracle():
+@pytest.mark.parametrize("D", [128, 8, 200])
+def test_merge_matches_oracle(D):
     g = torch.Generator().manual_seed(5)
-    B, L, H, D = 2, 300, 3, 128
+    B, L, H = 2, 301, 3
     o = torch.randn(B, L, H, D, generator=g)
     bo = torch.randn(B, L, H, D, generator=g)
     l = torch.randn(B, H, L, generator=g) * 3
