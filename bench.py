@@ -45,9 +45,9 @@ UNIT = "TFLOP/s"
 # (_src_hash); a changed source, or another workload, reports null.
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch, ncu on the gqa32k bench step
-    ("gqa32k", "fwd_tc_kernel"): (3.113e9 + 0.236e9, "8c026f6a91a0ee8a"),
-    ("gqa32k", "bwd_dkdv_kernel"): (4.072e9 + 0.122e9, "d1671f337daf1298"),
-    ("gqa32k", "bwd_dq_kernel"): (3.582e9 + 0.241e9, "d1671f337daf1298"),
+    ("gqa32k", "fwd_tc_kernel"): (3.113e9 + 0.236e9, "5f969814aac778c5"),
+    ("gqa32k", "bwd_dkdv_kernel"): (4.072e9 + 0.122e9, "c72560629edc0ece"),
+    ("gqa32k", "bwd_dq_kernel"): (3.582e9 + 0.241e9, "c72560629edc0ece"),
 }
 
 
