@@ -368,7 +368,13 @@ def run_ours(args, w, ws_, rank, local):
     dom = max(kern, key=lambda k: kern[k][0])
     d_ms, d_flops, d_src = kern[dom]
     achieved = tf(d_flops, d_ms)
-    peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    # the timed region is well under a second (K steps of tens of ms), so the
+    # kernels are held to the burst peak, not the seconds-long sustained one
+    peak = peaks["bf16_tflops"]
+    # the backward as the method counts it: F_bwd = 2.5 F_fwd (five tile
+    # products against the forward's two) over the dK/dV and dQ kernels' time,
+    # whatever products the kernels recompute
+    bwd_alg = tf(2.5 * pipe.f_fwd, per["bwd_dkdv"] + per["bwd_dq"])
     tr = TRAFFIC.get((w.name, dom))
     traffic = tr[0] if tr and tr[1] == _src_hash(d_src) else None
     value = job_tflops(pipe.f_fwd_bwd, ms_step, ws_)
@@ -395,7 +401,17 @@ def run_ours(args, w, ws_, rank, local):
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,
-                     "peak_kind": f"bf16_tflops_sustained ({peak_kind}): kernel timed inside a long step"},
+                     "peak_kind": f"bf16_tflops burst ({peak_kind}): the timed region is "
+                                  f"{K * ms_step / 1e3:.2f} s, not a seconds-long run",
+                     "counted": "products the kernel issues (the dK/dV kernel's four per tile "
+                                "are all algorithmic)",
+                     "algorithmic": {
+                         "fwd_tc_kernel": {"achieved": round(fwd_tf, 2),
+                                           "frac": round(fwd_tf / peak, 4),
+                                           "flops": "F_fwd = 4*128*128*D per non-empty tile-head"},
+                         "backward": {"achieved": round(bwd_alg, 2), "frac": round(bwd_alg / peak, 4),
+                                      "flops": "F_bwd = 2.5 F_fwd over the dK/dV + dQ kernels' time"},
+                     }},
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 3),
@@ -486,7 +502,8 @@ def _oracle_sample(w, rows):
     """fp64 oracle forward + backward on a bounded sample of the workload: the
     first query head of every kv group (Hkv heads, with their kv heads) and
     query rows [L - rows, L), in the original token order (the ring order
-    changes rounding only).  Returns (seconds, counted flops, heads)."""
+    changes rounding only).  Returns (seconds, counted flops, heads, threads
+    that ran work)."""
     import oracle
     inp = make_inputs(w.scaled(backward=True), with_dout=True)
     G = w.Hq // w.Hkv
@@ -507,20 +524,23 @@ def _oracle_sample(w, rows):
     flops = 3.5 * tiles * w.Hkv * 4 * 128 * 128 * w.D
     t0 = time.perf_counter()
     oracle.attn_fwd(q, k, v, rows=(r0, w.L), **kw)
+    used = oracle.last_threads()
     oracle.attn_bwd(q, k, v, do, rows=(r0, w.L), **kw)
-    return time.perf_counter() - t0, flops, w.Hkv
+    used = max(used, oracle.last_threads())
+    return time.perf_counter() - t0, flops, w.Hkv, used
 
 
 def cpu_baseline(w, rows):
     import oracle
     oracle.build()
-    secs, flops, heads = _oracle_sample(w, rows)
-    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": oracle.num_threads(),
+    secs, flops, heads, used = _oracle_sample(w, rows)
+    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": used,
             "kind": "oracle",
             "sample": f"{w.name}: {heads} of {w.Hq} query heads (one per kv group), query rows "
                       f"[{w.L - rows}, {w.L}) of {w.L}, batch {w.B}; fp64 forward (threads over "
-                      f"row blocks) + backward (threads over kv groups), {secs:.2f} s for "
-                      f"{flops:.3e} counted flops"}
+                      f"blocks of query rows) + backward (threads over blocks of query rows, then "
+                      f"of keys), {secs:.2f} s for {flops:.3e} counted flops; {used} of "
+                      f"{oracle.num_threads()} host threads ran work"}
 
 
 def run_reference(args, w):
@@ -529,13 +549,13 @@ def run_reference(args, w):
     rows = args.ref_rows
     for _ in range(args.warmup):
         _oracle_sample(w, rows)
-    times, flops, heads = [], 0.0, 0
+    times, flops, heads, cores = [], 0.0, 0, 1
     for _ in range(args.steps):
-        s, flops, heads = _oracle_sample(w, rows)
+        s, flops, heads, used = _oracle_sample(w, rows)
         times.append(s)
+        cores = max(cores, used)
     sec = sum(times) / len(times)
     v = flops / sec / 1e12
-    cores = oracle.num_threads()
     sample = (f"{w.name}: {heads} of {w.Hq} query heads (one per kv group), query rows "
               f"[{w.L - rows}, {w.L}) of {w.L}, fp64 forward + backward per step")
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": 1,

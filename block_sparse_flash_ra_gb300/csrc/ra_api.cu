@@ -451,11 +451,12 @@ struct BwdWs {
     int hsplit;
 };
 
-// Shared checks of the backward entry points; on success fills the device
-// cache and the workspace split.
-int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
-               const ra_block_mask *mask, void *ws, size_t ws_bytes, DevCache **dc, BwdWs *w,
-               bool allow_split = true)
+} // namespace
+
+// Checks of the backward entry points that do not involve the workspace:
+// params, tensor pointers, the mask, D and dtype.
+int bwd_validate(const ra_attn_params *p, const void *const *ptrs, int nptrs,
+                 const ra_block_mask *mask)
 {
     int rc = check_params(p);
     if (rc) return rc;
@@ -467,6 +468,30 @@ int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
     if (p->D != 64 && p->D != 128) return fail(RA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", p->D);
     if (p->dtype != RA_BF16)
         return fail(RA_ERR_UNSUPPORTED, "the backward is implemented for bf16 inputs");
+    return RA_OK;
+}
+
+int bwd_all_validate(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                     const void *out, const float *lse, const void *dout,
+                     const ra_block_mask *mask, const void *dq, const void *dk, const void *dv,
+                     const float *dsinks)
+{
+    if (!mask) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
+    if (p && p->sinks && !dsinks) return fail(RA_ERR_INVALID_ARG, "dsinks is NULL but sinks are given");
+    const void *ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
+    return bwd_validate(p, ptrs, 9, mask);
+}
+
+namespace {
+
+// Shared checks of the backward entry points; on success fills the device
+// cache and the workspace split.
+int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
+               const ra_block_mask *mask, void *ws, size_t ws_bytes, DevCache **dc, BwdWs *w,
+               bool allow_split = true)
+{
+    int rc = bwd_validate(p, ptrs, nptrs, mask);
+    if (rc) return rc;
     const size_t need = bwd_ws_bytes(p, allow_split);
     if (!ws || ws_bytes < need)
         return fail(RA_ERR_WORKSPACE, "backward workspace has %zu bytes, needs %zu", ws_bytes, need);
@@ -587,12 +612,12 @@ int bwd_all(const ra_attn_params *p, const void *q, const void *k, const void *v
             void *dq, void *dk, void *dv, float *dsinks, void *ws, size_t ws_bytes,
             ra_stream_t stream, bool allow_split)
 {
-    if (!mask) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
-    if (p && p->sinks && !dsinks) return fail(RA_ERR_INVALID_ARG, "dsinks is NULL but sinks are given");
+    int rc = bwd_all_validate(p, q, k, v, out, lse, dout, mask, dq, dk, dv, dsinks);
+    if (rc) return rc;
     const void *ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
     DevCache *dc = nullptr;
     BwdWs w{};
-    int rc = bwd_common(p, ptrs, 9, mask, ws, ws_bytes, &dc, &w, allow_split);
+    rc = bwd_common(p, ptrs, 9, mask, ws, ws_bytes, &dc, &w, allow_split);
     if (rc) return rc;
     const Problem pr = make_problem(p, mask, dc->status);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -97,6 +97,12 @@ int bwd_all(const ra_attn_params *p, const void *q, const void *k, const void *v
             void *dq, void *dk, void *dv, float *dsinks, void *ws, size_t ws_bytes,
             ra_stream_t stream, bool allow_split);
 size_t bwd_ws_min_bytes(const ra_attn_params *p);
+// Every argument check of ra_attn_bwd except those of the workspace, with
+// the same error codes and messages (RA_OK when the arguments are valid).
+int bwd_all_validate(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                     const void *out, const float *lse, const void *dout,
+                     const ra_block_mask *mask, const void *dq, const void *dk, const void *dv,
+                     const float *dsinks);
 
 // Records `msg` as this thread's last error message and returns `code`.
 int set_last_error(int code, const char *msg);

@@ -23,7 +23,8 @@
 namespace ra {
 namespace {
 
-// 8 MiB: enough for B * Hq * Lq up to about two million query rows.
+// 8 MiB: enough for B * Hq * Lq up to about one million query rows (8 bytes
+// per row: Delta and -lse * log2 e), with room for the dsinks partial sums.
 constexpr size_t kScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
@@ -63,8 +64,10 @@ RA_API int ra_attn_bwd_noalloc(const ra_attn_params *p, const void *q, const voi
                                const void *dout, const ra_block_mask *mask, void *dq, void *dk,
                                void *dv, float *dsinks, ra_stream_t stream)
 {
-    if (!p) return ra::set_last_error(RA_ERR_INVALID_ARG, "params is NULL");
-    if (ra_attn_bwd_workspace_size(p) == 0) return RA_ERR_INVALID_ARG; // the size query recorded why
+    // the arguments are checked exactly as ra_attn_bwd checks them (same codes),
+    // before the problem's size is compared with the built-in scratch
+    int rc = ra::bwd_all_validate(p, q, k, v, out, lse, dout, mask, dq, dk, dv, dsinks);
+    if (rc) return rc;
     // the built-in scratch serves the schedule without a dK/dV head split
     const size_t need = ra::bwd_ws_min_bytes(p);
     if (need > ra::kScratchBytes) {
@@ -76,7 +79,7 @@ RA_API int ra_attn_bwd_noalloc(const ra_attn_params *p, const void *q, const voi
         return ra::set_last_error(RA_ERR_WORKSPACE, msg);
     }
     void *scratch = nullptr;
-    int rc = ra::scratch_address(&scratch);
+    rc = ra::scratch_address(&scratch);
     if (rc) return rc;
     // Every value the backward reads from its workspace is written earlier in
     // the same call, so nothing in the scratch has to start at zero.

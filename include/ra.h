@@ -310,7 +310,9 @@ RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k,
  *   Nothing is allocated: no cudaMalloc / cudaFree is ever called.
  *   The first call on a device looks up the array's device address on that
  *   device (a synchronous runtime query); make that first call before any
- *   stream capture begins.
+ *   stream capture begins.  The address is kept for the life of the process:
+ *   after a cudaDeviceReset (or on another context of the same device) it is
+ *   stale, so this call is not supported once the device has been reset.
  *   All calls share the one array and it keeps the last call's contents.
  *   Calls whose GPU work overlaps in time (different streams, different
  *   threads, without ordering between them) race on it and give wrong
@@ -341,6 +343,9 @@ RA_API int ra_unpermute_tokens(const void *in, void *out, int B, int L, size_t r
 /*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: RA_OK, or RA_ERR_TIMEOUT if a kernel gave up a bounded wait.
+ * The library caches, per device, the device address of this word and the
+ * kernels' attributes on first use; resetting the device (cudaDeviceReset)
+ * after the library's first call on it is not supported.
  */
 RA_API int ra_get_device_status(ra_stream_t stream);
 

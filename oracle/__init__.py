@@ -80,7 +80,8 @@ def _load():
             vp, ci, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             lib.ora_attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, ci, ci, ci, ci]
             lib.ora_attn_fwd_ring.argtypes = [P, ci, vp, vp, vp, vp, vp, ci, ci]
-            lib.ora_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci]
+            lib.ora_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci,
+                                        ci, ci]
             lib.ora_merge.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci]
             lib.ora_merge.restype = None
             lib.ora_block_mask.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
@@ -92,7 +93,13 @@ def _load():
 
 
 def num_threads() -> int:
+    """OpenMP threads the oracle may use."""
     return int(_load().ora_num_threads())
+
+
+def last_threads() -> int:
+    """Threads that ran work in the last attn_fwd / attn_bwd call."""
+    return int(_load().ora_last_threads())
 
 
 def _f64(a):
@@ -172,11 +179,13 @@ def attn_fwd_ring(q, k, v, *, scale, n_shards, heads=None, **kw):
     return out, lse
 
 
-def attn_bwd(q, k, v, dout, *, scale, heads=None, rows=None, **kw):
+def attn_bwd(q, k, v, dout, *, scale, heads=None, rows=None, keys=None, **kw):
     """Exact gradient -> (dq, dk, dv, dsinks or None, out, lse).
 
-    ``heads`` / ``rows`` restrict the sums to the contributions of those
-    query heads / rows (dq of other rows stays 0)."""
+    ``heads`` / ``rows`` / ``keys`` restrict the sums to the contributions of
+    pairs with a query head, query row and key row in those ranges (dq of
+    other rows and dk / dv of other keys stay 0; dsinks sums the rows of the
+    row range)."""
     c = _Call(q, k, v, scale=scale, **kw)
     B, Lq, Lkv, Hq, Hkv, D = c.shape
     do = _f64(dout)
@@ -188,9 +197,10 @@ def attn_bwd(q, k, v, dout, *, scale, heads=None, rows=None, **kw):
     lse = np.full((B, Hq, Lq), -np.inf)
     lo, hi = heads if heads else (0, 0)
     rlo, rhi = rows if rows else (0, 0)
+    klo, khi = keys if keys else (0, 0)
     rc = _load().ora_attn_bwd(ctypes.byref(c.p), _ptr(c.q), _ptr(c.k), _ptr(c.v), _ptr(do),
                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ds), _ptr(out), _ptr(lse),
-                              lo, hi, rlo, rhi)
+                              lo, hi, rlo, rhi, klo, khi)
     if rc:
         raise ValueError(f"ora_attn_bwd failed ({rc})")
     return dq, dk, dv, ds, out, lse

@@ -81,14 +81,20 @@ static int ora_visible(const ora_params *p, int b, int i, int j)
     return 1;
 }
 
+/* The scale and soft cap applied to a finished dot product (R-order). */
+static double ora_cap(const ora_params *p, double acc)
+{
+    double s = p->scale * acc;
+    if (p->soft_cap > 0.0) s = p->soft_cap * tanh(s / p->soft_cap);
+    return s;
+}
+
 /* logit of one pair after scale and soft cap (R-order) */
 static double ora_logit(const ora_params *p, const double *qrow, const double *krow)
 {
     double acc = 0.0;
     for (int d = 0; d < p->D; ++d) acc += qrow[d] * krow[d];
-    double s = p->scale * acc;
-    if (p->soft_cap > 0.0) s = p->soft_cap * tanh(s / p->soft_cap);
-    return s;
+    return ora_cap(p, acc);
 }
 
 static inline const double *qrow_of(const ora_params *p, const double *q, int b, int i, int h)
@@ -145,13 +151,46 @@ static void ora_rows(const ora_params *p, const double *q, const double *k, cons
     }
 }
 
-/* Rows per materialised mask block: the whole (Lq x Lkv) mask of a batch row
- * when it has at most 4 Mi entries, else blocks of ORA_TILE query rows (the
- * same mask, materialised one row block at a time). */
-static int ora_row_block(const ora_params *p)
+/* Threads that ran at least one task of the last parallel call (the CPU
+ * baseline reports it as the core count it used). */
+static int ora_threads_used = 1;
+
+static int ora_max_threads(void)
 {
-    if ((size_t)p->Lq * (size_t)p->Lkv <= ((size_t)4 << 20)) return p->Lq;
-    return ORA_TILE;
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static int ora_thread_id(void)
+{
+#ifdef _OPENMP
+    return omp_get_thread_num();
+#else
+    return 0;
+#endif
+}
+
+static void ora_count_threads(const unsigned char *ran, int n)
+{
+    int c = 0;
+    for (int t = 0; t < n; ++t) c += ran[t] != 0;
+    ora_threads_used = c > 0 ? c : 1;
+}
+
+/* Rows per task of a parallel loop over `rows` rows of `B` batch rows (and
+ * `units` independent heads or groups): small enough that there are about
+ * four tasks per thread, at most one 128-row tile.  Only the schedule depends
+ * on it, never the arithmetic of a row. */
+static int ora_rows_per_task(int rows, int B, int units)
+{
+    const long want = 4L * ora_max_threads();
+    long per = ((long)rows * B * (units > 0 ? units : 1) + want - 1) / want;
+    if (per > ORA_TILE) per = ORA_TILE;
+    if (per < 1) per = 1;
+    return (int)per;
 }
 
 static void ora_fill_mask(const ora_params *p, int b, int i0, int i1, uint8_t *vis)
@@ -172,7 +211,8 @@ static int ora_check(const ora_params *p)
  * Only query heads [heads_lo, heads_hi) and query rows [rows_lo, rows_hi)
  * are computed (an empty range means all); the rest of out / lse is left
  * untouched.  Restricting rows or heads changes which rows are computed,
- * never how a row is computed. */
+ * never how a row is computed.  Tasks are blocks of rows of one batch row;
+ * each materialises its block's mask once and runs every head over it. */
 int ora_attn_fwd(const ora_params *p, const double *q, const double *k, const double *v,
                  double *out, double *lse, int heads_lo, int heads_hi, int rows_lo, int rows_hi)
 {
@@ -180,9 +220,12 @@ int ora_attn_fwd(const ora_params *p, const double *q, const double *k, const do
     if (heads_hi <= heads_lo) { heads_lo = 0; heads_hi = p->Hq; }
     if (rows_hi <= rows_lo) { rows_lo = 0; rows_hi = p->Lq; }
     if (heads_lo < 0 || heads_hi > p->Hq || rows_lo < 0 || rows_hi > p->Lq) return -1;
-    const int R = ora_row_block(p);
-    const int nblk = (p->Lq + R - 1) / R;
+    const int R = ora_rows_per_task(rows_hi - rows_lo, p->B, 1);
+    const int nblk = (rows_hi - rows_lo + R - 1) / R;
     const int D = p->D;
+    const int nthr = ora_max_threads();
+    unsigned char *ran = (unsigned char *)calloc((size_t)nthr, 1);
+    if (!ran) return -2;
     int err = 0;
 #pragma omp parallel
     {
@@ -197,10 +240,9 @@ int ora_attn_fwd(const ora_params *p, const double *q, const double *k, const do
 #pragma omp for schedule(dynamic, 1) collapse(2)
             for (int b = 0; b < p->B; ++b)
                 for (int blk = 0; blk < nblk; ++blk) {
-                    int i0 = blk * R, i1 = i0 + R < p->Lq ? i0 + R : p->Lq;
-                    if (i0 < rows_lo) i0 = rows_lo;
-                    if (i1 > rows_hi) i1 = rows_hi;
-                    if (i0 >= i1) continue;
+                    const int i0 = rows_lo + blk * R;
+                    const int i1 = i0 + R < rows_hi ? i0 + R : rows_hi;
+                    ran[ora_thread_id()] = 1;
                     ora_fill_mask(p, b, i0, i1, vis);
                     for (int h = heads_lo; h < heads_hi; ++h) {
                         ora_rows(p, q, k, v, b, h, i0, i1, 0, p->Lkv, vis, 1, orow, lrow, sbuf);
@@ -214,6 +256,8 @@ int ora_attn_fwd(const ora_params *p, const double *q, const double *k, const do
         }
         free(vis); free(sbuf); free(orow); free(lrow);
     }
+    ora_count_threads(ran, nthr);
+    free(ran);
     return err;
 }
 
@@ -333,94 +377,162 @@ int ora_attn_fwd_ring(const ora_params *p, int n_shards, const double *q, const 
     return err;
 }
 
+/* dS of one visible pair (the soft-cap factor included) and its P:
+ *   P = exp(s - lse),  dP = <dO_i, v_j>,  dS = P (dP - Delta_i) (1 - (s/cap)^2) */
+static void ora_pair_grad(const ora_params *p, const double *qr, const double *kr,
+                          const double *vr, const double *go, double l, double delta,
+                          double *pij_out, double *ds_out)
+{
+    double s = ora_logit(p, qr, kr);
+    double pij = exp(s - l);
+    double dp = 0.0;
+    for (int d = 0; d < p->D; ++d) dp += go[d] * vr[d];
+    double dsij = pij * (dp - delta);
+    if (p->soft_cap > 0.0) {
+        double t = s / p->soft_cap;
+        dsij *= 1.0 - t * t;
+    }
+    *pij_out = pij;
+    *ds_out = dsij;
+}
+
 /* Exact gradient of the plain forward (its own forward is recomputed here,
- * so no input comes from elsewhere).  With a head range / row range, only
- * the contributions of those query heads and rows are summed (dq of the
- * other rows stays 0); the result is the full gradient when the ranges are
- * empty (= all).  Summing per-chunk contributions as
- * [RS] _ring_attention_backward does gives the same sums.
+ * so no input comes from elsewhere).  Only pairs (i, j) with query row i in
+ * [rows_lo, rows_hi), key row j in [keys_lo, keys_hi) and query head in
+ * [heads_lo, heads_hi) contribute (an empty range means all); dq of rows and
+ * dk / dv of keys outside the ranges stay 0, and dsinks sums the rows of the
+ * row range.  The result is the full gradient when every range is all.
+ * Summing per-chunk contributions as [RS] _ring_attention_backward does gives
+ * the same sums.
  *   Delta_i = <dO_i, O_i>,  P_ij = exp(s_ij - lse_i) on visible pairs
  *   dV_j  += P_ij dO_i ;  dP_ij = <dO_i, v_j> ;  dS_ij = P_ij (dP_ij - Delta_i)
  *   dR_ij  = dS_ij * (1 - (s_ij / cap)^2)   (cap > 0; 1 otherwise)
  *   dQ_i  += scale dR_ij k_j ;  dK_j += scale dR_ij q_i
  *   dsink_h = - sum_{b,i} exp(sink_h - lse_i) Delta_i
- * dk, dv sum over the query heads sharing a kv head (R-gqa).  Parallel over
- * (b, kv head) so that no two threads write the same dk / dv row. */
+ * dk, dv sum over the query heads sharing a kv head (R-gqa).  Two parallel
+ * passes that own their outputs: dq by (b, h, block of query rows), summing
+ * keys in ascending order; dk / dv by (b, kv head, block of keys), summing
+ * the heads of the group, then query rows, in ascending order. */
 int ora_attn_bwd(const ora_params *p, const double *q, const double *k, const double *v,
                  const double *dout, double *dq, double *dk, double *dv, double *dsinks,
                  double *out_ws, double *lse_ws, int heads_lo, int heads_hi, int rows_lo,
-                 int rows_hi)
+                 int rows_hi, int keys_lo, int keys_hi)
 {
     if (ora_check(p)) return -1;
     if (heads_hi <= heads_lo) { heads_lo = 0; heads_hi = p->Hq; }
     if (rows_hi <= rows_lo) { rows_lo = 0; rows_hi = p->Lq; }
+    if (keys_hi <= keys_lo) { keys_lo = 0; keys_hi = p->Lkv; }
+    if (keys_lo < 0 || keys_hi > p->Lkv) return -1;
     int rc = ora_attn_fwd(p, q, k, v, out_ws, lse_ws, heads_lo, heads_hi, rows_lo, rows_hi);
     if (rc) return rc;
-    const int D = p->D, G = p->Hq / p->Hkv;
+    int used = ora_threads_used;
+    const int D = p->D, G = p->Hq / p->Hkv, H = heads_hi - heads_lo;
     memset(dq, 0, sizeof(double) * (size_t)p->B * p->Lq * p->Hq * D);
     memset(dk, 0, sizeof(double) * (size_t)p->B * p->Lkv * p->Hkv * D);
     memset(dv, 0, sizeof(double) * (size_t)p->B * p->Lkv * p->Hkv * D);
-    double *dsink_part = (double *)calloc((size_t)p->B * p->Hq, sizeof(double));
-    if (!dsink_part) return -2;
-    int err = 0;
-#pragma omp parallel
-    {
-        int ok = 1;
-        if (!ok) {
-#pragma omp atomic write
-            err = -2;
-        } else {
-#pragma omp for schedule(dynamic, 1) collapse(2)
-            for (int b = 0; b < p->B; ++b)
-                for (int g = 0; g < p->Hkv; ++g)
-                    for (int h = g * G; h < (g + 1) * G; ++h) {
-                        double ds_acc = 0.0;
-                        if (h < heads_lo || h >= heads_hi) continue;
+    const size_t nrow = (size_t)p->B * p->Hq * p->Lq;
+    double *delta = (double *)calloc(nrow, sizeof(double));
+    if (!delta) return -2;
+    const int nthr = ora_max_threads();
+    unsigned char *ran = (unsigned char *)calloc((size_t)nthr, 1);
+    if (!ran) { free(delta); return -2; }
+
+    /* Delta of every row in range; dsinks per head, rows in ascending order */
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < p->B; ++b)
+        for (int h = heads_lo; h < heads_hi; ++h)
+            for (int i = rows_lo; i < rows_hi; ++i) {
+                const double *o = out_ws + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
+                const double *go = dout + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
+                double s = 0.0;
+                for (int d = 0; d < D; ++d) s += go[d] * o[d];
+                delta[((size_t)b * p->Hq + h) * p->Lq + i] = s;
+            }
+    if (dsinks) {
+        for (int h = 0; h < p->Hq; ++h) dsinks[h] = 0.0;
+        if (p->sinks)
+            for (int h = heads_lo; h < heads_hi; ++h) {
+                double tot = 0.0;
+                for (int b = 0; b < p->B; ++b) {
+                    double acc = 0.0;
+                    for (int i = rows_lo; i < rows_hi; ++i) {
+                        const size_t r = ((size_t)b * p->Hq + h) * p->Lq + i;
+                        if (lse_ws[r] != -INFINITY) acc -= exp(p->sinks[h] - lse_ws[r]) * delta[r];
+                    }
+                    tot += acc;
+                }
+                dsinks[h] = tot;
+            }
+    }
+
+    /* pass 1: dq */
+    const int Rq = ora_rows_per_task(rows_hi - rows_lo, p->B, H);
+    const int nbq = (rows_hi - rows_lo + Rq - 1) / Rq;
+#pragma omp parallel for collapse(3) schedule(dynamic, 1)
+    for (int b = 0; b < p->B; ++b)
+        for (int h = heads_lo; h < heads_hi; ++h)
+            for (int blk = 0; blk < nbq; ++blk) {
+                ran[ora_thread_id()] = 1;
+                const int g = h / G;
+                const int i0 = rows_lo + blk * Rq;
+                const int i1 = i0 + Rq < rows_hi ? i0 + Rq : rows_hi;
+                for (int i = i0; i < i1; ++i) {
+                    const size_t r = ((size_t)b * p->Hq + h) * p->Lq + i;
+                    const double l = lse_ws[r];
+                    if (l == -INFINITY) continue;
+                    const double *qr = qrow_of(p, q, b, i, h);
+                    const double *go = dout + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
+                    double *gq = dq + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
+                    for (int j = keys_lo; j < keys_hi; ++j) {
+                        if (!ora_visible(p, b, i, j)) continue;
+                        const double *kr = krow_of(p, k, b, j, g);
+                        double pij, dsij;
+                        ora_pair_grad(p, qr, kr, krow_of(p, v, b, j, g), go, l, delta[r], &pij,
+                                      &dsij);
+                        for (int d = 0; d < D; ++d) gq[d] += p->scale * dsij * kr[d];
+                    }
+                }
+            }
+
+    /* pass 2: dk, dv */
+    const int Rk = ora_rows_per_task(keys_hi - keys_lo, p->B, p->Hkv);
+    const int nbk = (keys_hi - keys_lo + Rk - 1) / Rk;
+#pragma omp parallel for collapse(3) schedule(dynamic, 1)
+    for (int b = 0; b < p->B; ++b)
+        for (int g = 0; g < p->Hkv; ++g)
+            for (int blk = 0; blk < nbk; ++blk) {
+                const int h0 = g * G > heads_lo ? g * G : heads_lo;
+                const int h1 = (g + 1) * G < heads_hi ? (g + 1) * G : heads_hi;
+                if (h0 >= h1) continue;
+                ran[ora_thread_id()] = 1;
+                const int j0 = keys_lo + blk * Rk;
+                const int j1 = j0 + Rk < keys_hi ? j0 + Rk : keys_hi;
+                for (int j = j0; j < j1; ++j) {
+                    const double *kr = krow_of(p, k, b, j, g);
+                    const double *vr = krow_of(p, v, b, j, g);
+                    double *gk = dk + (((size_t)b * p->Lkv + j) * p->Hkv + g) * D;
+                    double *gv = dv + (((size_t)b * p->Lkv + j) * p->Hkv + g) * D;
+                    for (int h = h0; h < h1; ++h)
                         for (int i = rows_lo; i < rows_hi; ++i) {
-                            double l = lse_ws[((size_t)b * p->Hq + h) * p->Lq + i];
-                            const double *o = out_ws + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
-                            const double *go = dout + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
-                            double delta = 0.0;
-                            for (int d = 0; d < D; ++d) delta += go[d] * o[d];
-                            if (p->sinks && l != -INFINITY) ds_acc -= exp(p->sinks[h] - l) * delta;
-                            if (l == -INFINITY) continue;
+                            const size_t r = ((size_t)b * p->Hq + h) * p->Lq + i;
+                            const double l = lse_ws[r];
+                            if (l == -INFINITY || !ora_visible(p, b, i, j)) continue;
                             const double *qr = qrow_of(p, q, b, i, h);
-                            double *gq = dq + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
-                            for (int j = 0; j < p->Lkv; ++j) {
-                                if (!ora_visible(p, b, i, j)) continue;
-                                const double *kr = krow_of(p, k, b, j, g);
-                                const double *vr = krow_of(p, v, b, j, g);
-                                double s = ora_logit(p, qr, kr);
-                                double pij = exp(s - l);
-                                double dp = 0.0;
-                                for (int d = 0; d < D; ++d) dp += go[d] * vr[d];
-                                double dsij = pij * (dp - delta);
-                                if (p->soft_cap > 0.0) {
-                                    double t = s / p->soft_cap;
-                                    dsij *= 1.0 - t * t;
-                                }
-                                double *gk = dk + (((size_t)b * p->Lkv + j) * p->Hkv + g) * D;
-                                double *gv = dv + (((size_t)b * p->Lkv + j) * p->Hkv + g) * D;
-                                for (int d = 0; d < D; ++d) {
-                                    gv[d] += pij * go[d];
-                                    gq[d] += p->scale * dsij * kr[d];
-                                    gk[d] += p->scale * dsij * qr[d];
-                                }
+                            const double *go = dout + (((size_t)b * p->Lq + i) * p->Hq + h) * D;
+                            double pij, dsij;
+                            ora_pair_grad(p, qr, kr, vr, go, l, delta[r], &pij, &dsij);
+                            for (int d = 0; d < D; ++d) {
+                                gv[d] += pij * go[d];
+                                gk[d] += p->scale * dsij * qr[d];
                             }
                         }
-                        dsink_part[(size_t)b * p->Hq + h] = ds_acc;
-                    }
-        }
-    }
-    if (dsinks) {
-        for (int h = 0; h < p->Hq; ++h) {
-            double s = 0.0;
-            for (int b = 0; b < p->B; ++b) s += dsink_part[(size_t)b * p->Hq + h];
-            dsinks[h] = s;
-        }
-    }
-    free(dsink_part);
-    return err;
+                }
+            }
+    ora_count_threads(ran, nthr);
+    if (ora_threads_used < used) ora_threads_used = used;
+    free(ran);
+    free(delta);
+    return 0;
 }
 
 /* ------------------------------------------------------------------ */
@@ -519,11 +631,8 @@ int ora_permute(const uint8_t *in, uint8_t *out, int B, int L, size_t row_bytes,
     return 0;
 }
 
-int ora_num_threads(void)
-{
-#ifdef _OPENMP
-    return omp_get_max_threads();
-#else
-    return 1;
-#endif
-}
+int ora_num_threads(void) { return ora_max_threads(); }
+
+/* Threads that ran work in the last ora_attn_fwd / ora_attn_bwd call (for
+ * the backward: the larger of its forward and gradient phases). */
+int ora_last_threads(void) { return ora_threads_used; }

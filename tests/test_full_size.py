@@ -61,9 +61,10 @@ def run_gpu(w, inp):
                        local_mask=d["local_mask"])
     m = ra.build_mask(p)
     out, lse = ra.forward(p, d["q"], d["k"], d["v"], m)
-    grads = None
+    grads = dsinks = None
     if w.backward:
-        grads = ra.backward(p, d["q"], d["k"], d["v"], out, lse, d["dout"], m)[:3]
+        dq, dk, dv, dsinks = ra.backward(p, d["q"], d["k"], d["v"], out, lse, d["dout"], m)
+        grads = (dq, dk, dv)
     if w.zigzag:
         out = ra.unpermute(out, N)
         # lse is (B, H, L): unpermute along L through a (B, L, H) view
@@ -74,7 +75,7 @@ def run_gpu(w, inp):
     assert ra.ra_get_device_status() == ra.RA_OK
     res = dict(out=f64(out), lse=f64(lse))
     if grads is not None:
-        res.update(dq=f64(grads[0]), dk=f64(grads[1]), dv=f64(grads[2]))
+        res.update(dq=f64(grads[0]), dk=f64(grads[1]), dv=f64(grads[2]), dsinks=f64(dsinks))
     return res
 
 
@@ -132,12 +133,40 @@ def _grad_rows(w, inp):
     return (w.L - 128, w.L), None
 
 
-BWD = ["packed16k", "long64k", "gqa32k", "local8k"]
+BWD = ["packed16k", "long64k", "gqa32k", "local8k", "mqa32k"]
+
+# Workloads whose longest dK/dV columns are checked too: under causal masking
+# keys 0..127 are seen by every query row, so their dk / dv sum the most
+# tiles (every query tile of the sequence, times the heads of the group).
+DEEP = ("gqa32k", "long64k")
+
+
+def _check_deep_columns(w, got, q, k, v, do, kw):
+    """dk / dv of the first 128 keys of kv head 0 (original order) against the
+    oracle over every query row of the heads of that group: the oracle
+    restricted to those keys gives their sums exactly."""
+    G = w.Hq // w.Hkv
+    _, dk, dv, _, _, _ = oracle.attn_bwd(q, k, v, do, heads=(0, G), keys=(0, 128), **kw)
+    assert rel_l2(got["dk"][:, 0:128, 0:1], dk[:, 0:128, 0:1]) <= GRAD_TOL, w.name
+    assert rel_l2(got["dv"][:, 0:128, 0:1], dv[:, 0:128, 0:1]) <= GRAD_TOL, w.name
+
+
+def _check_dsinks(w, q, k, v, do, kw, heads):
+    """dsinks of `heads`, which sums exp(sink - lse) Delta over every query row:
+    the oracle over all rows of those heads (keys restricted to the last 128,
+    which does not change dsinks and keeps the pair loop short)."""
+    L = w.L
+    _, _, _, ds, _, _ = oracle.attn_bwd(q, k, v, do, heads=heads, keys=(L - 128, L), **kw)
+    return ds[heads[0]:heads[1]]
 
 
 @pytest.mark.parametrize("name", BWD)
 def test_full_size_backward_sampled_rows(name):
     w = WORKLOADS[name]
+    if not w.backward:
+        # a forward-only configuration: its backward drawn with a dO (the
+        # shapes, cap, sinks and permutation of the configuration)
+        w = w.scaled(backward=True)
     inp = make_inputs(w)
     got = run_gpu(w, inp)
     q, k, v, do = f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["dout"])
@@ -170,6 +199,13 @@ def test_full_size_backward_sampled_rows(name):
     assert rel_l2(got["dq"][:, rs, hs], dq[:, rs, hs]) <= GRAD_TOL
     assert rel_l2(got["dk"][bs, rs, 0:1], dk[bs, rs, 0:1]) <= GRAD_TOL
     assert rel_l2(got["dv"][bs, rs, 0:1], dv[bs, rs, 0:1]) <= GRAD_TOL
+    if name in DEEP:
+        _check_deep_columns(w, got, q, k, v, do, kw)
+    if w.sinks:
+        # dsinks of the first and the last query head, each over all 32K rows
+        for hh in ((0, 1), (w.Hq - 1, w.Hq)):
+            want = _check_dsinks(w, q, k, v, do, kw, hh)
+            assert rel_l2(got["dsinks"][hh[0]:hh[1]], want) <= GRAD_TOL, (name, hh)
 
 
 def test_full_size_block_map_and_permutation_bit_exact():

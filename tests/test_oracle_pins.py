@@ -400,6 +400,13 @@ def test_row_and_head_restriction_equals_full():
              for r in ((0, 50), (50, 96)) for hh in ((0, 1), (1, 4))]
     for t in range(4):
         np.testing.assert_allclose(sum(pp[t] for pp in parts), full[t], atol=1e-12)
+    # key ranges split the pair sums the same way (dsinks, a sum over rows, is
+    # the same in every key-restricted call)
+    kparts = [oracle.attn_bwd(q, k, v, do, keys=kr, **kw) for kr in ((0, 40), (40, 96))]
+    for t in range(3):
+        np.testing.assert_allclose(sum(pp[t] for pp in kparts), full[t], atol=1e-12)
+    np.testing.assert_array_equal(kparts[0][3], full[3])
+    assert np.all(kparts[0][1][:, 40:] == 0) and np.all(kparts[1][2][:, :40] == 0)
 
 
 # ------------------------------------------------- local mask (non-causal ring)
