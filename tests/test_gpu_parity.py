@@ -348,6 +348,37 @@ def test_merge_matches_oracle(D):
     assert np.max(np.abs(do.cpu().double().numpy() - ro)) < 1e-5
 
 
+def test_merge_extreme_lse_gaps():
+    # lse gaps of +-80 (sigmoid ~ e^-80 or 1 - e^-80, softplus ~ e^-80 or 80),
+    # a -inf block after a finite running lse (a shard with nothing visible
+    # for the row), and both -inf: O and lse must follow the oracle's update
+    g = torch.Generator().manual_seed(9)
+    B, L, H, D = 1, 64, 2, 128
+    o = torch.randn(B, L, H, D, generator=g)
+    bo = torch.randn(B, L, H, D, generator=g)
+    l = torch.randn(B, H, L, generator=g)
+    bl = l.clone()
+    bl[:, :, 0:16] += 80.0
+    bl[:, :, 16:32] -= 80.0
+    bl[:, :, 32:40] = -math.inf
+    bl[:, :, 40:48] += 30.0
+    bl[:, :, 48:56] -= 30.0
+    l[:, :, 56:60] = -math.inf
+    l[:, :, 60:64] = bl[:, :, 60:64] = -math.inf
+    ro, rl = oracle.merge(o.double().numpy(), l.double().numpy(), bo.double().numpy(),
+                          bl.double().numpy())
+    do, dl = o.cuda(), l.cuda()
+    ra.ra_merge_out_lse(do, dl, bo.cuda(), bl.cuda(), B, L, H, D)
+    torch.cuda.synchronize()
+    dl = dl.cpu().double().numpy()
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(dl), fin)
+    assert np.max(np.abs(dl[fin] - rl[fin])) <= 1e-5 * np.maximum(1.0, np.abs(rl[fin])).max()
+    got_o = do.cpu().double().numpy()
+    assert not np.isnan(got_o).any()
+    assert np.max(np.abs(got_o - ro)) < 1e-5
+
+
 # ------------------------------------------------------------ backward
 BWD_CASES = {
     "causal_gqa": W(Hq=4, Hkv=2, L=512, seed=31, n_shards=2),
