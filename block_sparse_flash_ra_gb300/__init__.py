@@ -26,7 +26,8 @@ __all__ = [
     "ra_build_block_mask", "ra_attn_fwd_workspace_size", "ra_attn_fwd", "ra_merge_out_lse",
     "ra_attn_bwd_workspace_size", "ra_attn_bwd", "ra_attn_bwd_prep", "ra_attn_bwd_dkdv",
     "ra_attn_bwd_dq", "ra_attn_bwd_noalloc", "ra_attn_bwd_noalloc_max_workspace",
-    "ra_permute_tokens", "ra_unpermute_tokens",
+    "ra_permute_tokens", "ra_unpermute_tokens", "RA_STEP_SINKS", "RA_STEP_FIRST",
+    "ra_attn_fwd_step", "ra_attn_bwd_step", "ra_cast_from_f32", "ra_add_f32",
     "ra_get_device_status", "ra_launch_count", "ra_selftest_wait_timeout", "make_params", "build_mask", "forward", "backward", "permute",
     "unpermute",
 ]
@@ -40,6 +41,8 @@ RA_ERR_TIMEOUT = -5
 RA_BF16 = 0
 RA_FP32 = 1
 RA_TILE = 128
+RA_STEP_SINKS = 1
+RA_STEP_FIRST = 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libra_gb300.so")
@@ -115,6 +118,10 @@ def lib():
             L.ra_permute_tokens.argtypes = [vp, vp, ci, ci, sz, ci, vp]
             L.ra_unpermute_tokens.argtypes = [vp, vp, ci, ci, sz, ci, vp]
             L.ra_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, M, vp, vp, vp, vp, vp]
+            L.ra_attn_fwd_step.argtypes = [P, vp, vp, vp, M, ci, vp, vp, vp, vp]
+            L.ra_attn_bwd_step.argtypes = [P, vp, vp, vp, vp, M, vp, vp, vp, vp, sz, vp]
+            L.ra_cast_from_f32.argtypes = [vp, vp, sz, ci, vp]
+            L.ra_add_f32.argtypes = [vp, vp, sz, vp]
             L.ra_attn_bwd_noalloc_max_workspace.restype = sz
             L.ra_get_device_status.argtypes = [vp]
             L.ra_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
@@ -228,6 +235,28 @@ def ra_attn_bwd_dkdv(params, q, k, v, dout, mask, dk, dv, ws, stream=None):
 def ra_attn_bwd_dq(params, q, k, v, dout, mask, dq, ws, stream=None):
     _check(lib().ra_attn_bwd_dq(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
                                 ctypes.byref(mask), _ptr(dq), _ptr(ws), _wsb(ws), _stream(stream)))
+
+
+def ra_attn_fwd_step(params, q, k, v, mask, flags, out_run, lse_run, out=None, stream=None):
+    """One ring step of the forward: merge the chunk (k, v) into (out_run, lse_run)."""
+    _check(lib().ra_attn_fwd_step(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v),
+                                  ctypes.byref(mask), int(flags), _ptr(out_run), _ptr(lse_run),
+                                  _ptr(out), _stream(stream)))
+
+
+def ra_attn_bwd_step(params, q, k, v, dout, mask, dq_acc, dk_acc, dv_acc, ws, stream=None):
+    """One ring step of the backward: += the pair's gradients into fp32 accumulators."""
+    _check(lib().ra_attn_bwd_step(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                  ctypes.byref(mask), _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc),
+                                  _ptr(ws), _wsb(ws), _stream(stream)))
+
+
+def ra_cast_from_f32(inp, out, n, dtype, stream=None) -> None:
+    _check(lib().ra_cast_from_f32(_ptr(inp), _ptr(out), int(n), int(dtype), _stream(stream)))
+
+
+def ra_add_f32(acc, x, n, stream=None) -> None:
+    _check(lib().ra_add_f32(_ptr(acc), _ptr(x), int(n), _stream(stream)))
 
 
 def ra_permute_tokens(inp, out, B, L, row_bytes, n_shards, stream=None) -> None:

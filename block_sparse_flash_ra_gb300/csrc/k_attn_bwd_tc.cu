@@ -500,6 +500,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_ld32(lane_base + C::kColDV + o_col + c * 32, a);
                     tmem_ld32(lane_base + C::kColDK + o_col + c * 32, bk);
                     tmem_ld_wait();
+                    if (p.acc_dk) {
+                        // ring step: add to the chunk's travelling fp32 accumulators
+                        float4 *ak4 = reinterpret_cast<float4 *>(p.acc_dk + orow + c * 32);
+                        float4 *av4 = reinterpret_cast<float4 *>(p.acc_dv + orow + c * 32);
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4) {
+                            float4 tk = ak4[k4], tv = av4[k4];
+                            tk.x += p.scale * bk[4 * k4];
+                            tk.y += p.scale * bk[4 * k4 + 1];
+                            tk.z += p.scale * bk[4 * k4 + 2];
+                            tk.w += p.scale * bk[4 * k4 + 3];
+                            tv.x += a[4 * k4];
+                            tv.y += a[4 * k4 + 1];
+                            tv.z += a[4 * k4 + 2];
+                            tv.w += a[4 * k4 + 3];
+                            ak4[k4] = tk;
+                            av4[k4] = tv;
+                        }
+                        continue;
+                    }
                     if (split) {
                         float4 *pk4 = reinterpret_cast<float4 *>(part_k + prow + c * 32);
                         float4 *pv4 = reinterpret_cast<float4 *>(part_v + prow + c * 32);
@@ -528,6 +548,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         dkp[k4] = w;
                     }
                 }
+            } else if (p.acc_dk) {
+                // ring step: a column with nothing visible adds nothing
             } else if (split) {
                 float4 *pk4 = reinterpret_cast<float4 *>(part_k + prow);
                 float4 *pv4 = reinterpret_cast<float4 *>(part_v + prow);
@@ -975,6 +997,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     float a[32];
                     tmem_ld32(lane_base + C::kColDQ + o_col + c * 32, a);
                     tmem_ld_wait();
+                    if (p.acc_dq) {
+                        // ring step: add to the local fp32 dq accumulator
+                        float4 *aq4 = reinterpret_cast<float4 *>(
+                            p.acc_dq + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D + o_col + c * 32);
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4) {
+                            float4 t = aq4[k4];
+                            t.x += p.scale * a[4 * k4];
+                            t.y += p.scale * a[4 * k4 + 1];
+                            t.z += p.scale * a[4 * k4 + 2];
+                            t.w += p.scale * a[4 * k4 + 3];
+                            aq4[k4] = t;
+                        }
+                        continue;
+                    }
                     uint4 *dst = reinterpret_cast<uint4 *>(qrow + c * 32);
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {
@@ -986,7 +1023,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         dst[k4] = v;
                     }
                 }
-            } else {
+            } else if (!p.acc_dq) {
                 uint4 *dst = reinterpret_cast<uint4 *>(qrow);
                 for (int k4 = 0; k4 < kOH / 8; ++k4) dst[k4] = make_uint4(0, 0, 0, 0);
             }

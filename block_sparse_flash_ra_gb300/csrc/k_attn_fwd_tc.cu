@@ -152,6 +152,115 @@ constexpr uint32_t kSideRegs = 48;
 static_assert(256 * kSoftmaxRegs + 128 * kCorrRegs + 128 * kSideRegs <= kFwdThreads * kLaunchRegs,
               "register split exceeds the block's launch registers");
 
+// Correction-warp work of one unit in ring-step mode (ra_attn_fwd_step):
+// the chunk's partial (O_s, lse_s) -- (0, -inf) for an empty chunk, with the
+// sink in the denominator when `sink_here` -- merged by the pages' update
+// (_update_out_and_lse) into the running pair (p.run_out, p.run_lse) of this
+// thread's query row, read from global memory (unless p.step_first: then the
+// running pair is (0, -inf)) and written back; the bf16 `out`, if given, gets
+// the merged row too.  O_s passes through TMEM columns [kColRun, +D) (idle in
+// this mode), so that O_acc is released to the next unit as soon as it has
+// been read.  Returns false when a wait gave up.
+template <int D, typename WaitAll>
+__device__ __forceinline__ bool step_merge(const Problem &p, const Unit &x, int row, int qi,
+                                           uint32_t lane_base, const Bars &bars, const float *stat_l,
+                                           const float *stat_m, uint32_t &nshard, uint32_t &n_of,
+                                           bool sink_here, float sink2, __nv_bfloat16 *out,
+                                           WaitAll &wait_all)
+{
+    using C = FwdCfg<D>;
+    const size_t ro = (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D;
+    float *lrun = p.run_lse + ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
+    const bool nonempty = x.cnt > 0; // uniform over the CTA
+    float lse_s = sink_here ? sink2 * kLn2 : -INFINITY;
+    if (nonempty) {
+        const int slot = nshard & 1;
+        if (!wait_all(bars.stat_full + slot, (nshard >> 1) & 1)) return false;
+        ++nshard;
+        float l = stat_l[slot * 256 + row] + stat_l[slot * 256 + 128 + row];
+        const float m_ref = stat_m[slot * 128 + row];
+        if (!wait_all(bars.o_full, n_of++ & 1)) return false;
+        tc_fence_after();
+        float m_fin = m_ref, fac = 1.f;
+        if (sink_here) {
+            m_fin = fmaxf(m_ref, sink2);
+            fac = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_fin);
+            l = l * fac + ex2_approx(sink2 - m_fin);
+        }
+        float inv = 0.f;
+        if (l > 0.f) {
+            lse_s = (m_fin + lg2_approx(l)) * kLn2;
+            inv = fac * rcp_approx(l);
+        } else {
+            lse_s = -INFINITY;
+        }
+        // O_s = O_acc / l into the idle O_run columns; then O_acc is free
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+            float a[16];
+            tmem_ld16(lane_base + C::kColO + c * 16, a);
+            tmem_ld_wait();
+            if (c == D / 16 - 1) {
+                tc_fence_before();
+                mbar_arrive(bars.o_empty);
+            }
+            uint32_t w16[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w16[j] = __float_as_uint(a[j] * inv);
+            tmem_st16(lane_base + C::kColRun + c * 16, w16);
+        }
+        tmem_st_wait();
+    }
+    const float lse_in = p.step_first ? -INFINITY : *lrun;
+    const bool first = lse_in == -INFINITY;
+    const float w = first ? 1.f : sigmoid_fast(lse_s - lse_in);
+    float *grow = p.run_out + ro;
+    __nv_bfloat16 *orow = out ? out + ro : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < D / 16; ++c) {
+        float os[16];
+        if (nonempty) {
+            tmem_ld16(lane_base + C::kColRun + c * 16, os);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) os[j] = 0.f;
+        }
+        float4 *g4 = reinterpret_cast<float4 *>(grow + c * 16);
+        float nv[16];
+        if (first) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) nv[j] = os[j];
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 cv = g4[k];
+                nv[4 * k + 0] = cv.x - w * (cv.x - os[4 * k + 0]);
+                nv[4 * k + 1] = cv.y - w * (cv.y - os[4 * k + 1]);
+                nv[4 * k + 2] = cv.z - w * (cv.z - os[4 * k + 2]);
+                nv[4 * k + 3] = cv.w - w * (cv.w - os[4 * k + 3]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            g4[k] = make_float4(nv[4 * k + 0], nv[4 * k + 1], nv[4 * k + 2], nv[4 * k + 3]);
+        if (orow) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                uint4 v;
+                v.x = pack_bf16x2(nv[8 * k + 0], nv[8 * k + 1]);
+                v.y = pack_bf16x2(nv[8 * k + 2], nv[8 * k + 3]);
+                v.z = pack_bf16x2(nv[8 * k + 4], nv[8 * k + 5]);
+                v.w = pack_bf16x2(nv[8 * k + 6], nv[8 * k + 7]);
+                dst[k] = v;
+            }
+        }
+    }
+    *lrun = first ? lse_s : lse_in + softplus_fast(lse_s - lse_in);
+    return true;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -367,6 +476,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float *lrow = lse + ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
             const bool has_sink = p.sinks != nullptr;
             const float sink2 = has_sink ? p.sinks[x.h] * kLog2e : 0.f;
+            if (p.run_out) {
+                // one ring step: merge this chunk's partial into the running
+                // pair in global memory (one shard per unit, N == 1)
+                if (!(ok = step_merge<D>(p, x, row, qi, lane_base, bars, stat_l, stat_m, nshard, n_of,
+                                         has_sink && p.step_sink, sink2, out, wait_all)))
+                    break;
+                continue;
+            }
             float lse_run = -INFINITY;
             bool orun_set = false;    // uniform: O_run columns hold this unit's data
             bool out_written = false; // uniform: the last merge stored the output itself

@@ -257,6 +257,9 @@ Problem make_problem(const ra_attn_params *p, const ra_block_mask *m, int *statu
     }
     x.hsplit = 1;
     x.dkv_part = nullptr;
+    x.run_out = x.run_lse = nullptr;
+    x.step_sink = x.step_first = 0;
+    x.acc_dq = x.acc_dk = x.acc_dv = nullptr;
     x.status = status;
     x.timeout_ns = g_timeout_ns.load();
     return x;
@@ -409,6 +412,75 @@ RA_API int ra_attn_fwd(const ra_attn_params *p, const void *q, const void *k, co
     if ((rc = encode_rows(&tv, v, p->B, p->Lkv, p->Hkv, p->D))) return rc;
     e = launch_fwd_tc(pr, &tq, &tk, &tv, out, lse, dc->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    count(1);
+    return RA_OK;
+}
+
+RA_API int ra_attn_fwd_step(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                            const ra_block_mask *mask, int flags, float *out_run, float *lse_run,
+                            void *out, ra_stream_t stream)
+{
+    int rc = check_params(p);
+    if (rc) return rc;
+    if (p->n_virtual_shards != 1)
+        return fail(RA_ERR_INVALID_ARG, "a ring step takes one key/value chunk: n_virtual_shards "
+                                        "must be 1 (got %d)", p->n_virtual_shards);
+    if (flags & ~(RA_STEP_SINKS | RA_STEP_FIRST)) return fail(RA_ERR_INVALID_ARG, "unknown step flags");
+    if (!q || !k || !v || !out_run || !lse_run) return fail(RA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_run) ||
+        !aligned16(lse_run) || (out && !aligned16(out)))
+        return fail(RA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+    if ((rc = check_mask(p, mask))) return rc;
+    if (p->D != 64 && p->D != 128) return fail(RA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", p->D);
+    if (p->dtype != RA_BF16)
+        return fail(RA_ERR_UNSUPPORTED, "ring steps are implemented for bf16 inputs");
+    DevCache *dc = nullptr;
+    if ((rc = device_cache(&dc))) return rc;
+    Problem pr = make_problem(p, mask, dc->status);
+    pr.run_out = out_run;
+    pr.run_lse = lse_run;
+    pr.step_sink = (flags & RA_STEP_SINKS) ? 1 : 0;
+    pr.step_first = (flags & RA_STEP_FIRST) ? 1 : 0;
+    cudaError_t e;
+    bool &done = p->D == 64 ? dc->attr_fwd64 : dc->attr_fwd128;
+    if (!done) {
+        if ((e = fwd_tc_set_attributes(p->D)) != cudaSuccess) return cuda_fail(e, "forward attributes");
+        done = true;
+    }
+    alignas(64) CUtensorMap tq, tk, tv;
+    if ((rc = encode_rows(&tq, q, p->B, p->Lq, p->Hq, p->D))) return rc;
+    if ((rc = encode_rows(&tk, k, p->B, p->Lkv, p->Hkv, p->D))) return rc;
+    if ((rc = encode_rows(&tv, v, p->B, p->Lkv, p->Hkv, p->D))) return rc;
+    e = launch_fwd_tc(pr, &tq, &tk, &tv, out, lse_run, dc->num_sms,
+                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "forward step launch");
+    count(1);
+    return RA_OK;
+}
+
+RA_API int ra_cast_from_f32(const float *in, void *out, size_t n, int dtype, ra_stream_t stream)
+{
+    if (!in || !out) return fail(RA_ERR_INVALID_ARG, "NULL pointer");
+    if (n == 0) return fail(RA_ERR_INVALID_ARG, "n must be positive");
+    if (dtype != RA_BF16 && dtype != RA_FP32) return fail(RA_ERR_INVALID_ARG, "dtype must be RA_BF16 or RA_FP32");
+    if (!aligned16(in) || !aligned16(out)) return fail(RA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    const size_t ob = n * (dtype == RA_BF16 ? 2 : 4);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
+    if (a < b + ob && b < a + n * 4) return fail(RA_ERR_INVALID_ARG, "in and out overlap");
+    cudaError_t e = launch_cast_from_f32(in, out, n, dtype, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cast launch");
+    count(1);
+    return RA_OK;
+}
+
+RA_API int ra_add_f32(float *acc, const float *x, size_t n, ra_stream_t stream)
+{
+    if (!acc || !x) return fail(RA_ERR_INVALID_ARG, "NULL pointer");
+    if (n == 0) return fail(RA_ERR_INVALID_ARG, "n must be positive");
+    const uintptr_t a = reinterpret_cast<uintptr_t>(acc), b = reinterpret_cast<uintptr_t>(x);
+    if (a != b && a < b + n * 4 && b < a + n * 4) return fail(RA_ERR_INVALID_ARG, "acc and x overlap");
+    cudaError_t e = launch_add_f32(acc, x, n, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "add launch");
     count(1);
     return RA_OK;
 }
@@ -591,6 +663,29 @@ RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k,
     if (rc) return rc;
     const Problem pr = make_problem(p, mask, dc->status);
     return bwd_tc_kernels(p, dc, pr, kDq, q, k, v, dout, w, dq, nullptr, nullptr,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+RA_API int ra_attn_bwd_step(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                            const void *dout, const ra_block_mask *mask, float *dq_acc,
+                            float *dk_acc, float *dv_acc, const void *ws, size_t ws_bytes,
+                            ra_stream_t stream)
+{
+    if (!mask) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
+    if (p && p->n_virtual_shards != 1)
+        return fail(RA_ERR_INVALID_ARG, "a ring step takes one key/value chunk: n_virtual_shards "
+                                        "must be 1 (got %d)", p->n_virtual_shards);
+    const void *ptrs[7] = {q, k, v, dout, dq_acc, dk_acc, dv_acc};
+    DevCache *dc = nullptr;
+    BwdWs w{};
+    int rc = bwd_common(p, ptrs, 7, mask, const_cast<void *>(ws), ws_bytes, &dc, &w, false);
+    if (rc) return rc;
+    Problem pr = make_problem(p, mask, dc->status);
+    pr.acc_dq = dq_acc;
+    pr.acc_dk = dk_acc;
+    pr.acc_dv = dv_acc;
+    // the gradient kernels never write their bf16 outputs in this mode
+    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, dout, w, dq_acc, dk_acc, dv_acc,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 

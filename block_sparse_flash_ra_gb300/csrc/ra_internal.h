@@ -43,6 +43,18 @@ struct Problem {
     // that a reduction sums into dk, dv
     int hsplit;
     float *dkv_part;
+    // one ring step (ra_attn_fwd_step / ra_attn_bwd_step): a single KV chunk
+    // (N == 1) whose results are merged into, or added to, fp32 state in
+    // global memory instead of being written as the final outputs.
+    //   forward: run_out (B, Lq, Hq, D) and run_lse (B, Hq, Lq) are the
+    //   running pair (read unless step_first, then written); step_sink counts
+    //   the sinks in this step; the bf16 `out` of the launch, if not NULL,
+    //   receives the merged result (the last step's cast).
+    //   backward: acc_dq (B, Lq, Hq, D), acc_dk / acc_dv (B, Lkv, Hkv, D)
+    //   receive += of the step's scaled gradients (hsplit == 1).
+    float *run_out, *run_lse;
+    int step_sink, step_first;
+    float *acc_dq, *acc_dk, *acc_dv;
     // failure reporting
     int *status;
     uint64_t timeout_ns;
@@ -79,6 +91,10 @@ cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_
 cudaError_t launch_bwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,
                                 const float *dout, const float *lse, const float *delta,
                                 float *dq, float *dk, float *dv, cudaStream_t s);
+
+// fp32 -> bf16 (or a copy for fp32) of n elements; acc += x over n floats
+cudaError_t launch_cast_from_f32(const float *in, void *out, size_t n, int dtype, cudaStream_t s);
+cudaError_t launch_add_f32(float *acc, const float *x, size_t n, cudaStream_t s);
 
 cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, int *gave_up, cudaStream_t s);
 

@@ -325,6 +325,68 @@ RA_API int ra_attn_bwd_noalloc(const ra_attn_params *p, const void *q, const voi
 RA_API size_t ra_attn_bwd_noalloc_max_workspace(void);
 
 /*
+ * One step of the ring, for callers that run the ring themselves -- one
+ * query shard per GPU, key/value chunks passed from device to device
+ * ("ejKernel ring_attention._ring_splash" module source,
+ * _ring_attention_forward: the loop body; _ring_attention_backward: the
+ * scan body).  The params describe the step's pair: Lq = the local query
+ * rows, Lkv = the rows of the key/value chunk this step holds, and
+ * n_virtual_shards = 1; positions and segment ids of the chunk travel with
+ * it (kv_pos / kv_seg), so that the causal rule q_pos >= kv_pos is the pages'
+ * per-step offset device_idx * q_len - kv_src * kv_len when the positions are
+ * the tokens' global indices.  The block map is built for these params.
+ */
+enum { RA_STEP_SINKS = 1, RA_STEP_FIRST = 2 };
+
+/*
+ * Forward step: the chunk's partial (out, lse) -- with the sinks in the
+ * denominator when flags has RA_STEP_SINKS (the pages: step 0 only) -- merged
+ * by _update_out_and_lse into the running pair.
+ *   q (B,Lq,Hq,D), k, v (B,Lkv,Hkv,D) bf16: the local queries and the chunk.
+ *   out_run (B,Lq,Hq,D) fp32 and lse_run (B,Hq,Lq) fp32: the running pair,
+ *   read and written in place; with RA_STEP_FIRST they are not read and the
+ *   running pair is taken as (0, -inf) (the pages' initial state).
+ *   out: NULL, or (B,Lq,Hq,D) bf16 that also receives the merged output (the
+ *   final cast to the query dtype after the last step).
+ * lse_run ends as the natural-log lse of the rows over every chunk merged so
+ * far (-inf for rows with nothing visible).
+ * Errors: RA_ERR_INVALID_ARG (n_virtual_shards != 1, flags, pointers, mask),
+ * RA_ERR_UNSUPPORTED (D, fp32 inputs), RA_ERR_CUDA.
+ */
+RA_API int ra_attn_fwd_step(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                            const ra_block_mask *mask, int flags, float *out_run, float *lse_run,
+                            void *out, ra_stream_t stream);
+
+/*
+ * Backward step: the gradient contributions of the pair (local queries, this
+ * chunk), computed with the FINAL out and lse, added to fp32 accumulators:
+ *   dq_acc (B,Lq,Hq,D) += this chunk's part of dq (the local accumulator);
+ *   dk_acc, dv_acc (B,Lkv,Hkv,D) += the local queries' part of the chunk's
+ *   dk, dv (the accumulators that travel with the chunk).
+ * ws: the workspace ra_attn_bwd_prep filled for the same local rows (Delta,
+ * -lse * log2 e); run ra_attn_bwd_prep once per backward, before the steps
+ * (it also gives this device's dsinks, whose sum over the devices is the
+ * pages' psum).  The query heads of a kv head are never split here.
+ * Errors: as ra_attn_bwd.
+ */
+RA_API int ra_attn_bwd_step(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                            const void *dout, const ra_block_mask *mask, float *dq_acc,
+                            float *dk_acc, float *dv_acc, const void *ws, size_t ws_bytes,
+                            ra_stream_t stream);
+
+/*
+ * The ring's last elementwise steps (_ring_attention_backward: the casts of
+ * dq, dk, dv "to input dtypes"; the psum of dsinks).
+ *   ra_cast_from_f32: out[i] = in[i] in `dtype` (RA_BF16: round to nearest
+ *   even; RA_FP32: a copy), n elements, buffers 16-byte aligned and disjoint.
+ *   ra_add_f32: acc[i] += x[i], n floats (the sum of per-device dsinks when
+ *   several ring devices share one GPU).
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_CUDA.
+ */
+RA_API int ra_cast_from_f32(const float *in, void *out, size_t n, int dtype, ra_stream_t stream);
+RA_API int ra_add_f32(float *acc, const float *x, size_t n, ra_stream_t stream);
+
+/*
  * Zigzag load-balancing permutation along the sequence (Kvax context
  * parallelism).  The sequence of L rows is split into 2N chunks of L/(2N);
  * virtual device d holds chunk d followed by chunk 2N-1-d, so permuted row

@@ -50,3 +50,35 @@ def attention(q, k, v, *, scale, soft_cap=None, causal=False, q_pos=None, kv_pos
     p = np.where(np.isfinite(lse)[..., None], p, 0.0)
     out = np.einsum("bhij,bjhd->bihd", p, vv)
     return out, lse
+
+
+def chunk_grads(q, k, v, dout, lse, delta, *, scale, soft_cap=None, causal=False, q_pos=None,
+                kv_pos=None, q_seg=None, kv_seg=None, pad=-1):
+    """Gradient contributions of one (query rows, key chunk) pair with the
+    FINAL lse of the query rows and Delta = <dO, O> (B, H, Lq): returns
+    (dq, dk, dv) of this pair, dk / dv summed over the query heads of a kv
+    head."""
+    q, k, v, dout = (np.asarray(a, np.float64) for a in (q, k, v, dout))
+    B, Lq, Hq, D = q.shape
+    Lkv, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    kk = np.repeat(k, G, axis=2)
+    vv = np.repeat(v, G, axis=2)
+    raw = scale * np.einsum("bihd,bjhd->bhij", q, kk)
+    s = soft_cap * np.tanh(raw / soft_cap) if soft_cap else raw
+    vis = visibility(B, Lq, Lkv, causal=causal, q_pos=q_pos, kv_pos=kv_pos, q_seg=q_seg,
+                     kv_seg=kv_seg, pad=pad)[:, None]
+    lse = np.asarray(lse, np.float64)
+    fin = np.isfinite(lse)[..., None]
+    with np.errstate(invalid="ignore", over="ignore"):
+        p = np.where(vis & fin, np.exp(s - np.where(fin, lse[..., None], 0.0)), 0.0)
+    dp = np.einsum("bihd,bjhd->bhij", dout, vv)
+    ds = p * (dp - np.asarray(delta, np.float64)[..., None])
+    if soft_cap:
+        ds = ds * (1.0 - (s / soft_cap) ** 2)
+    dq = scale * np.einsum("bhij,bjhd->bihd", ds, kk)
+    dk_h = scale * np.einsum("bhij,bihd->bjhd", ds, q)
+    dv_h = np.einsum("bhij,bihd->bjhd", p, dout)
+    dk = dk_h.reshape(B, Lkv, Hkv, G, D).sum(axis=3)
+    dv = dv_h.reshape(B, Lkv, Hkv, G, D).sum(axis=3)
+    return dq, dk, dv
