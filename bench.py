@@ -187,6 +187,8 @@ class Pipeline:
             kv_seg=src["kv_seg"], sinks=d["sinks"], local_mask=d["local_mask"])
         self.mask_buf = torch.empty(ra.ra_block_mask_bytes(self.params), dtype=torch.uint8, device="cuda")
         self.ws = torch.empty(ra.ra_attn_bwd_workspace_size(self.params), dtype=torch.uint8, device="cuda")
+        n_fws = ra.ra_attn_fwd_workspace_size(self.params)
+        self.fws = torch.empty(n_fws, dtype=torch.uint8, device="cuda") if n_fws else None
         self.mask = ra.RaBlockMask()
         self.names = ["permute", "mask", "fwd", "unpermute_fwd", "bwd_prep", "bwd_dkdv", "bwd_dq",
                       "unpermute_bwd"]
@@ -231,7 +233,7 @@ class Pipeline:
         ra.ra_build_block_mask(self.params, self.mask_buf, self.mask)
         mark("mask", 1)
         mark("fwd", 0)
-        ra.ra_attn_fwd(self.params, p["q"], p["k"], p["v"], self.mask, self.out, self.lse)
+        ra.ra_attn_fwd(self.params, p["q"], p["k"], p["v"], self.mask, self.out, self.lse, ws=self.fws)
         mark("fwd", 1)
         mark("unpermute_fwd", 0)
         if w.zigzag:

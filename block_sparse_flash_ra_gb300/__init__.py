@@ -311,11 +311,15 @@ def build_mask(params, device=None, stream=None) -> RaBlockMask:
     return ra_build_block_mask(params, buf, stream=stream)
 
 
-def forward(params, q, k, v, mask, stream=None):
+def forward(params, q, k, v, mask, stream=None, workspace=True):
+    """Forward; with ``workspace`` the optional fp32 workspace that lets the
+    library run two query heads per CTA is allocated (when it applies)."""
     B, Lq, Hq, D = q.shape
     out = torch.empty_like(q)
     lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
-    ra_attn_fwd(params, q, k, v, mask, out, lse, stream=stream)
+    n = ra_attn_fwd_workspace_size(params) if workspace else 0
+    ws = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    ra_attn_fwd(params, q, k, v, mask, out, lse, ws=ws, stream=stream)
     return out, lse
 
 

@@ -1,0 +1,750 @@
+// k_attn_fwd2_tc.cu -- the forward of k_attn_fwd_tc.cu with two query heads
+// per CTA in ping-pong, for D = 128 and an even number of query heads per kv
+// head (GQA, MQA).
+//
+// What it computes is the same ("ejKernel ring_attention._ring_splash"
+// module source, _ring_attention_forward and _update_out_and_lse; Kvax
+// "Flash Attention for JAX", flash_attention): for each (b, h, 128-row query
+// tile) on virtual device d the KV shards are visited in ring order
+// s = (d - t) mod N, each shard's non-empty tiles go through an online
+// softmax, and the shard's partial (O_s = O_acc / l, lse_s), with the sink in
+// the denominator at t = 0, is merged into the running (O_run, lse_run) by the
+// sigmoid/softplus update.  Output bf16, lse fp32.
+//
+// Design (one CTA per SM, persistent, longest-row-first static schedule over
+// pairs of query heads h0 = 2j, h1 = 2j + 1 of one (b, q tile) -- the pair
+// shares its kv head, so every K and V tile is loaded once for both):
+//   warps 0-3   softmax of head A (h0): thread t owns query row t and all 128
+//               columns of its S row -- no exchange between threads
+//   warps 4-7   softmax of head B (h1), the same
+//   warps 8-11  correction warpgroup: the ring's shard-end merge of both
+//               heads and the unit's bf16 output and lse
+//   warp 12     TMA producer: Q of both heads once per unit, K and V tiles
+//               into 2-stage rings
+//   warp 13     TMEM allocator and single-thread MMA issuer
+//   warps 14-15 no role (setmaxnreg donors)
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384),
+// O_B [384,512); P (bf16) overwrites the first 64 columns of its S buffer.
+// MMA order per tile g: PV_A(g), S_A(g+1), PV_B(g), S_B(g+1): while one
+// head's softmax runs, the tensor pipe computes the other head's products,
+// and the two softmax warpgroups interleave their exponent phases on the
+// MUFU units instead of running them at the same time.  S_X(g+1) completing
+// implies PV_X(g) has completed (one issuing thread, in order), so a softmax
+// warp never waits for a PV product separately.
+// The running output O_run of both heads lives in the caller's workspace
+// (fp32, one slot per CTA): at a shard end the correction warps first copy
+// O_s = O_acc / l out of TMEM (to O_run itself for the unit's first merge,
+// else to a staging slot), release O_acc to the next shard's first PV
+// product, and only then merge staging into O_run -- off the softmax's path.
+#include <math.h>
+
+#include "ra_sched.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kD2 = 128;
+constexpr int kTileBytes2 = kTile * kD2 * 2; // 32 KB: one 128-row bf16 tile
+constexpr int kStages2 = 2;                  // K and V rings
+// CTAs the workspace has slots for (at most one per SM; a fixed figure, so
+// that the workspace size does not depend on the device)
+constexpr int kFwd2Slots = 160;
+
+struct Fwd2Cfg {
+    static constexpr int kQAOff = 0;
+    static constexpr int kQBOff = kTileBytes2;
+    static constexpr int kKOff = 2 * kTileBytes2;
+    static constexpr int kVOff = kKOff + kStages2 * kTileBytes2;
+    static constexpr int kBarOff = kVOff + kStages2 * kTileBytes2;
+    // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2],
+    // s_full[2 heads], p_full[2], stat_full[2 heads][2 slots], o_full[2],
+    // o_empty[2], drain
+    static constexpr int kNumBars = 2 + 4 * kStages2 + 2 + 2 + 4 + 2 + 2 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kStatOff = kMiscOff + 16; // l then m: [2 heads][2 slots][128] each
+    static constexpr int kSmemUsed = kStatOff + 2 * 2 * 2 * 128 * 4;
+    static constexpr int kSmem = kSmemUsed + 1024;
+    static_assert(kSmem <= 232448, "forward shared memory exceeds the 227 KB per-block limit");
+    static constexpr uint32_t kColO = 256; // O_A at 256, O_B at 384
+    static constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16(128, kD2, false, true);
+};
+
+struct Bars2 {
+    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
+        *stat_full, *o_full, *o_empty, *drain;
+};
+
+__device__ __forceinline__ Bars2 carve_bars2(uint8_t *smem)
+{
+    using C = Fwd2Cfg;
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    Bars2 r;
+    r.q_full = b;
+    r.q_empty = b + 1;
+    r.k_full = b + 2;
+    r.k_empty = r.k_full + kStages2;
+    r.v_full = r.k_empty + kStages2;
+    r.v_empty = r.v_full + kStages2;
+    r.s_full = r.v_empty + kStages2;  // [head]
+    r.p_full = r.s_full + 2;          // [head]
+    r.stat_full = r.p_full + 2;       // [head][slot]
+    r.o_full = r.stat_full + 4;       // [head]
+    r.o_empty = r.o_full + 2;         // [head]
+    r.drain = r.o_empty + 2;
+    return r;
+}
+
+// Work unit u -> (row id b*nq+qt from the longest-first order, head pair).
+struct Unit2 {
+    int b, qt, h0, row, cnt, dev;
+    const int32_t *list, *shard, *pfwd;
+};
+
+__device__ __forceinline__ Unit2 unit2_of(const Problem &p, int u)
+{
+    const int pairs = p.Hq >> 1;
+    Unit2 x;
+    x.row = p.fwd_order[u / pairs];
+    x.h0 = 2 * (u % pairs);
+    x.b = x.row / p.nq;
+    x.qt = x.row - x.b * p.nq;
+    x.cnt = p.fwd_cnt[x.row];
+    x.dev = x.qt / p.tq;
+    x.list = p.fwd_idx + (size_t)x.row * p.nk;
+    x.shard = p.fwd_shard + (size_t)x.row * (p.N + 1);
+    x.pfwd = p.part_fwd + (size_t)x.row * (p.N + 1);
+    return x;
+}
+
+// Walk over a unit's non-empty tiles in ring order: shards s = (dev - t) mod N
+// for t = 0..N-1, each shard's tiles in ascending order.
+struct RingWalk {
+    int t, e, hi;
+    __device__ __forceinline__ void start(const Problem &p, const Unit2 &x)
+    {
+        t = -1;
+        e = hi = 0;
+        advance_shard(p, x);
+    }
+    __device__ __forceinline__ void advance_shard(const Problem &p, const Unit2 &x)
+    {
+        while (e >= hi && ++t < p.N) {
+            const int src = (x.dev - t + p.N) % p.N;
+            e = x.shard[src];
+            hi = x.shard[src + 1];
+        }
+    }
+    __device__ __forceinline__ bool valid(const Problem &p) const { return t < p.N; }
+    // the current tile; `first` / `last`: it opens / closes its shard
+    __device__ __forceinline__ void get(const Unit2 &x, int &kt, bool &first, bool &last,
+                                        int lo_of_shard) const
+    {
+        kt = x.list[e];
+        first = (e == lo_of_shard);
+        last = (e == hi - 1);
+    }
+};
+
+constexpr int kThreads2 = 512;
+constexpr int kCorrWarp0_2 = 8;
+constexpr int kProducerWarp2 = 12;
+constexpr int kMmaWarp2 = 13;
+constexpr int kLaunchRegs2 = 128;
+constexpr uint32_t kSoftmaxRegs2 = 176;
+constexpr uint32_t kCorrRegs2 = 64;
+constexpr uint32_t kSideRegs2 = 96;
+static_assert(256 * kSoftmaxRegs2 + 128 * kCorrRegs2 + 128 * kSideRegs2 <= kThreads2 * kLaunchRegs2,
+              "register split exceeds the block's launch registers");
+
+// Visibility bits of a whole 128-column row of a PARTIAL tile: bit z of word
+// w is set iff query row qi sees kv row kt * 128 + 32 w + z.
+__device__ __forceinline__ uint4 row_bits128(const Problem &p, int slot, int row, int b, int kt,
+                                             int qi, int q_seg, bool q_pad, int q_pos)
+{
+    if (slot < p.part_cap)
+        return __ldg(reinterpret_cast<const uint4 *>(p.part_rows + ((size_t)slot * kTile + row) * 4));
+    const uint2 lo = row_bits_derived(p, b, kt * kTile, qi, q_seg, q_pad ? 1 : 0, q_pos);
+    const uint2 hi = row_bits_derived(p, b, kt * kTile + 64, qi, q_seg, q_pad ? 1 : 0, q_pos);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
+}
+
+__device__ __forceinline__ void store_bf16_16(__nv_bfloat16 *dst, const float *v)
+{
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * k + 0], v[8 * k + 1]);
+        w.y = pack_bf16x2(v[8 * k + 2], v[8 * k + 3]);
+        w.z = pack_bf16x2(v[8 * k + 4], v[8 * k + 5]);
+        w.w = pack_bf16x2(v[8 * k + 6], v[8 * k + 7]);
+        d4[k] = w;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads2, 1)
+    fwd2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, Problem p,
+                   __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
+                   float *__restrict__ ws)
+{
+    using C = Fwd2Cfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const Bars2 bars = carve_bars2(smem);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+    const WaitCtx ctx{abort_flag, p.status, p.timeout_ns};
+    float *stat_l = reinterpret_cast<float *>(smem + C::kStatOff); // [head][slot][128]
+    float *stat_m = stat_l + 2 * 2 * 128;                           // [head][slot][128]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int U = p.B * p.nq * (p.Hq >> 1);
+    const int G = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
+        for (int s = 0; s < kStages2; ++s) {
+            mbar_init(bars.k_full + s, 1);
+            mbar_init(bars.k_empty + s, 1);
+            mbar_init(bars.v_full + s, 1);
+            mbar_init(bars.v_empty + s, 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bars.s_full + h, 1);
+            mbar_init(bars.p_full + h, 128);
+            mbar_init(bars.stat_full + 2 * h, 128);
+            mbar_init(bars.stat_full + 2 * h + 1, 128);
+            mbar_init(bars.o_full + h, 1);
+            mbar_init(bars.o_empty + h, 128);
+        }
+        mbar_init(bars.drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp2) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp2 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp >= kProducerWarp2) {
+        regs_shrink<kSideRegs2>();
+        if (warp == kProducerWarp2 && lane == 0) {
+            // ------------------------------------------------------------ producer
+            uint32_t g = 0, uq = 0;
+            uint32_t k_issued[kStages2] = {}, v_issued[kStages2] = {};
+            bool ok = true;
+            for (int r = 0; ok && r * G < U; ++r) {
+                const int u = unit_index(r, blockIdx.x, G);
+                if (u >= U) continue;
+                const Unit2 x = unit2_of(p, u);
+                if (x.cnt == 0) continue;
+                if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
+                mbar_expect_tx(bars.q_full, 2 * kTileBytes2);
+                for (int hb = 0; hb < 2; ++hb) {
+                    tma_load_4d(smem + C::kQAOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h0,
+                                x.qt * kTile, x.b);
+                    tma_load_4d(smem + C::kQBOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h0 + 1,
+                                x.qt * kTile, x.b);
+                }
+                ++uq;
+                const int g_kv = x.h0 / p.G;
+                RingWalk it;
+                for (it.start(p, x); ok && it.valid(p); ++it.e, it.advance_shard(p, x)) {
+                    const int kt = x.list[it.e];
+                    const int st = g % kStages2;
+                    const uint32_t ph = ((g / kStages2) & 1) ^ 1;
+                    if (!(ok = mbar_wait(bars.k_empty + st, ph, ctx))) break;
+                    mbar_expect_tx(bars.k_full + st, kTileBytes2);
+                    for (int hb = 0; hb < 2; ++hb)
+                        tma_load_4d(smem + C::kKOff + st * kTileBytes2 + hb * 16384, &tm_k,
+                                    bars.k_full + st, hb * 64, g_kv, kt * kTile, x.b);
+                    ++k_issued[st];
+                    if (!(ok = mbar_wait(bars.v_empty + st, ph, ctx))) break;
+                    mbar_expect_tx(bars.v_full + st, kTileBytes2);
+                    for (int hb = 0; hb < 2; ++hb)
+                        tma_load_4d(smem + C::kVOff + st * kTileBytes2 + hb * 16384, &tm_v,
+                                    bars.v_full + st, hb * 64, g_kv, kt * kTile, x.b);
+                    ++v_issued[st];
+                    ++g;
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < kStages2; ++s) {
+                    if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
+                    if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
+                }
+                if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
+            }
+        } else if (warp == kMmaWarp2 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            // Shared-memory descriptors are built once; an operand at byte
+            // offset o from a base has the base's descriptor plus o / 16 (the
+            // start-address field cannot carry: shared memory is < 256 KB).
+            const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kQAOff), 16, 1024);
+            const uint64_t dq1 = sdesc_sw128(smem_u32(smem + C::kQBOff), 16, 1024);
+            const uint64_t dk = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+            const uint64_t dv = sdesc_sw128(smem_u32(smem + C::kVOff), 16384, 1024);
+            constexpr uint64_t kStageStep = kTileBytes2 >> 4;
+            uint32_t gk = 0, gv = 0, gp = 0, uq = 0, n_oe = 0;
+            bool ok = true;
+#define RA_ISSUE_S(QD, TCOL, KS)                                                                   \
+    do {                                                                                           \
+        const uint64_t kd_ = dk + (uint64_t)(KS) * kStageStep;                                     \
+        _Pragma("unroll") for (int kk = 0; kk < kD2 / 16; ++kk) {                                  \
+            const uint64_t o_ = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);              \
+            mma_ss(tmem + (TCOL), (QD) + o_, kd_ + o_, C::kIdescQK, kk > 0 ? 1u : 0u);             \
+        }                                                                                          \
+    } while (0)
+#define RA_ISSUE_PV(H, VS, FIRST)                                                                  \
+    do {                                                                                           \
+        const uint64_t vd_ = dv + (uint64_t)(VS) * kStageStep;                                     \
+        _Pragma("unroll") for (int kk = 0; kk < kTile / 16; ++kk)                                  \
+            mma_ts(tmem + C::kColO + (H) * 128, tmem + (H) * 128 + kk * 8,                         \
+                   vd_ + (uint64_t)((kk * 2048) >> 4), C::kIdescPV, (kk > 0 || !(FIRST)) ? 1u : 0u); \
+    } while (0)
+            for (int r = 0; ok && r * G < U; ++r) {
+                const int u = unit_index(r, blockIdx.x, G);
+                if (u >= U) continue;
+                const Unit2 x = unit2_of(p, u);
+                if (x.cnt == 0) continue;
+                if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                ++uq;
+                RingWalk it;
+                it.start(p, x);
+                int lo = it.e; // first position of the current shard
+                int kt;
+                bool cf, cl;
+                it.get(x, kt, cf, cl, lo);
+                uint32_t ks = gk % kStages2;
+                if (!(ok = mbar_wait(bars.k_full + ks, (gk / kStages2) & 1, ctx))) break;
+                tc_fence_after();
+                RA_ISSUE_S(dq0, 0, ks);
+                tc_commit(bars.s_full + 0);
+                RA_ISSUE_S(dq1, 128, ks);
+                tc_commit(bars.s_full + 1);
+                tc_commit(bars.k_empty + ks);
+                ++gk;
+                int done = 1;
+                if (done == x.cnt) tc_commit(bars.q_empty);
+                while (true) {
+                    // the next tile in ring order, if any
+                    const int cur_t = it.t;
+                    ++it.e;
+                    it.advance_shard(p, x);
+                    const bool has_next = it.valid(p);
+                    bool nf = false, nl = false;
+                    if (has_next) {
+                        if (it.t != cur_t) lo = it.e; // the walk entered a new shard
+                        int nkt;
+                        it.get(x, nkt, nf, nl, lo);
+                    }
+                    const uint32_t vs = gv % kStages2;
+                    ks = gk % kStages2;
+                    // head A: PV of this tile, then S of the next (its S buffer held P)
+                    if (!(ok = mbar_wait(bars.p_full + 0, gp & 1, ctx))) break;
+                    if (!(ok = mbar_wait(bars.v_full + vs, (gv / kStages2) & 1, ctx))) break;
+                    if (cf && !(ok = mbar_wait(bars.o_empty + 0, (n_oe & 1) ^ 1, ctx))) break;
+                    tc_fence_after();
+                    if (cf) RA_ISSUE_PV(0, vs, true); else RA_ISSUE_PV(0, vs, false);
+                    if (cl) tc_commit(bars.o_full + 0);
+                    if (has_next) {
+                        if (!(ok = mbar_wait(bars.k_full + ks, (gk / kStages2) & 1, ctx))) break;
+                        tc_fence_after();
+                        RA_ISSUE_S(dq0, 0, ks);
+                        tc_commit(bars.s_full + 0);
+                    }
+                    // head B, the same
+                    if (!(ok = mbar_wait(bars.p_full + 1, gp & 1, ctx))) break;
+                    if (cf && !(ok = mbar_wait(bars.o_empty + 1, (n_oe & 1) ^ 1, ctx))) break;
+                    tc_fence_after();
+                    if (cf) RA_ISSUE_PV(1, vs, true); else RA_ISSUE_PV(1, vs, false);
+                    tc_commit(bars.v_empty + vs);
+                    if (cl) tc_commit(bars.o_full + 1);
+                    if (cf) ++n_oe;
+                    ++gv;
+                    ++gp;
+                    if (!has_next) break;
+                    RA_ISSUE_S(dq1, 128, ks);
+                    tc_commit(bars.s_full + 1);
+                    tc_commit(bars.k_empty + ks);
+                    ++gk;
+                    if (++done == x.cnt) tc_commit(bars.q_empty);
+                    cf = nf;
+                    cl = nl;
+                }
+            }
+#undef RA_ISSUE_S
+#undef RA_ISSUE_PV
+            tc_commit(bars.drain);
+            wait_drain(bars.drain, 0, kDrainNs);
+        }
+    } else if (warp >= kCorrWarp0_2) {
+        regs_shrink<kCorrRegs2>();
+        // ------------------------------------------------------------ correction
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        // this CTA's workspace: O_run[2 heads] then staging[2 heads], (128, D) fp32 each
+        float *orun_base = ws + (size_t)blockIdx.x * 4 * kTile * kD2;
+        uint32_t nshard = 0, n_of = 0;
+        bool ok = true;
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+        };
+        for (int r = 0; ok && r * G < U; ++r) {
+            const int u = unit_index(r, blockIdx.x, G);
+            if (u >= U) continue;
+            const Unit2 x = unit2_of(p, u);
+            const int qi = x.qt * kTile + row;
+            const bool has_sink = p.sinks != nullptr;
+            float sink2[2], lse_run[2] = {-INFINITY, -INFINITY};
+            bool out_written[2] = {false, false}, orun_set[2] = {false, false};
+            for (int h = 0; h < 2; ++h) sink2[h] = has_sink ? p.sinks[x.h0 + h] * kLog2e : 0.f;
+            int tiles_done = 0;
+            for (int t = 0; ok && x.cnt > 0 && t < p.N; ++t) {
+                const int src = (x.dev - t + p.N) % p.N;
+                const int lo = x.shard[src], hi = x.shard[src + 1];
+                const bool sink_here = has_sink && t == 0;
+                if (lo == hi) {
+                    if (sink_here)
+                        for (int h = 0; h < 2; ++h) {
+                            const float ls = sink2[h] * kLn2;
+                            lse_run[h] = (lse_run[h] == -INFINITY) ? ls
+                                                                   : lse_run[h] + softplus_fast(ls - lse_run[h]);
+                        }
+                    continue;
+                }
+                tiles_done += hi - lo;
+                const bool last = tiles_done == x.cnt;
+                const int slot = nshard & 1;
+                float w[2], lse_s[2];
+                bool first[2];
+                // phase 1, per head: O_s = O_acc / l out of TMEM, then O_acc is free
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!(ok = wait_all(bars.stat_full + 2 * h + slot, (nshard >> 1) & 1))) break;
+                    float l = stat_l[(h * 2 + slot) * 128 + row];
+                    const float m_ref = stat_m[(h * 2 + slot) * 128 + row];
+                    if (!(ok = wait_all(bars.o_full + h, n_of & 1))) break;
+                    tc_fence_after();
+                    float m_fin = m_ref, fac = 1.f;
+                    if (sink_here) {
+                        m_fin = fmaxf(m_ref, sink2[h]);
+                        fac = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_fin);
+                        l = l * fac + ex2_approx(sink2[h] - m_fin);
+                    }
+                    float inv = 0.f;
+                    lse_s[h] = -INFINITY;
+                    if (l > 0.f) {
+                        lse_s[h] = (m_fin + lg2_approx(l)) * kLn2;
+                        inv = fac * rcp_approx(l);
+                    }
+                    first[h] = lse_run[h] == -INFINITY;
+                    w[h] = first[h] ? 1.f : sigmoid_fast(lse_s[h] - lse_run[h]);
+                    // the first merge of the unit takes the block: O_s goes
+                    // straight to O_run (or, if also the last, to the output)
+                    float *dst = orun_base + ((first[h] ? 0 : 2) + h) * kTile * kD2 + (size_t)row * kD2;
+                    __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h0 + h) * kD2;
+#pragma unroll
+                    for (int c = 0; c < kD2 / 16; ++c) {
+                        float a[16];
+                        tmem_ld16(lane_base + C::kColO + h * 128 + c * 16, a);
+                        tmem_ld_wait();
+                        if (c == kD2 / 16 - 1) {
+                            tc_fence_before();
+                            mbar_arrive(bars.o_empty + h);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) a[j] *= inv;
+                        if (first[h] && last) {
+                            store_bf16_16(orow + c * 16, a);
+                        } else {
+                            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 16);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                d4[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+                        }
+                    }
+                }
+                if (!ok) break;
+                ++nshard;
+                ++n_of;
+                // phase 2, per head: O_run -= w (O_run - O_s) from the staging slot
+                for (int h = 0; h < 2; ++h) {
+                    if (!first[h]) {
+                        float *orun = orun_base + h * kTile * kD2 + (size_t)row * kD2;
+                        const float *stg = orun_base + (2 + h) * kTile * kD2 + (size_t)row * kD2;
+                        __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h0 + h) * kD2;
+                        const float wh = w[h];
+#pragma unroll 2
+                        for (int c = 0; c < kD2 / 16; ++c) {
+                            float4 cv[4], sv[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                // O_run is still (0, lse_run) after a sink-only step
+                                cv[k] = orun_set[h] ? reinterpret_cast<const float4 *>(orun + c * 16)[k]
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                                sv[k] = reinterpret_cast<const float4 *>(stg + c * 16)[k];
+                            }
+                            float nv[16];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                nv[4 * k + 0] = cv[k].x - wh * (cv[k].x - sv[k].x);
+                                nv[4 * k + 1] = cv[k].y - wh * (cv[k].y - sv[k].y);
+                                nv[4 * k + 2] = cv[k].z - wh * (cv[k].z - sv[k].z);
+                                nv[4 * k + 3] = cv[k].w - wh * (cv[k].w - sv[k].w);
+                            }
+                            if (last) {
+                                store_bf16_16(orow + c * 16, nv);
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    reinterpret_cast<float4 *>(orun + c * 16)[k] =
+                                        make_float4(nv[4 * k], nv[4 * k + 1], nv[4 * k + 2], nv[4 * k + 3]);
+                            }
+                        }
+                    }
+                    lse_run[h] = first[h] ? lse_s[h] : lse_run[h] + softplus_fast(lse_s[h] - lse_run[h]);
+                    orun_set[h] = true;
+                    out_written[h] = last;
+                }
+            }
+            if (!ok) break;
+            // ---- epilogue of both heads: the output unless the last merge
+            // stored it (O_run, or zeros for a row that saw nothing), and lse
+            for (int h = 0; h < 2; ++h) {
+                if (x.cnt == 0 && has_sink) lse_run[h] = sink2[h] * kLn2;
+                __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h0 + h) * kD2;
+                if (!out_written[h]) {
+                    if (orun_set[h]) {
+                        const float *orun = orun_base + h * kTile * kD2 + (size_t)row * kD2;
+                        for (int c = 0; c < kD2 / 16; ++c) {
+                            float a[16];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float4 v4 = reinterpret_cast<const float4 *>(orun + c * 16)[k];
+                                a[4 * k] = v4.x;
+                                a[4 * k + 1] = v4.y;
+                                a[4 * k + 2] = v4.z;
+                                a[4 * k + 3] = v4.w;
+                            }
+                            store_bf16_16(orow + c * 16, a);
+                        }
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow);
+                        for (int k = 0; k < kD2 / 8; ++k) dst[k] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                lse[((size_t)x.b * p.Hq + x.h0 + h) * p.Lq + qi] = lse_run[h];
+            }
+        }
+    } else {
+        regs_grow<kSoftmaxRegs2>();
+        // ------------------------------------------------------------ softmax
+        // Warpgroup hx (0: head A, 1: head B); thread t owns query row t.
+        const int hx = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t s_col = hx * 128;
+        const float scale2 = p.scale * kLog2e;
+        const float cap = p.soft_cap;
+        const float cap2 = cap * kLog2e;
+        const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
+        const float a_mul = cap > 0.f ? 1.f : scale2;
+        uint32_t g = 0, nshard = 0;
+        bool ok = true;
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+        };
+        for (int r = 0; ok && r * G < U; ++r) {
+            const int u = unit_index(r, blockIdx.x, G);
+            if (u >= U) continue;
+            const Unit2 x = unit2_of(p, u);
+            if (x.cnt == 0) continue;
+            const int qi = x.qt * kTile + row;
+            const int my_pos = p.q_pos ? p.q_pos[(size_t)x.b * p.Lq + qi] : qi;
+            const int my_seg = p.q_seg ? p.q_seg[(size_t)x.b * p.Lq + qi] : 0;
+            const bool my_pad = p.q_seg && my_seg == p.pad_id;
+            const uint8_t *crow = p.tile_class + (size_t)x.row * p.nk;
+            for (int t = 0; ok && t < p.N; ++t) {
+                const int src = (x.dev - t + p.N) % p.N;
+                const int lo = x.shard[src], hi = x.shard[src + 1];
+                if (lo == hi) continue;
+                int pslot = x.pfwd[src];
+                float m_ref = -INFINITY, l = 0.f;
+                for (int e = lo; ok && e < hi; ++e) {
+                    const int kt = x.list[e];
+                    const bool partial = crow[kt] == RA_TILE_PARTIAL;
+                    uint4 vis = make_uint4(~0u, ~0u, ~0u, ~0u);
+                    if (partial)
+                        vis = row_bits128(p, pslot++, row, x.b, kt, qi, my_seg, my_pad, my_pos);
+                    if (!(ok = wait_all(bars.s_full + hx, g & 1))) break;
+                    tc_fence_after();
+                    float s[128];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, s + 32 * c);
+                    tmem_ld_wait();
+                    if (cap > 0.f) {
+                        float xa = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 128; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
+                        if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny)) {
+                            const float kk = scale_over_cap;
+                            const float2 A = make_float2(cap2 * kk, cap2 * kk);
+                            const float2 B = make_float2(cap2 * kTanhC3 * kk * kk * kk,
+                                                         cap2 * kTanhC3 * kk * kk * kk);
+#pragma unroll
+                            for (int j = 0; j < 128; j += 2) {
+                                const float2 v = make_float2(s[j], s[j + 1]);
+                                const float2 rr = fmul2(v, ffma2(fmul2(v, v), B, A));
+                                s[j] = rr.x;
+                                s[j + 1] = rr.y;
+                            }
+                        } else if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
+                            const float2 k2 = make_float2(scale_over_cap, scale_over_cap);
+                            const float2 d7 = make_float2(cap2 * kTanhC7, cap2 * kTanhC7);
+                            const float2 d5 = make_float2(cap2 * kTanhC5, cap2 * kTanhC5);
+                            const float2 d3 = make_float2(cap2 * kTanhC3, cap2 * kTanhC3);
+                            const float2 d1 = make_float2(cap2, cap2);
+#pragma unroll
+                            for (int j = 0; j < 128; j += 2) {
+                                const float2 xx = fmul2(make_float2(s[j], s[j + 1]), k2);
+                                const float2 x2 = fmul2(xx, xx);
+                                float2 pp = ffma2(x2, d7, d5);
+                                pp = ffma2(x2, pp, d3);
+                                pp = ffma2(x2, pp, d1);
+                                const float2 rr = fmul2(xx, pp);
+                                s[j] = rr.x;
+                                s[j + 1] = rr.y;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 128; ++j) s[j] = cap2 * tanh_fast(s[j] * scale_over_cap);
+                        }
+                    }
+                    if (partial) {
+                        const uint32_t vw[4] = {vis.x, vis.y, vis.z, vis.w};
+#pragma unroll
+                        for (int j = 0; j < 128; ++j)
+                            if (!((vw[j >> 5] >> (j & 31)) & 1u)) s[j] = -INFINITY;
+                    }
+                    float mx[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        mx[k] = max3(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+                        for (int j = 24; j < 128; j += 16) mx[k] = max3(mx[k], s[k + j], s[k + j + 8]);
+                    }
+                    const float tmax = a_mul * max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]),
+                                                    fmaxf(mx[6], mx[7]));
+                    const float m_new = fmaxf(m_ref, tmax);
+                    const bool need = (m_ref != -INFINITY) && (m_new > m_ref + 8.f);
+                    if (m_ref == -INFINITY) m_ref = m_new;
+                    if (__any_sync(0xffffffffu, need)) {
+                        // rescale O: PV(g-1) of this head completed before S(g) did
+                        const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
+                        if (need) {
+                            l *= f;
+                            m_ref = m_new;
+                        }
+#pragma unroll 1
+                        for (int c = 0; c < kD2 / 32; ++c) {
+                            float o[32];
+                            tmem_ld32(lane_base + C::kColO + hx * 128 + c * 32, o);
+                            tmem_ld_wait();
+                            uint32_t w32[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) w32[j] = __float_as_uint(o[j] * f);
+                            tmem_st32(lane_base + C::kColO + hx * 128 + c * 32, w32);
+                        }
+                        tmem_st_wait();
+                    }
+                    const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                    const float2 am2 = make_float2(a_mul, a_mul);
+                    const float2 nm2 = make_float2(-m_use, -m_use);
+                    float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                    make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int j = 0; j < 64; j += 2) {
+                            const int jj = hh * 64 + j;
+                            const float2 x2 = ffma2(make_float2(s[jj], s[jj + 1]), am2, nm2);
+                            const float2 e2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
+                            ls[(j >> 1) & 3] = fadd2(ls[(j >> 1) & 3], e2);
+                            pk[j >> 1] = pack_bf16x2(e2.x, e2.y);
+                        }
+                        // P elements 64hh..64hh+63 -> columns [32hh, 32hh+32), already read
+                        tmem_st32(lane_base + s_col + hh * 32, pk);
+                    }
+                    const float2 l01 = fadd2(ls[0], ls[1]), l23 = fadd2(ls[2], ls[3]);
+                    const float2 l03 = fadd2(l01, l23);
+                    l += l03.x + l03.y;
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bars.p_full + hx);
+                    ++g;
+                }
+                if (!ok) break;
+                // ---- shard end: post the row sum and max for the correction warps
+                const int slot = nshard & 1;
+                ++nshard;
+                stat_l[(hx * 2 + slot) * 128 + row] = l;
+                stat_m[(hx * 2 + slot) * 128 + row] = m_ref;
+                mbar_arrive(bars.stat_full + 2 * hx + slot);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp2) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+} // namespace
+
+size_t fwd2_ws_bytes() { return (size_t)kFwd2Slots * 4 * kTile * kD2 * 4; }
+
+bool fwd2_supported(const Problem &p) { return p.D == kD2 && (p.G % 2) == 0 && (p.Hq % 2) == 0; }
+
+cudaError_t fwd2_set_attributes()
+{
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fwd2_tc_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kLaunchRegs2) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(fwd2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Fwd2Cfg::kSmem);
+}
+
+cudaError_t launch_fwd2_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,
+                           void *out, float *lse, float *ws, int num_sms, cudaStream_t s)
+{
+    const int U = p.B * p.nq * (p.Hq / 2);
+    int grid = U < num_sms ? U : num_sms;
+    if (grid > kFwd2Slots) grid = kFwd2Slots;
+    fwd2_tc_kernel<<<grid, kThreads2, Fwd2Cfg::kSmem, s>>>(
+        *static_cast<const CUtensorMap *>(tm_q), *static_cast<const CUtensorMap *>(tm_k),
+        *static_cast<const CUtensorMap *>(tm_v), p, static_cast<__nv_bfloat16 *>(out), lse, ws);
+    return cudaGetLastError();
+}
+
+} // namespace ra

@@ -47,7 +47,7 @@ struct DevCache {
     int num_sms = 0;
     int *status = nullptr;
     bool attr_fwd64 = false, attr_fwd128 = false, attr_bwd64 = false, attr_bwd128 = false,
-         attr_simt64 = false, attr_simt128 = false;
+         attr_simt64 = false, attr_simt128 = false, attr_fwd2 = false;
 };
 DevCache g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -367,8 +367,9 @@ RA_API int ra_build_block_mask(const ra_attn_params *p, void *buf, size_t buf_by
 
 RA_API size_t ra_attn_fwd_workspace_size(const ra_attn_params *p)
 {
-    (void)p;
-    return 0;
+    if (check_params(p) != RA_OK) return 0;
+    const Problem pr = make_problem(p, nullptr, nullptr);
+    return (p->dtype == RA_BF16 && fwd2_supported(pr)) ? fwd2_ws_bytes() : 0;
 }
 
 RA_API int ra_attn_fwd(const ra_attn_params *p, const void *q, const void *k, const void *v,
@@ -401,15 +402,28 @@ RA_API int ra_attn_fwd(const ra_attn_params *p, const void *q, const void *k, co
         count(1);
         return RA_OK;
     }
+    alignas(64) CUtensorMap tq, tk, tv;
+    if ((rc = encode_rows(&tq, q, p->B, p->Lq, p->Hq, p->D))) return rc;
+    if ((rc = encode_rows(&tk, k, p->B, p->Lkv, p->Hkv, p->D))) return rc;
+    if ((rc = encode_rows(&tv, v, p->B, p->Lkv, p->Hkv, p->D))) return rc;
+    // two query heads per CTA when the problem allows it and the caller gave
+    // the workspace for their running outputs; else one head per CTA
+    if (fwd2_supported(pr) && ws && ws_bytes >= fwd2_ws_bytes() &&
+        (reinterpret_cast<uintptr_t>(ws) & 255u) == 0) {
+        if (!dc->attr_fwd2) {
+            if ((e = fwd2_set_attributes()) != cudaSuccess) return cuda_fail(e, "forward attributes");
+            dc->attr_fwd2 = true;
+        }
+        e = launch_fwd2_tc(pr, &tq, &tk, &tv, out, lse, static_cast<float *>(ws), dc->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+        count(1);
+        return RA_OK;
+    }
     bool &done = p->D == 64 ? dc->attr_fwd64 : dc->attr_fwd128;
     if (!done) {
         if ((e = fwd_tc_set_attributes(p->D)) != cudaSuccess) return cuda_fail(e, "forward attributes");
         done = true;
     }
-    alignas(64) CUtensorMap tq, tk, tv;
-    if ((rc = encode_rows(&tq, q, p->B, p->Lq, p->Hq, p->D))) return rc;
-    if ((rc = encode_rows(&tk, k, p->B, p->Lkv, p->Hkv, p->D))) return rc;
-    if ((rc = encode_rows(&tv, v, p->B, p->Lkv, p->Hkv, p->D))) return rc;
     e = launch_fwd_tc(pr, &tq, &tk, &tv, out, lse, dc->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     count(1);

@@ -78,6 +78,14 @@ cudaError_t launch_fwd_simt_f32(const Problem &p, const float *q, const float *k
                                 float *out, float *lse, cudaStream_t s);
 cudaError_t launch_fwd_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,
                           void *out, float *lse, int num_sms, cudaStream_t s);
+// The two-heads-per-CTA forward (D = 128, an even number of query heads per
+// kv head): its workspace bytes, whether it serves a problem, attributes and
+// launch (ws: fwd2_ws_bytes() bytes, 256-byte aligned).
+size_t fwd2_ws_bytes();
+bool fwd2_supported(const Problem &p);
+cudaError_t fwd2_set_attributes();
+cudaError_t launch_fwd2_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,
+                           void *out, float *lse, float *ws, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, int dtype,
                            const float *lse, float *delta, float *nlse2, float *dsink_part,
                            float *dsinks, cudaStream_t s);

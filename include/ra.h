@@ -213,8 +213,12 @@ RA_API size_t ra_block_mask_bytes(const ra_attn_params *p);
 RA_API int ra_build_block_mask(const ra_attn_params *p, void *buf, size_t buf_bytes,
                                ra_block_mask *out, ra_stream_t stream);
 
-/* Workspace bytes of ra_attn_fwd (0: the forward keeps its running state on
- * chip). */
+/* Workspace bytes of ra_attn_fwd: 0 when the forward keeps its running state
+ * on chip; for bf16 inputs with D = 128 and an even number of query heads
+ * per kv head (GQA, MQA) the forward runs two query heads per CTA and keeps
+ * their running ring outputs in this fp32 workspace (one fixed-size slot per
+ * CTA, about 40 MiB whatever the problem size).  Passing a smaller workspace
+ * (or none) is allowed: the forward then runs one head per CTA. */
 RA_API size_t ra_attn_fwd_workspace_size(const ra_attn_params *p);
 
 /*
@@ -226,7 +230,9 @@ RA_API size_t ra_attn_fwd_workspace_size(const ra_attn_params *p);
  *   s = (d - t) mod N (d = the tile's own shard, t = 0..N-1), empty tiles are
  *   skipped, the sink enters at t = 0 only, and each shard's partial is merged
  *   into the running (out, lse) by the sigmoid/softplus update.
- * Errors: RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_WORKSPACE, RA_ERR_CUDA.
+ *   ws, ws_bytes: optional workspace (ra_attn_fwd_workspace_size, 256-byte
+ *   aligned), see above; results are the same either way up to rounding.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA.
  */
 RA_API int ra_attn_fwd(const ra_attn_params *p, const void *q, const void *k, const void *v,
                        const ra_block_mask *mask, void *out, float *lse, void *ws,

@@ -97,10 +97,10 @@ class Case:
     def mask(self):
         return ra.build_mask(self.params)
 
-    def gpu_fwd(self):
+    def gpu_fwd(self, workspace=True):
         m = self.mask()
         d = self.dev
-        return ra.forward(self.params, d["q"], d["k"], d["v"], m) + (m,)
+        return ra.forward(self.params, d["q"], d["k"], d["v"], m, workspace=workspace) + (m,)
 
     def oracle_fwd(self, ring=True):
         h = self.host
@@ -135,10 +135,13 @@ FWD_CASES = {
 }
 
 
+# workspace: with it, D = 128 problems whose kv heads serve an even number of
+# query heads run the two-heads-per-CTA forward; without it, one head per CTA
+@pytest.mark.parametrize("workspace", [True, False], ids=["ws", "no_ws"])
 @pytest.mark.parametrize("name", list(FWD_CASES))
-def test_forward_matches_oracle(name):
+def test_forward_matches_oracle(name, workspace):
     c = Case(FWD_CASES[name])
-    out, lse, _ = c.gpu_fwd()
+    out, lse, _ = c.gpu_fwd(workspace)
     torch.cuda.synchronize()
     o_ref, l_ref = c.oracle_fwd()
     check_fwd(out, lse, o_ref, l_ref)
@@ -156,11 +159,12 @@ STRUCT_CASES = {
 }
 
 
+@pytest.mark.parametrize("workspace", [True, False], ids=["ws", "no_ws"])
 @pytest.mark.parametrize("name", list(STRUCT_CASES))
-def test_forward_structured_matches_oracle(name):
+def test_forward_structured_matches_oracle(name, workspace):
     w, st = STRUCT_CASES[name]
     c = Case(w, structure=st, seed_struct=7)
-    out, lse, _ = c.gpu_fwd()
+    out, lse, _ = c.gpu_fwd(workspace)
     torch.cuda.synchronize()
     o_ref, l_ref = c.oracle_fwd()
     check_fwd(out, lse, o_ref, l_ref)
