@@ -230,22 +230,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 return true;
             };
             // S^T = K Q^T into columns [0,128)
+            // descriptors are built once per operand; an offset o adds o / 16
+            const uint64_t kd = sdesc_sw128(k_base, 16, 1024), vd = sdesc_sw128(v_base, 16, 1024);
             auto issue_s = [&](uint32_t q_base) {
+                const uint64_t qd = sdesc_sw128(q_base, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem, sdesc_sw128(k_base + off, 16, 1024),
-                           sdesc_sw128(q_base + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                    const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem, kd + o, qd + o, kIdescT, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bars.s_full);
             };
             // dP^T = V dO^T into columns [128,256)
             auto issue_dp = [&](uint32_t do_base) {
+                const uint64_t dd = sdesc_sw128(do_base, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
-                           sdesc_sw128(do_base + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                    const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + C::kColDP, vd + o, dd + o, kIdescT, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bars.dp_full);
             };
@@ -272,10 +274,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // dV += P^T dO   (A = P^T from TMEM, B = dO as a K=q x N=D MN-major tile)
                     if (!(ok = mbar_wait(bars.p_ready, n & 1, ctx))) break;
                     tc_fence_after();
+                    const uint64_t dmn = sdesc_sw128(do_base, 16384, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         mma_ts(tmem + C::kColDV, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
-                               sdesc_sw128(do_base + kk * 2048, 16384, 1024), C::kIdescAcc,
+                               dmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                (i > 0 || kk > 0) ? 1u : 0u);
                     if (i + 1 < steps) {
                         if (!(ok = wait_stage(n + 1))) break;
@@ -284,10 +287,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // dK += dS^T Q
                     if (!(ok = mbar_wait(bars.ds_ready, n & 1, ctx))) break;
                     tc_fence_after();
+                    const uint64_t qmn = sdesc_sw128(q_base, 16384, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
-                               sdesc_sw128(q_base + kk * 2048, 16384, 1024), C::kIdescAcc,
+                               qmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                (i > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bars.st_empty + n % C::kStages);
                 }
@@ -762,24 +766,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 return true;
             };
             // S = Q K^T of tile t into columns [0,128)
+            // descriptors are built once per operand; an offset o adds o / 16
+            const uint64_t qd = sdesc_sw128(q_base, 16, 1024), dod = sdesc_sw128(do_base, 16, 1024);
             auto issue_s = [&](uint32_t t) {
-                const uint32_t kb = k_base + (t % C::kKStages) * C::kTileBytes;
+                const uint64_t kd = sdesc_sw128(k_base + (t % C::kKStages) * C::kTileBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem, sdesc_sw128(q_base + off, 16, 1024),
-                           sdesc_sw128(kb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                    const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem, qd + o, kd + o, kIdescT, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bars.s_full);
             };
             // dP = dO V^T of tile t into its dP buffer; V's stage is free after it
             auto issue_dp = [&](uint32_t t) {
-                const uint32_t vb = v_base + (t % C::kVStages) * C::kTileBytes;
+                const uint64_t vd = sdesc_sw128(v_base + (t % C::kVStages) * C::kTileBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem + C::dp_col(t), sdesc_sw128(do_base + off, 16, 1024),
-                           sdesc_sw128(vb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+                    const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + C::dp_col(t), dod + o, vd + o, kIdescT, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bars.dp_full + (t & 1));
                 tc_commit(bars.v_empty + t % C::kVStages);
@@ -815,11 +819,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (!(ok = mbar_wait(bars.ds_ready + (g & 1), (g >> 1) & 1, ctx))) break;
                     tc_fence_after();
                     const int sk = g % C::kKStages;
-                    const uint32_t kb = k_base + sk * C::kTileBytes;
+                    const uint64_t kmn = sdesc_sw128(k_base + sk * C::kTileBytes, 16384, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         mma_ts(tmem + C::kColDQ, tmem + C::dp_col(g) + kk * 8 + (kk >= 4 ? 32 : 0),
-                               sdesc_sw128(kb + kk * 2048, 16384, 1024), C::kIdescAcc,
+                               kmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                (e > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bars.k_empty + sk);
                 }

@@ -142,13 +142,13 @@ constexpr int kCorrThreads = 128;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr int kFwdThreads = 512;
-// setmaxnreg split: 256 x 192 + 128 x 80 + 128 x 48 = 65536 = 512 x 128, the
+// setmaxnreg split: 256 x 184 + 128 x 64 + 128 x 80 = 65536 = 512 x 128, the
 // block's registers at launch (the kernel is built for 128 per thread; the
 // launcher checks that count before the first launch)
 constexpr int kLaunchRegs = 128;
-constexpr uint32_t kSoftmaxRegs = 192;
-constexpr uint32_t kCorrRegs = 80;
-constexpr uint32_t kSideRegs = 48;
+constexpr uint32_t kSoftmaxRegs = 184;
+constexpr uint32_t kCorrRegs = 64;
+constexpr uint32_t kSideRegs = 80;
 static_assert(256 * kSoftmaxRegs + 128 * kCorrRegs + 128 * kSideRegs <= kFwdThreads * kLaunchRegs,
               "register split exceeds the block's launch registers");
 
@@ -376,9 +376,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------------ MMA issuer
             if (lane == 0) {
-                const uint32_t q_base = smem_u32(smem + C::kQOff);
-                const uint32_t k_base = smem_u32(smem + C::kKOff);
-                const uint32_t v_base = smem_u32(smem + C::kVOff);
+                // descriptors are built once per operand; an offset o adds o / 16
+                const uint64_t qd = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
+                const uint64_t kd0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+                const uint64_t vd0 = sdesc_sw128(smem_u32(smem + C::kVOff), 16384, 1024);
+                constexpr uint32_t kStageStep = C::kTileBytes >> 4;
                 uint32_t g = 0, uq = 0, n_oe = 0;
                 bool have_prev = false, prev_first = false, prev_last = false;
                 uint32_t prev_g = 0;
@@ -393,10 +395,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     // warps must have read the previous shard's
                     if (first && !mbar_wait(bars.o_empty, (n_oe++ & 1) ^ 1, ctx)) return false;
                     tc_fence_after();
-                    const uint32_t vb = v_base + st * C::kTileBytes;
+                    const uint64_t vd = vd0 + (uint64_t)(st * kStageStep);
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, 16384, 1024);
+                        const uint64_t bdesc = vd + (uint32_t)((kk * 2048) >> 4);
                         // P of kv rows 16kk..16kk+15: the half of warps 0-3 (kk < 4) sits
                         // in columns [0,32) of the S buffer, the other half in [64,96)
                         const uint32_t acol = sb * 128 + kk * 8 + (kk >= 4 ? 32 : 0);
@@ -425,12 +427,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             if (!(ok = mbar_wait(bars.k_full + st, (g / C::kKStages) & 1, ctx))) break;
                             tc_fence_after();
                             const int sb = g & 1;
-                            const uint32_t kb = k_base + st * C::kTileBytes;
+                            const uint64_t kd = kd0 + (uint64_t)(st * kStageStep);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                mma_ss(tmem + sb * 128, sdesc_sw128(q_base + off, 16, 1024),
-                                       sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+                                const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                                mma_ss(tmem + sb * 128, qd + o, kd + o, C::kIdescQK, kk > 0 ? 1u : 0u);
                             }
                             tc_commit(bars.k_empty + st);
                             tc_commit(bars.s_full + sb);
