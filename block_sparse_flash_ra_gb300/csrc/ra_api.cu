@@ -179,11 +179,22 @@ int dkdv_head_split(const ra_attn_params *p)
 
 // Backward workspace: Delta and -lse*log2 e per row, dsinks partials per
 // (b, head, q tile), and with a head split the fp32 dK / dV partials.
+// bf16 copies of q, k, v and dout that the fp32 backward's tensor-core
+// kernels read (fp32 inputs are rounded to bf16 once, in a prologue).
+size_t bwd_f32_copy_bytes(const ra_attn_params *p)
+{
+    const size_t nq = (size_t)p->B * p->Lq * p->Hq * p->D, nk = (size_t)p->B * p->Lkv * p->Hkv * p->D;
+    return 2 * up256(nq * 2) + 2 * up256(nk * 2);
+}
+
 size_t bwd_ws_bytes(const ra_attn_params *p, bool allow_split)
 {
     const size_t rows = (size_t)p->B * p->Hq * p->Lq;
     const size_t part = (size_t)p->Hq * p->B * (p->Lq / RA_TILE);
     size_t n = 2 * up256(rows * 4) + up256(part * 4);
+    // fp32 inputs: the gradients accumulate straight into the fp32 outputs,
+    // so the query heads are never split; the bf16 copies come first
+    if (p->dtype == RA_FP32) return bwd_f32_copy_bytes(p) + n;
     const int hs = allow_split ? dkdv_head_split(p) : 1;
     if (hs > 1) n += up256(2 * (size_t)hs * p->B * p->Lkv * p->Hkv * p->D * 4);
     return n;
@@ -542,7 +553,7 @@ struct BwdWs {
 // Checks of the backward entry points that do not involve the workspace:
 // params, tensor pointers, the mask, D and dtype.
 int bwd_validate(const ra_attn_params *p, const void *const *ptrs, int nptrs,
-                 const ra_block_mask *mask)
+                 const ra_block_mask *mask, bool allow_fp32 = false)
 {
     int rc = check_params(p);
     if (rc) return rc;
@@ -552,8 +563,9 @@ int bwd_validate(const ra_attn_params *p, const void *const *ptrs, int nptrs,
     }
     if (mask && (rc = check_mask(p, mask))) return rc;
     if (p->D != 64 && p->D != 128) return fail(RA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", p->D);
-    if (p->dtype != RA_BF16)
-        return fail(RA_ERR_UNSUPPORTED, "the backward is implemented for bf16 inputs");
+    if (p->dtype != RA_BF16 && !allow_fp32)
+        return fail(RA_ERR_UNSUPPORTED, "this backward stage is implemented for bf16 inputs "
+                                        "(ra_attn_bwd takes fp32 too)");
     return RA_OK;
 }
 
@@ -565,7 +577,7 @@ int bwd_all_validate(const ra_attn_params *p, const void *q, const void *k, cons
     if (!mask) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
     if (p && p->sinks && !dsinks) return fail(RA_ERR_INVALID_ARG, "dsinks is NULL but sinks are given");
     const void *ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
-    return bwd_validate(p, ptrs, 9, mask);
+    return bwd_validate(p, ptrs, 9, mask, true);
 }
 
 namespace {
@@ -574,9 +586,9 @@ namespace {
 // cache and the workspace split.
 int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
                const ra_block_mask *mask, void *ws, size_t ws_bytes, DevCache **dc, BwdWs *w,
-               bool allow_split = true)
+               bool allow_split = true, bool allow_fp32 = false)
 {
-    int rc = bwd_validate(p, ptrs, nptrs, mask);
+    int rc = bwd_validate(p, ptrs, nptrs, mask, allow_fp32);
     if (rc) return rc;
     const size_t need = bwd_ws_bytes(p, allow_split);
     if (!ws || ws_bytes < need)
@@ -585,11 +597,11 @@ int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
         return fail(RA_ERR_WORKSPACE, "backward workspace must be 256-byte aligned");
     if ((rc = device_cache(dc))) return rc;
     const size_t rows_bytes = up256((size_t)p->B * p->Hq * p->Lq * 4);
-    uint8_t *b = static_cast<uint8_t *>(ws);
+    uint8_t *b = static_cast<uint8_t *>(ws) + (p->dtype == RA_FP32 ? bwd_f32_copy_bytes(p) : 0);
     w->delta = reinterpret_cast<float *>(b);
     w->nlse2 = reinterpret_cast<float *>(b + rows_bytes);
     w->part = reinterpret_cast<float *>(b + 2 * rows_bytes);
-    w->hsplit = allow_split ? dkdv_head_split(p) : 1;
+    w->hsplit = (allow_split && p->dtype != RA_FP32) ? dkdv_head_split(p) : 1;
     const size_t part_bytes = up256((size_t)p->Hq * p->B * (p->Lq / RA_TILE) * 4);
     w->dkv_part = w->hsplit > 1 ? reinterpret_cast<float *>(b + 2 * rows_bytes + part_bytes) : nullptr;
     return RA_OK;
@@ -726,14 +738,37 @@ int bwd_all(const ra_attn_params *p, const void *q, const void *k, const void *v
     const void *ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
     DevCache *dc = nullptr;
     BwdWs w{};
-    rc = bwd_common(p, ptrs, 9, mask, ws, ws_bytes, &dc, &w, allow_split);
+    rc = bwd_common(p, ptrs, 9, mask, ws, ws_bytes, &dc, &w, allow_split, true);
     if (rc) return rc;
-    const Problem pr = make_problem(p, mask, dc->status);
+    Problem pr = make_problem(p, mask, dc->status);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_bwd_pre(pr, out, dout, p->dtype, lse, w.delta, w.nlse2, w.part, dsinks, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward preprocessing launch");
     count(p->sinks ? 2 : 1);
-    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, dout, w, dq, dk, dv, s);
+    if (p->dtype == RA_BF16)
+        return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, dout, w, dq, dk, dv, s);
+    // fp32 inputs: Delta and dsinks above come from the fp32 out / dout; the
+    // tensor-core kernels read bf16 copies of q, k, v, dout made here and add
+    // their fp32 gradients into dq, dk, dv, zeroed first
+    const size_t nq = (size_t)p->B * p->Lq * p->Hq * p->D, nk = (size_t)p->B * p->Lkv * p->Hkv * p->D;
+    uint8_t *cb = static_cast<uint8_t *>(ws);
+    void *q16 = cb, *do16 = cb + up256(nq * 2), *k16 = cb + 2 * up256(nq * 2),
+         *v16 = cb + 2 * up256(nq * 2) + up256(nk * 2);
+    const struct { const void *src; void *dst; size_t n; } casts[4] = {
+        {q, q16, nq}, {dout, do16, nq}, {k, k16, nk}, {v, v16, nk}};
+    for (const auto &c : casts) {
+        if ((e = launch_cast_from_f32(static_cast<const float *>(c.src), c.dst, c.n, RA_BF16, s)) !=
+            cudaSuccess)
+            return cuda_fail(e, "fp32 -> bf16 cast launch");
+        count(1);
+    }
+    const struct { void *dst; size_t n; } zero[3] = {{dq, nq}, {dk, nk}, {dv, nk}};
+    for (const auto &z : zero)
+        if ((e = cudaMemsetAsync(z.dst, 0, z.n * 4, s)) != cudaSuccess) return cuda_fail(e, "gradient zeroing");
+    pr.acc_dq = static_cast<float *>(dq);
+    pr.acc_dk = static_cast<float *>(dk);
+    pr.acc_dv = static_cast<float *>(dv);
+    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q16, k16, v16, do16, w, dq, dk, dv, s);
 }
 
 size_t bwd_ws_min_bytes(const ra_attn_params *p) { return bwd_ws_bytes(p, false); }

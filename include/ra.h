@@ -260,13 +260,18 @@ RA_API int ra_merge_out_lse(float *out, float *lse, const float *block_out,
  * * Hkv * D floats, hs = the number of chunks, a power of two dividing
  * Hq/Hkv): the dK/dV stage then splits each kv head's query heads over hs
  * work units, so that the units spread evenly over the SMs, and sums the
- * partials afterwards. */
+ * partials afterwards.  For fp32 inputs: no split, and bf16 copies of q, k,
+ * v and dout (2 bytes per element) in front. */
 RA_API size_t ra_attn_bwd_workspace_size(const ra_attn_params *p);
 
 /*
  * Backward (_ring_attention_backward): the exact gradient of ra_attn_fwd's
  * output, computed with the final out and lse.
- *   q, k, v, out, dout in p->dtype; lse from ra_attn_fwd;
+ *   q, k, v, out, dout in p->dtype (bf16, or fp32: Delta and dsinks are then
+ *   formed from the fp32 out and dout, the tensor-core products read bf16
+ *   copies of q, k, v and dout made in the workspace -- each input rounded to
+ *   bf16 once -- and the gradients accumulate in fp32 straight into dq, dk,
+ *   dv); lse from ra_attn_fwd;
  *   dq (B,Lq,Hq,D), dk, dv (B,Lkv,Hkv,D) in p->dtype, overwritten (dk, dv
  *   summed over the query heads that share a kv head);
  *   dsinks (Hq) fp32, overwritten, summed over batch and all rows; may be
@@ -288,7 +293,8 @@ RA_API int ra_attn_bwd(const ra_attn_params *p, const void *q, const void *k, co
  *                     and dsinks (if sinks);
  *   ra_attn_bwd_dkdv  dk, dv (one work unit per kv head and 128-row kv tile);
  *   ra_attn_bwd_dq    dq     (one work unit per query head and query tile).
- * dkdv and dq read lse and Delta only through ws.
+ * dkdv and dq read lse and Delta only through ws.  These stages take bf16
+ * inputs only (RA_ERR_UNSUPPORTED for fp32); ra_attn_bwd takes both.
  */
 RA_API int ra_attn_bwd_prep(const ra_attn_params *p, const void *out, const float *lse,
                             const void *dout, float *dsinks, void *ws, size_t ws_bytes,

@@ -393,6 +393,12 @@ BWD_CASES = {
     "cap20": W(Hq=4, Hkv=2, soft_cap=20.0, L=512, seed=39),
     "d64_cap20_sinks": W(D=64, Hq=4, Hkv=2, soft_cap=20.0, sinks=True, L=512, seed=40),
     "ragged_n5_b2": W(B=2, Hq=6, Hkv=2, L=640, n_shards=5, seed=38),
+    # fp32 inputs: the gradient kernels read bf16 copies (rounded once) and
+    # accumulate into fp32 dq, dk, dv; Delta and dsinks come from fp32 out, dO
+    "tiny_fp32": WORKLOADS["tiny"].scaled(backward=True),
+    "fp32_gqa_sinks_cap20_zigzag": W(dtype="fp32", Hq=4, Hkv=2, sinks=True, soft_cap=20.0, L=512,
+                                     zigzag=True, seed=42),
+    "fp32_mqa_d64": W(dtype="fp32", D=64, Hq=4, Hkv=1, is_mqa=True, L=512, n_shards=4, seed=43),
 }
 
 
