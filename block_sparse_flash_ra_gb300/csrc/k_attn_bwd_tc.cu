@@ -37,14 +37,26 @@ namespace {
 constexpr uint32_t kIdescT = idesc_bf16(128, 128, false, false); // S^T / dP^T / S / dP
 
 // Warps 0-7: the softmax-gradient work in two warpgroups, each over 64 of the
-// 128 tile columns; warp 8: TMA producer; warp 9: TMEM owner and MMA issuer.
+// 128 tile columns; warp 8: TMA producer; warp 9: TMEM owner and MMA issuer;
+// warps 10-11: no role (with warps 8-9 they form the warpgroup that gives
+// registers to the softmax warpgroups through setmaxnreg).
 // The bf16 operand (P^T, dS^T or dS) each group writes back to TMEM lands on
 // columns [0,32) (group 0) or [64,96) (group 1) of the fp32 tile it read,
 // so the 16-row K chunks kk of the next MMA sit at column 8*kk + 32*(kk>=4).
 constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 384;
+// setmaxnreg split: 256 x 176 + 128 x 152 = 64512 = 384 x 168, the block's
+// registers at launch (the kernels are built for 168 per thread, the most a
+// 384-thread block can have: three warps share each sub-partition's 16K;
+// the launcher checks the count before the first launch).  The issuing warps
+// then have room to spare: spills there slow every product the CTA issues.
+constexpr int kBwdLaunchRegs = 168;
+constexpr uint32_t kBwdSoftmaxRegs = 176;
+constexpr uint32_t kBwdSideRegs = 152;
+static_assert(256 * kBwdSoftmaxRegs + 128 * kBwdSideRegs <= kBwdThreads * kBwdLaunchRegs,
+              "register split exceeds the block's launch registers");
 
 // ====================================================================== dkdv
 template <int D>
@@ -166,143 +178,147 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == kProducerWarp) {
-        // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            uint32_t n = 0, uk = 0;
-            uint32_t st_issued[C::kStages] = {};
-            bool ok = true;
-            for (int r = 0; ok && r * Gd < U; ++r) {
-                const int u = unit_index(r, blockIdx.x, Gd);
-                if (u >= U) continue;
-                const ColUnit x = col_unit(p, u);
-                if (x.cnt == 0) continue;
-                if (!(ok = mbar_wait(bars.kv_empty, (uk & 1) ^ 1, ctx))) break;
-                mbar_expect_tx(bars.kv_full, 2 * C::kTileBytes);
-                for (int hb = 0; hb < D / 64; ++hb) {
-                    tma_load_4d(smem + C::kKOff + hb * 16384, &tm_k, bars.kv_full, hb * 64, x.hkv,
-                                x.kt * kTile, x.b);
-                    tma_load_4d(smem + C::kVOff + hb * 16384, &tm_v, bars.kv_full, hb * 64, x.hkv,
-                                x.kt * kTile, x.b);
-                }
-                ++uk;
-                for (int gi = 0; ok && gi < x.gc; ++gi) {
-                    const int h = x.h0 + gi;
-                    for (int e = 0; e < x.cnt; ++e) {
-                        const int qt = x.list[e];
-                        const int st = n % C::kStages;
-                        if (!(ok = mbar_wait(bars.st_empty + st, ((n / C::kStages) & 1) ^ 1, ctx))) break;
-                        uint8_t *sb = smem + C::kStageOff + st * C::kStageBytes;
-                        mbar_expect_tx(bars.st_full + st, 2 * C::kTileBytes + 1024);
-                        for (int hb = 0; hb < D / 64; ++hb) {
-                            tma_load_4d(sb + hb * 16384, &tm_q, bars.st_full + st, hb * 64, h,
-                                        qt * kTile, x.b);
-                            tma_load_4d(sb + C::kTileBytes + hb * 16384, &tm_do, bars.st_full + st,
-                                        hb * 64, h, qt * kTile, x.b);
+    if (warp >= kProducerWarp) {
+        regs_shrink<kBwdSideRegs>();
+        if (warp == kProducerWarp) {
+            // ---------------------------------------------------------- producer
+            if (lane == 0) {
+                uint32_t n = 0, uk = 0;
+                uint32_t st_issued[C::kStages] = {};
+                bool ok = true;
+                for (int r = 0; ok && r * Gd < U; ++r) {
+                    const int u = unit_index(r, blockIdx.x, Gd);
+                    if (u >= U) continue;
+                    const ColUnit x = col_unit(p, u);
+                    if (x.cnt == 0) continue;
+                    if (!(ok = mbar_wait(bars.kv_empty, (uk & 1) ^ 1, ctx))) break;
+                    mbar_expect_tx(bars.kv_full, 2 * C::kTileBytes);
+                    for (int hb = 0; hb < D / 64; ++hb) {
+                        tma_load_4d(smem + C::kKOff + hb * 16384, &tm_k, bars.kv_full, hb * 64, x.hkv,
+                                    x.kt * kTile, x.b);
+                        tma_load_4d(smem + C::kVOff + hb * 16384, &tm_v, bars.kv_full, hb * 64, x.hkv,
+                                    x.kt * kTile, x.b);
+                    }
+                    ++uk;
+                    for (int gi = 0; ok && gi < x.gc; ++gi) {
+                        const int h = x.h0 + gi;
+                        for (int e = 0; e < x.cnt; ++e) {
+                            const int qt = x.list[e];
+                            const int st = n % C::kStages;
+                            if (!(ok = mbar_wait(bars.st_empty + st, ((n / C::kStages) & 1) ^ 1, ctx))) break;
+                            uint8_t *sb = smem + C::kStageOff + st * C::kStageBytes;
+                            mbar_expect_tx(bars.st_full + st, 2 * C::kTileBytes + 1024);
+                            for (int hb = 0; hb < D / 64; ++hb) {
+                                tma_load_4d(sb + hb * 16384, &tm_q, bars.st_full + st, hb * 64, h,
+                                            qt * kTile, x.b);
+                                tma_load_4d(sb + C::kTileBytes + hb * 16384, &tm_do, bars.st_full + st,
+                                            hb * 64, h, qt * kTile, x.b);
+                            }
+                            const size_t li = ((size_t)x.b * p.Hq + h) * p.Lq + (size_t)qt * kTile;
+                            bulk_load(sb + 2 * C::kTileBytes, nlse2 + li, 512, bars.st_full + st);
+                            bulk_load(sb + 2 * C::kTileBytes + 512, delta + li, 512, bars.st_full + st);
+                            ++st_issued[st];
+                            ++n;
                         }
-                        const size_t li = ((size_t)x.b * p.Hq + h) * p.Lq + (size_t)qt * kTile;
-                        bulk_load(sb + 2 * C::kTileBytes, nlse2 + li, 512, bars.st_full + st);
-                        bulk_load(sb + 2 * C::kTileBytes + 512, delta + li, 512, bars.st_full + st);
-                        ++st_issued[st];
-                        ++n;
                     }
                 }
-            }
-            if (!ok) {
-                for (int s = 0; s < C::kStages; ++s)
-                    if (st_issued[s]) wait_drain(bars.st_full + s, (st_issued[s] - 1) & 1, kDrainNs);
-                if (uk) wait_drain(bars.kv_full, (uk - 1) & 1, kDrainNs);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t k_base = smem_u32(smem + C::kKOff);
-            const uint32_t v_base = smem_u32(smem + C::kVOff);
-            uint32_t n = 0, uk = 0;
-            bool ok = true;
-            auto stage_base = [&](uint32_t step) {
-                return smem_u32(smem + C::kStageOff + (step % C::kStages) * C::kStageBytes);
-            };
-            auto wait_stage = [&](uint32_t step) -> bool {
-                if (!mbar_wait(bars.st_full + step % C::kStages, (step / C::kStages) & 1, ctx)) return false;
-                tc_fence_after();
-                return true;
-            };
-            // S^T = K Q^T into columns [0,128)
-            // descriptors are built once per operand; an offset o adds o / 16
-            const uint64_t kd = sdesc_sw128(k_base, 16, 1024), vd = sdesc_sw128(v_base, 16, 1024);
-            auto issue_s = [&](uint32_t q_base) {
-                const uint64_t qd = sdesc_sw128(q_base, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem, kd + o, qd + o, kIdescT, kk > 0 ? 1u : 0u);
+                if (!ok) {
+                    for (int s = 0; s < C::kStages; ++s)
+                        if (st_issued[s]) wait_drain(bars.st_full + s, (st_issued[s] - 1) & 1, kDrainNs);
+                    if (uk) wait_drain(bars.kv_full, (uk - 1) & 1, kDrainNs);
                 }
-                tc_commit(bars.s_full);
-            };
-            // dP^T = V dO^T into columns [128,256)
-            auto issue_dp = [&](uint32_t do_base) {
-                const uint64_t dd = sdesc_sw128(do_base, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + C::kColDP, vd + o, dd + o, kIdescT, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bars.dp_full);
-            };
-            // Issue order per step n (each product overlaps a softmax phase):
-            //   dP(n) | phase A(n);  dV(n), S(n+1) | phase B(n);
-            //   dK(n), dP(n+1) | phase A(n+1).
-            // S(n+1) may overwrite P^T(n) once dV(n) is issued (MMAs run in
-            // order); dP(n+1) may overwrite dS^T(n) once dK(n) is issued.
-            for (int r = 0; ok && r * Gd < U; ++r) {
-                const int u = unit_index(r, blockIdx.x, Gd);
-                if (u >= U) continue;
-                const ColUnit x = col_unit(p, u);
-                if (x.cnt == 0) continue;
-                if (!(ok = mbar_wait(bars.kv_full, uk & 1, ctx))) break;
-                tc_fence_after();
-                ++uk;
-                const int steps = x.gc * x.cnt;
-                if (!(ok = wait_stage(n))) break;
-                issue_s(stage_base(n));
-                for (int i = 0; i < steps; ++i, ++n) {
-                    const uint32_t q_base = stage_base(n);
-                    const uint32_t do_base = q_base + C::kTileBytes;
-                    issue_dp(do_base);
-                    // dV += P^T dO   (A = P^T from TMEM, B = dO as a K=q x N=D MN-major tile)
-                    if (!(ok = mbar_wait(bars.p_ready, n & 1, ctx))) break;
+            }
+        } else if (warp == kMmaWarp) {
+            // ---------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                const uint32_t k_base = smem_u32(smem + C::kKOff);
+                const uint32_t v_base = smem_u32(smem + C::kVOff);
+                uint32_t n = 0, uk = 0;
+                bool ok = true;
+                auto stage_base = [&](uint32_t step) {
+                    return smem_u32(smem + C::kStageOff + (step % C::kStages) * C::kStageBytes);
+                };
+                auto wait_stage = [&](uint32_t step) -> bool {
+                    if (!mbar_wait(bars.st_full + step % C::kStages, (step / C::kStages) & 1, ctx)) return false;
                     tc_fence_after();
-                    const uint64_t dmn = sdesc_sw128(do_base, 16384, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + C::kColDV, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
-                               dmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
-                               (i > 0 || kk > 0) ? 1u : 0u);
-                    if (i + 1 < steps) {
-                        if (!(ok = wait_stage(n + 1))) break;
-                        issue_s(stage_base(n + 1));
+                    return true;
+                };
+                // S^T = K Q^T into columns [0,128)
+                // descriptors are built once per operand; an offset o adds o / 16
+                const uint64_t kd = sdesc_sw128(k_base, 16, 1024), vd = sdesc_sw128(v_base, 16, 1024);
+                auto issue_s = [&](uint32_t q_base) {
+                    const uint64_t qd = sdesc_sw128(q_base, 16, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        mma_ss(tmem, kd + o, qd + o, kIdescT, kk > 0 ? 1u : 0u);
                     }
-                    // dK += dS^T Q
-                    if (!(ok = mbar_wait(bars.ds_ready, n & 1, ctx))) break;
+                    tc_commit(bars.s_full);
+                };
+                // dP^T = V dO^T into columns [128,256)
+                auto issue_dp = [&](uint32_t do_base) {
+                    const uint64_t dd = sdesc_sw128(do_base, 16, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        mma_ss(tmem + C::kColDP, vd + o, dd + o, kIdescT, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bars.dp_full);
+                };
+                // Issue order per step n (each product overlaps a softmax phase):
+                //   dP(n) | phase A(n);  dV(n), S(n+1) | phase B(n);
+                //   dK(n), dP(n+1) | phase A(n+1).
+                // S(n+1) may overwrite P^T(n) once dV(n) is issued (MMAs run in
+                // order); dP(n+1) may overwrite dS^T(n) once dK(n) is issued.
+                for (int r = 0; ok && r * Gd < U; ++r) {
+                    const int u = unit_index(r, blockIdx.x, Gd);
+                    if (u >= U) continue;
+                    const ColUnit x = col_unit(p, u);
+                    if (x.cnt == 0) continue;
+                    if (!(ok = mbar_wait(bars.kv_full, uk & 1, ctx))) break;
                     tc_fence_after();
-                    const uint64_t qmn = sdesc_sw128(q_base, 16384, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
-                               qmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
-                               (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bars.st_empty + n % C::kStages);
+                    ++uk;
+                    const int steps = x.gc * x.cnt;
+                    if (!(ok = wait_stage(n))) break;
+                    issue_s(stage_base(n));
+                    for (int i = 0; i < steps; ++i, ++n) {
+                        const uint32_t q_base = stage_base(n);
+                        const uint32_t do_base = q_base + C::kTileBytes;
+                        issue_dp(do_base);
+                        // dV += P^T dO   (A = P^T from TMEM, B = dO as a K=q x N=D MN-major tile)
+                        if (!(ok = mbar_wait(bars.p_ready, n & 1, ctx))) break;
+                        tc_fence_after();
+                        const uint64_t dmn = sdesc_sw128(do_base, 16384, 1024);
+    #pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ts(tmem + C::kColDV, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
+                                   dmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                        if (i + 1 < steps) {
+                            if (!(ok = wait_stage(n + 1))) break;
+                            issue_s(stage_base(n + 1));
+                        }
+                        // dK += dS^T Q
+                        if (!(ok = mbar_wait(bars.ds_ready, n & 1, ctx))) break;
+                        tc_fence_after();
+                        const uint64_t qmn = sdesc_sw128(q_base, 16384, 1024);
+    #pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
+                                   qmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bars.st_empty + n % C::kStages);
+                    }
+                    if (!ok) break;
+                    tc_commit(bars.kv_empty);
+                    tc_commit(bars.acc_ready);
                 }
-                if (!ok) break;
-                tc_commit(bars.kv_empty);
-                tc_commit(bars.acc_ready);
+                tc_commit(bars.drain);
+                wait_drain(bars.drain, 0, kDrainNs);
             }
-            tc_commit(bars.drain);
-            wait_drain(bars.drain, 0, kDrainNs);
         }
     } else {
+        regs_grow<kBwdSoftmaxRegs>();
         // ---------------------------------------------------------- softmax-grad
         // Warps 0-7 in two warpgroups: group wg handles query columns
         // 64*wg..64*wg+63 (and D/2 columns of dK, dV) of kv row 32*(w%4)+lane.
@@ -702,138 +718,142 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == kProducerWarp) {
-        // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            uint32_t g = 0, uq = 0;
-            uint32_t k_issued[C::kKStages] = {}, v_issued[C::kVStages] = {};
-            bool ok = true;
-            for (int r = 0; ok && r * Gd < U; ++r) {
-                const int u = unit_index(r, blockIdx.x, Gd);
-                if (u >= U) continue;
-                const RowUnit x = row_unit(p, u);
-                if (x.cnt == 0) continue;
-                if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
-                mbar_expect_tx(bars.q_full, 2 * C::kTileBytes);
-                for (int hb = 0; hb < D / 64; ++hb) {
-                    tma_load_4d(smem + C::kQOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h,
-                                x.qt * kTile, x.b);
-                    tma_load_4d(smem + C::kDoOff + hb * 16384, &tm_do, bars.q_full, hb * 64, x.h,
-                                x.qt * kTile, x.b);
-                }
-                ++uq;
-                const int g_kv = x.h / p.G;
-                for (int e = 0; e < x.cnt; ++e) {
-                    const int kt = x.list[e];
-                    const int sk = g % C::kKStages;
-                    if (!(ok = mbar_wait(bars.k_empty + sk, ((g / C::kKStages) & 1) ^ 1, ctx))) break;
-                    mbar_expect_tx(bars.k_full + sk, C::kTileBytes);
-                    for (int hb = 0; hb < D / 64; ++hb)
-                        tma_load_4d(smem + C::kKOff + sk * C::kTileBytes + hb * 16384, &tm_k,
-                                    bars.k_full + sk, hb * 64, g_kv, kt * kTile, x.b);
-                    ++k_issued[sk];
-                    const int sv = g % C::kVStages;
-                    if (!(ok = mbar_wait(bars.v_empty + sv, ((g / C::kVStages) & 1) ^ 1, ctx))) break;
-                    mbar_expect_tx(bars.v_full + sv, C::kTileBytes);
-                    for (int hb = 0; hb < D / 64; ++hb)
-                        tma_load_4d(smem + C::kVOff + sv * C::kTileBytes + hb * 16384, &tm_v,
-                                    bars.v_full + sv, hb * 64, g_kv, kt * kTile, x.b);
-                    ++v_issued[sv];
-                    ++g;
-                }
-            }
-            if (!ok) {
-                for (int s = 0; s < C::kKStages; ++s)
-                    if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
-                for (int s = 0; s < C::kVStages; ++s)
-                    if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
-                if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t q_base = smem_u32(smem + C::kQOff);
-            const uint32_t do_base = smem_u32(smem + C::kDoOff);
-            const uint32_t k_base = smem_u32(smem + C::kKOff);
-            const uint32_t v_base = smem_u32(smem + C::kVOff);
-            uint32_t g = 0, uq = 0;
-            bool ok = true;
-            auto wait_kv = [&](uint32_t t) -> bool {
-                if (!mbar_wait(bars.k_full + t % C::kKStages, (t / C::kKStages) & 1, ctx)) return false;
-                if (!mbar_wait(bars.v_full + t % C::kVStages, (t / C::kVStages) & 1, ctx)) return false;
-                tc_fence_after();
-                return true;
-            };
-            // S = Q K^T of tile t into columns [0,128)
-            // descriptors are built once per operand; an offset o adds o / 16
-            const uint64_t qd = sdesc_sw128(q_base, 16, 1024), dod = sdesc_sw128(do_base, 16, 1024);
-            auto issue_s = [&](uint32_t t) {
-                const uint64_t kd = sdesc_sw128(k_base + (t % C::kKStages) * C::kTileBytes, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem, qd + o, kd + o, kIdescT, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bars.s_full);
-            };
-            // dP = dO V^T of tile t into its dP buffer; V's stage is free after it
-            auto issue_dp = [&](uint32_t t) {
-                const uint64_t vd = sdesc_sw128(v_base + (t % C::kVStages) * C::kTileBytes, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + C::dp_col(t), dod + o, vd + o, kIdescT, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bars.dp_full + (t & 1));
-                tc_commit(bars.v_empty + t % C::kVStages);
-            };
-            // Issue order: S(g) and dP(g) together, as soon as phase A(g-1) has
-            // read S(g-1) (S is single-buffered); dQ(g) once phase B(g) has
-            // written dS(g) over dP(g).  dP is double-buffered, so dP(g+1)
-            // never waits for dQ(g): the softmax phases of tile g+1 overlap
-            // the products dQ(g), S(g+2), dP(g+2).  dP(g+1) overwrites the
-            // buffer of dS(g-1), whose reader dQ(g-1) is already issued.
-            for (int r = 0; ok && r * Gd < U; ++r) {
-                const int u = unit_index(r, blockIdx.x, Gd);
-                if (u >= U) continue;
-                const RowUnit x = row_unit(p, u);
-                if (x.cnt == 0) continue;
-                if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
-                tc_fence_after();
-                ++uq;
-                if (!(ok = wait_kv(g))) break;
-                issue_s(g);
-                issue_dp(g);
-                if (x.cnt == 1) tc_commit(bars.q_empty);
-                for (int e = 0; e < x.cnt; ++e, ++g) {
-                    if (!(ok = mbar_wait(bars.s_free, g & 1, ctx))) break;
-                    if (e + 1 < x.cnt) {
-                        if (!(ok = wait_kv(g + 1))) break;
-                        issue_s(g + 1);
-                        issue_dp(g + 1);
-                        // Q and dO of the unit are read by nothing after this
-                        if (e + 2 == x.cnt) tc_commit(bars.q_empty);
+    if (warp >= kProducerWarp) {
+        regs_shrink<kBwdSideRegs>();
+        if (warp == kProducerWarp) {
+            // ---------------------------------------------------------- producer
+            if (lane == 0) {
+                uint32_t g = 0, uq = 0;
+                uint32_t k_issued[C::kKStages] = {}, v_issued[C::kVStages] = {};
+                bool ok = true;
+                for (int r = 0; ok && r * Gd < U; ++r) {
+                    const int u = unit_index(r, blockIdx.x, Gd);
+                    if (u >= U) continue;
+                    const RowUnit x = row_unit(p, u);
+                    if (x.cnt == 0) continue;
+                    if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
+                    mbar_expect_tx(bars.q_full, 2 * C::kTileBytes);
+                    for (int hb = 0; hb < D / 64; ++hb) {
+                        tma_load_4d(smem + C::kQOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h,
+                                    x.qt * kTile, x.b);
+                        tma_load_4d(smem + C::kDoOff + hb * 16384, &tm_do, bars.q_full, hb * 64, x.h,
+                                    x.qt * kTile, x.b);
                     }
-                    // dQ += dS K   (A = dS from TMEM, B = K as a K=kv x N=D MN-major tile)
-                    if (!(ok = mbar_wait(bars.ds_ready + (g & 1), (g >> 1) & 1, ctx))) break;
-                    tc_fence_after();
-                    const int sk = g % C::kKStages;
-                    const uint64_t kmn = sdesc_sw128(k_base + sk * C::kTileBytes, 16384, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + C::kColDQ, tmem + C::dp_col(g) + kk * 8 + (kk >= 4 ? 32 : 0),
-                               kmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
-                               (e > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bars.k_empty + sk);
+                    ++uq;
+                    const int g_kv = x.h / p.G;
+                    for (int e = 0; e < x.cnt; ++e) {
+                        const int kt = x.list[e];
+                        const int sk = g % C::kKStages;
+                        if (!(ok = mbar_wait(bars.k_empty + sk, ((g / C::kKStages) & 1) ^ 1, ctx))) break;
+                        mbar_expect_tx(bars.k_full + sk, C::kTileBytes);
+                        for (int hb = 0; hb < D / 64; ++hb)
+                            tma_load_4d(smem + C::kKOff + sk * C::kTileBytes + hb * 16384, &tm_k,
+                                        bars.k_full + sk, hb * 64, g_kv, kt * kTile, x.b);
+                        ++k_issued[sk];
+                        const int sv = g % C::kVStages;
+                        if (!(ok = mbar_wait(bars.v_empty + sv, ((g / C::kVStages) & 1) ^ 1, ctx))) break;
+                        mbar_expect_tx(bars.v_full + sv, C::kTileBytes);
+                        for (int hb = 0; hb < D / 64; ++hb)
+                            tma_load_4d(smem + C::kVOff + sv * C::kTileBytes + hb * 16384, &tm_v,
+                                        bars.v_full + sv, hb * 64, g_kv, kt * kTile, x.b);
+                        ++v_issued[sv];
+                        ++g;
+                    }
                 }
-                if (!ok) break;
-                tc_commit(bars.acc_ready);
+                if (!ok) {
+                    for (int s = 0; s < C::kKStages; ++s)
+                        if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
+                    for (int s = 0; s < C::kVStages; ++s)
+                        if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
+                    if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
+                }
             }
-            tc_commit(bars.drain);
-            wait_drain(bars.drain, 0, kDrainNs);
+        } else if (warp == kMmaWarp) {
+            // ---------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                const uint32_t q_base = smem_u32(smem + C::kQOff);
+                const uint32_t do_base = smem_u32(smem + C::kDoOff);
+                const uint32_t k_base = smem_u32(smem + C::kKOff);
+                const uint32_t v_base = smem_u32(smem + C::kVOff);
+                uint32_t g = 0, uq = 0;
+                bool ok = true;
+                auto wait_kv = [&](uint32_t t) -> bool {
+                    if (!mbar_wait(bars.k_full + t % C::kKStages, (t / C::kKStages) & 1, ctx)) return false;
+                    if (!mbar_wait(bars.v_full + t % C::kVStages, (t / C::kVStages) & 1, ctx)) return false;
+                    tc_fence_after();
+                    return true;
+                };
+                // S = Q K^T of tile t into columns [0,128)
+                // descriptors are built once per operand; an offset o adds o / 16
+                const uint64_t qd = sdesc_sw128(q_base, 16, 1024), dod = sdesc_sw128(do_base, 16, 1024);
+                auto issue_s = [&](uint32_t t) {
+                    const uint64_t kd = sdesc_sw128(k_base + (t % C::kKStages) * C::kTileBytes, 16, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        mma_ss(tmem, qd + o, kd + o, kIdescT, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bars.s_full);
+                };
+                // dP = dO V^T of tile t into its dP buffer; V's stage is free after it
+                auto issue_dp = [&](uint32_t t) {
+                    const uint64_t vd = sdesc_sw128(v_base + (t % C::kVStages) * C::kTileBytes, 16, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        mma_ss(tmem + C::dp_col(t), dod + o, vd + o, kIdescT, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bars.dp_full + (t & 1));
+                    tc_commit(bars.v_empty + t % C::kVStages);
+                };
+                // Issue order: S(g) and dP(g) together, as soon as phase A(g-1) has
+                // read S(g-1) (S is single-buffered); dQ(g) once phase B(g) has
+                // written dS(g) over dP(g).  dP is double-buffered, so dP(g+1)
+                // never waits for dQ(g): the softmax phases of tile g+1 overlap
+                // the products dQ(g), S(g+2), dP(g+2).  dP(g+1) overwrites the
+                // buffer of dS(g-1), whose reader dQ(g-1) is already issued.
+                for (int r = 0; ok && r * Gd < U; ++r) {
+                    const int u = unit_index(r, blockIdx.x, Gd);
+                    if (u >= U) continue;
+                    const RowUnit x = row_unit(p, u);
+                    if (x.cnt == 0) continue;
+                    if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                    tc_fence_after();
+                    ++uq;
+                    if (!(ok = wait_kv(g))) break;
+                    issue_s(g);
+                    issue_dp(g);
+                    if (x.cnt == 1) tc_commit(bars.q_empty);
+                    for (int e = 0; e < x.cnt; ++e, ++g) {
+                        if (!(ok = mbar_wait(bars.s_free, g & 1, ctx))) break;
+                        if (e + 1 < x.cnt) {
+                            if (!(ok = wait_kv(g + 1))) break;
+                            issue_s(g + 1);
+                            issue_dp(g + 1);
+                            // Q and dO of the unit are read by nothing after this
+                            if (e + 2 == x.cnt) tc_commit(bars.q_empty);
+                        }
+                        // dQ += dS K   (A = dS from TMEM, B = K as a K=kv x N=D MN-major tile)
+                        if (!(ok = mbar_wait(bars.ds_ready + (g & 1), (g >> 1) & 1, ctx))) break;
+                        tc_fence_after();
+                        const int sk = g % C::kKStages;
+                        const uint64_t kmn = sdesc_sw128(k_base + sk * C::kTileBytes, 16384, 1024);
+    #pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ts(tmem + C::kColDQ, tmem + C::dp_col(g) + kk * 8 + (kk >= 4 ? 32 : 0),
+                                   kmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
+                                   (e > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bars.k_empty + sk);
+                    }
+                    if (!ok) break;
+                    tc_commit(bars.acc_ready);
+                }
+                tc_commit(bars.drain);
+                wait_drain(bars.drain, 0, kDrainNs);
+            }
         }
     } else {
+        regs_grow<kBwdSoftmaxRegs>();
         // ---------------------------------------------------------- softmax-grad
         // Warps 0-7 in two warpgroups: group wg handles kv columns
         // 64*wg..64*wg+63 (and D/2 columns of dQ) of query row 32*(w%4)+lane.
@@ -1074,8 +1094,13 @@ cudaError_t bwd_set_attributes_d()
                           (const void *)bwd_dq_kernel<D, false>, (const void *)bwd_dq_kernel<D, true>};
     const int smem[4] = {DkdvCfg<D>::kSmem, DkdvCfg<D>::kSmem, DqCfg<D>::kSmem, DqCfg<D>::kSmem};
     for (int i = 0; i < 4; ++i) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
+        // the setmaxnreg split draws on the registers the block is launched
+        // with: refuse a build that gives each thread fewer than it assumes
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fns[i]);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs < kBwdLaunchRegs) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
