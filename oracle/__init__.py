@@ -85,6 +85,7 @@ def _load():
             lib.ora_merge.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci]
             lib.ora_merge.restype = None
             lib.ora_block_mask.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
+            lib.ora_block_mask_sized.argtypes = [P, ci, ci, vp, vp, vp, vp, vp, vp, vp]
             lib.ora_permute.argtypes = [vp, vp, ci, ci, sz, ci, ci]
             lib.ora_zigzag_source.argtypes = [ci, ci, ci]
             lib.ora_ring_source.argtypes = [ci, ci, ci]
@@ -217,13 +218,14 @@ def merge(out, lse, block_out, block_lse):
 
 
 def block_mask(B, Lq, Lkv, *, causal, q_pos=None, kv_pos=None, q_seg=None, kv_seg=None,
-               pad_segment_id=-1, local_mask=None):
-    """Tile classes (0 empty, 1 partial, 2 full) and tile lists, see ra_oracle.c."""
+               pad_segment_id=-1, local_mask=None, block_q=TILE, block_kv=TILE):
+    """Tile classes (0 empty, 1 partial, 2 full) and tile lists, see ra_oracle.c,
+    on a grid of block_q query rows x block_kv key rows (128 x 128 by default)."""
     q_pos, kv_pos, q_seg, kv_seg = map(_i32, (q_pos, kv_pos, q_seg, kv_seg))
     lm, lq_s, lk_s = _local(local_mask, Lq, Lkv)
     p = _Params(B, Lq, Lkv, 1, 1, 1, 1.0, 0.0, int(bool(causal)), int(pad_segment_id),
                 _ptr(q_pos), _ptr(kv_pos), _ptr(q_seg), _ptr(kv_seg), None, _ptr(lm), lq_s, lk_s)
-    nq, nk = Lq // TILE, Lkv // TILE
+    nq, nk = Lq // block_q, Lkv // block_kv
     cls = np.zeros((B, nq, nk), np.uint8)
     fcnt = np.zeros(B * nq, np.int32)
     fidx = np.zeros((B * nq, nk), np.int32)
@@ -231,8 +233,9 @@ def block_mask(B, Lq, Lkv, *, causal, q_pos=None, kv_pos=None, q_seg=None, kv_se
     bidx = np.zeros((B * nk, nq), np.int32)
     ford = np.zeros(B * nq, np.int32)
     bord = np.zeros(B * nk, np.int32)
-    rc = _load().ora_block_mask(ctypes.byref(p), _ptr(cls), _ptr(fcnt), _ptr(fidx), _ptr(bcnt),
-                                _ptr(bidx), _ptr(ford), _ptr(bord))
+    rc = _load().ora_block_mask_sized(ctypes.byref(p), int(block_q), int(block_kv), _ptr(cls),
+                                      _ptr(fcnt), _ptr(fidx), _ptr(bcnt), _ptr(bidx), _ptr(ford),
+                                      _ptr(bord))
     if rc:
         raise ValueError(f"ora_block_mask failed ({rc})")
     return dict(tile_class=cls, fwd_cnt=fcnt, fwd_idx=fidx, bwd_cnt=bcnt, bwd_idx=bidx,

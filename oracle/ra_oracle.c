@@ -556,21 +556,28 @@ static int ora_cmp_desc(const void *a, const void *b)
     return x->id < y->id ? -1 : (x->id > y->id ? 1 : 0);
 }
 
-int ora_block_mask(const ora_params *p, uint8_t *cls, int32_t *fwd_cnt, int32_t *fwd_idx,
-                   int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order, int32_t *bwd_order)
+/* The same classification on a grid of bq query rows x bk key rows (the
+ * backward's own block sizes, [RS] make_ring_attention with
+ * block_sizes.has_backward_blocks: the dkv MaskInfo built on the
+ * (block_q_dkv, block_kv_dkv) grid; [KVAX] create_attention_mask computing
+ * the backward mask).  nq = Lq / bq, nk = Lkv / bk; arrays as above with
+ * those nq, nk. */
+int ora_block_mask_sized(const ora_params *p, int bq, int bk, uint8_t *cls, int32_t *fwd_cnt,
+                         int32_t *fwd_idx, int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order,
+                         int32_t *bwd_order)
 {
-    if (p->Lq % ORA_TILE || p->Lkv % ORA_TILE || p->B <= 0) return -1;
-    const int nq = p->Lq / ORA_TILE, nk = p->Lkv / ORA_TILE;
+    if (bq <= 0 || bk <= 0 || p->Lq % bq || p->Lkv % bk || p->B <= 0) return -1;
+    const int nq = p->Lq / bq, nk = p->Lkv / bk;
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int b = 0; b < p->B; ++b)
         for (int qt = 0; qt < nq; ++qt)
             for (int kt = 0; kt < nk; ++kt) {
                 long cnt = 0;
-                for (int i = qt * ORA_TILE; i < (qt + 1) * ORA_TILE; ++i)
-                    for (int j = kt * ORA_TILE; j < (kt + 1) * ORA_TILE; ++j)
+                for (int i = qt * bq; i < (qt + 1) * bq; ++i)
+                    for (int j = kt * bk; j < (kt + 1) * bk; ++j)
                         cnt += ora_visible(p, b, i, j);
                 cls[((size_t)b * nq + qt) * nk + kt] =
-                    cnt == 0 ? 0 : (cnt == (long)ORA_TILE * ORA_TILE ? 2 : 1);
+                    cnt == 0 ? 0 : (cnt == (long)bq * bk ? 2 : 1);
             }
     for (int b = 0; b < p->B; ++b) {
         for (int qt = 0; qt < nq; ++qt) {
@@ -600,6 +607,13 @@ int ora_block_mask(const ora_params *p, uint8_t *cls, int32_t *fwd_cnt, int32_t 
     for (int r = 0; r < p->B * nk; ++r) bwd_order[r] = tmp[r].id;
     free(tmp);
     return 0;
+}
+
+int ora_block_mask(const ora_params *p, uint8_t *cls, int32_t *fwd_cnt, int32_t *fwd_idx,
+                   int32_t *bwd_cnt, int32_t *bwd_idx, int32_t *fwd_order, int32_t *bwd_order)
+{
+    return ora_block_mask_sized(p, ORA_TILE, ORA_TILE, cls, fwd_cnt, fwd_idx, bwd_cnt, bwd_idx,
+                                fwd_order, bwd_order);
 }
 
 /* ------------------------------------------------------------------ */

@@ -362,6 +362,40 @@ def test_block_mask_bruteforce(seed):
     assert np.array_equal(m["bwd_order"], bord)
 
 
+@pytest.mark.parametrize("bq,bk", [(64, 128), (128, 64), (64, 64), (32, 128)])
+def test_block_mask_other_block_sizes_bruteforce(bq, bk):
+    # the backward's own grid (the dkv MaskInfo of make_ring_attention on
+    # (block_q_dkv, block_kv_dkv)): classes from per-pair counts, lists, orders
+    g = torch.Generator().manual_seed(bq + bk)
+    B, L = 2, 512
+    seg, pos = random_structure(g, B, L, n_docs_max=5, pad_max=150)
+    kw = dict(causal=True, q_pos=pos.numpy(), kv_pos=pos.numpy(), q_seg=seg.numpy(),
+              kv_seg=seg.numpy())
+    m = oracle.block_mask(B, L, L, block_q=bq, block_kv=bk, **kw)
+    vis = brute.visibility(B, L, L, **kw)
+    nq, nk = L // bq, L // bk
+    cnt = vis.reshape(B, nq, bq, nk, bk).sum(axis=(2, 4))
+    cls = np.where(cnt == 0, 0, np.where(cnt == bq * bk, 2, 1)).astype(np.uint8)
+    assert np.array_equal(m["tile_class"], cls)
+    colcls = cls.transpose(0, 2, 1).reshape(B * nk, nq)
+    for c in range(B * nk):
+        nz = np.nonzero(colcls[c])[0]
+        assert m["bwd_cnt"][c] == len(nz)
+        assert np.array_equal(m["bwd_idx"][c][:len(nz)], nz)
+        assert np.all(m["bwd_idx"][c][len(nz):] == -1)
+    rowcls = cls.reshape(B * nq, nk)
+    for r in range(B * nq):
+        assert m["fwd_cnt"][r] == np.count_nonzero(rowcls[r])
+    assert np.array_equal(m["bwd_order"], np.lexsort((np.arange(B * nk), -m["bwd_cnt"])))
+    # halving the query blocks splits each 128-row class: a 128 x bk block is
+    # EMPTY iff both halves are, FULL iff both are
+    if (bq, bk) == (64, 128):
+        m128 = oracle.block_mask(B, L, L, **kw)["tile_class"]
+        halves = cls.reshape(B, nq // 2, 2, nk)
+        assert np.array_equal(m128 == 0, np.all(halves == 0, axis=2))
+        assert np.array_equal(m128 == 2, np.all(halves == 2, axis=2))
+
+
 # ------------------------------------------------------------ permutation
 @pytest.mark.parametrize("dtype", [np.uint8, np.int32, np.float32, np.float64])
 @pytest.mark.parametrize("n", [1, 2, 8])
