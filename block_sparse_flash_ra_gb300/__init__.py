@@ -64,6 +64,7 @@ class RaAttnParams(ctypes.Structure):
         ("q_pos", ctypes.c_void_p), ("kv_pos", ctypes.c_void_p),
         ("q_seg", ctypes.c_void_p), ("kv_seg", ctypes.c_void_p),
         ("sinks", ctypes.c_void_p), ("local_mask", ctypes.c_void_p),
+        ("block_q_dkv", ctypes.c_int),
     ]
 
 
@@ -75,7 +76,9 @@ class RaBlockMask(ctypes.Structure):
         ("bwd_order", ctypes.c_void_p), ("fwd_shard", ctypes.c_void_p),
         ("part_fwd", ctypes.c_void_p), ("part_bwd", ctypes.c_void_p),
         ("part_rows", ctypes.c_void_p), ("part_cols", ctypes.c_void_p),
-        ("n_part", ctypes.c_void_p), ("B", ctypes.c_int), ("nq", ctypes.c_int),
+        ("n_part", ctypes.c_void_p), ("dkv_class", ctypes.c_void_p), ("dkv_cnt", ctypes.c_void_p),
+        ("dkv_idx", ctypes.c_void_p), ("dkv_slot", ctypes.c_void_p), ("dkv_order", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("nq", ctypes.c_int),
         ("nk", ctypes.c_int), ("n_shards", ctypes.c_int), ("part_cap", ctypes.c_int),
         ("key", ctypes.c_uint64),
     ]
@@ -289,10 +292,11 @@ _DT = {torch.bfloat16: RA_BF16, torch.float32: RA_FP32}
 
 def make_params(q, k, *, scale, causal=False, soft_cap=0.0, n_virtual_shards=1, is_mqa=False,
                 pad_segment_id=-1, q_pos=None, kv_pos=None, q_seg=None, kv_seg=None,
-                sinks=None, local_mask=None) -> RaAttnParams:
+                sinks=None, local_mask=None, block_q_dkv=0) -> RaAttnParams:
     """Params for q (B,Lq,Hq,D) and k (B,Lkv,Hkv,D) tensors; keeps the
     position / segment / sink / local-mask tensors referenced by the struct
-    alive.  ``local_mask``: (Lq/N, Lkv/N) uint8 device tensor (non-causal only)."""
+    alive.  ``local_mask``: (Lq/N, Lkv/N) uint8 device tensor (non-causal only).
+    ``block_q_dkv``: 0 / 128, or 64 for the dK/dV stage's own 64-row grid."""
     B, Lq, Hq, D = q.shape
     Lkv, Hkv = k.shape[1], k.shape[2]
     if q.dtype not in _DT:
@@ -300,7 +304,7 @@ def make_params(q, k, *, scale, causal=False, soft_cap=0.0, n_virtual_shards=1, 
     p = RaAttnParams(B, Lq, Lkv, Hq, Hkv, D, _DT[q.dtype], float(scale),
                      float(soft_cap or 0.0), int(bool(causal)), int(bool(is_mqa)),
                      int(n_virtual_shards), int(pad_segment_id), _ptr(q_pos), _ptr(kv_pos),
-                     _ptr(q_seg), _ptr(kv_seg), _ptr(sinks), _ptr(local_mask))
+                     _ptr(q_seg), _ptr(kv_seg), _ptr(sinks), _ptr(local_mask), int(block_q_dkv))
     p._keep = (q_pos, kv_pos, q_seg, kv_seg, sinks, local_mask)
     return p
 

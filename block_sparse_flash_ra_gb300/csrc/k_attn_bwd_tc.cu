@@ -1157,6 +1157,15 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *t
     return cudaGetLastError();
 }
 
+cudaError_t launch_dkv_reduce(const Problem &p, void *dk, void *dv, cudaStream_t s)
+{
+    const size_t n = (size_t)p.B * p.Lkv * p.Hkv * p.D;
+    const unsigned blocks = (unsigned)((n / 4 + 255) / 256);
+    dkv_reduce_kernel<<<blocks, 256, 0, s>>>(p.dkv_part, p.hsplit, n, static_cast<__nv_bfloat16 *>(dk),
+                                             static_cast<__nv_bfloat16 *>(dv));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
                              const void *tm_v, const void *tm_do, const float *nlse2,
                              const float *delta, void *dq, int num_sms, cudaStream_t s)

@@ -29,7 +29,7 @@
 //    one block per number writes the 128 x 128 visibility bits of the tile of
 //    that row-order number (row-major) and of that column-order number
 //    (transposed), for the numbers below the capacity.
-#include "ra_internal.h"
+#include "ra_sched.cuh"
 
 namespace ra {
 namespace {
@@ -632,6 +632,79 @@ __global__ void __launch_bounds__(128) part_bits_kernel(Problem p, const int32_t
 
 } // namespace
 
+// The backward's grid of 64 query rows x 128 kv rows, one CTA per kv-tile
+// column (thread j = kv row j).  Each non-empty 128 x 128 tile of the column
+// gives its two 64-row halves: a FULL tile two FULL blocks; a PARTIAL tile
+// is split by counting the visible pairs of each half from its stored column
+// bits (or, past the block capacity, from positions and segments), so the
+// classes are exact.  Lists keep ascending block order; each entry carries
+// its parent's column-order partial number (-1 for FULL parents).
+__global__ void __launch_bounds__(kTile) dkv_columns_kernel(Problem p, const uint8_t *cls,
+                                                            const int32_t *bwd_cnt,
+                                                            const int32_t *bwd_idx,
+                                                            const int32_t *part_bwd,
+                                                            const uint32_t *part_cols,
+                                                            uint8_t *dkv_class, int32_t *dkv_cnt,
+                                                            int32_t *dkv_idx, int32_t *dkv_slot)
+{
+    const int b = blockIdx.y, kt = blockIdx.x, j = threadIdx.x;
+    const int nq2 = 2 * p.nq;
+    const int col = b * p.nk + kt;
+    __shared__ int red[kTile / 32];
+    for (int qb = j; qb < nq2; qb += kTile)
+        dkv_class[((size_t)b * nq2 + qb) * p.nk + kt] = RA_TILE_EMPTY;
+    __syncthreads();
+    const int kj = kt * kTile + j;
+    const int kv_pos = p.kv_pos ? p.kv_pos[(size_t)b * p.Lkv + kj] : kj;
+    const int kv_seg = p.kv_seg ? p.kv_seg[(size_t)b * p.Lkv + kj] : 0;
+    const int cnt = bwd_cnt[col];
+    const int32_t *list = bwd_idx + (size_t)col * p.nq;
+    int32_t *oidx = dkv_idx + (size_t)col * nq2;
+    int32_t *oslot = dkv_slot + (size_t)col * nq2;
+    int slot = part_bwd[col], n = 0; // uniform over the CTA
+    for (int e = 0; e < cnt; ++e) {
+        const int qt = list[e];
+        const uint8_t c = cls[((size_t)b * p.nq + qt) * p.nk + kt];
+        uint8_t half_cls[2];
+        int s = -1;
+        if (c == RA_TILE_FULL) {
+            half_cls[0] = half_cls[1] = RA_TILE_FULL;
+        } else {
+            s = slot++;
+            for (int h = 0; h < 2; ++h) {
+                uint2 bits;
+                if (s < p.part_cap)
+                    bits = reinterpret_cast<const uint2 *>(part_cols + ((size_t)s * kTile + j) * 4)[h];
+                else
+                    bits = col_bits_derived(p, b, qt * kTile + 64 * h, kj, kv_seg, kv_pos);
+                int v = __popc(bits.x) + __popc(bits.y);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if ((j & 31) == 0) red[j >> 5] = v;
+                __syncthreads();
+                const int tot = red[0] + red[1] + red[2] + red[3];
+                __syncthreads();
+                half_cls[h] = tot == 0 ? RA_TILE_EMPTY
+                                       : (tot == 64 * kTile ? RA_TILE_FULL : RA_TILE_PARTIAL);
+            }
+        }
+        for (int h = 0; h < 2; ++h) {
+            if (half_cls[h] == RA_TILE_EMPTY) continue;
+            if (j == 0) {
+                dkv_class[((size_t)b * nq2 + 2 * qt + h) * p.nk + kt] = half_cls[h];
+                oidx[n] = 2 * qt + h;
+                oslot[n] = s;
+            }
+            ++n;
+        }
+    }
+    for (int r = n + j; r < nq2; r += kTile) {
+        oidx[r] = -1;
+        oslot[r] = -1;
+    }
+    if (j == 0) dkv_cnt[col] = n;
+}
+
 size_t mask_scratch_ints(int B, int nq, int nk, int N)
 {
     const size_t local_tiles = (size_t)(nq / N) * (nk / N); // one byte each
@@ -647,7 +720,7 @@ int mask_part_cap(int B, int nq, int nk)
 }
 
 cudaError_t launch_mask_build(const Problem &pin, const ra_block_mask &m, int32_t *scratch,
-                              cudaStream_t s)
+                              bool dkv_grid, cudaStream_t s)
 {
     Problem p = pin;
     p.part_cap = m.part_cap;
@@ -676,6 +749,19 @@ cudaError_t launch_mask_build(const Problem &pin, const ra_block_mask &m, int32_
         cols_list);
     part_bits_kernel<<<m.part_cap, kTile, 0, s>>>(p, m.n_part, rows_list, cols_list, m.part_rows,
                                                  m.part_cols);
+    if (!dkv_grid) return cudaGetLastError();
+    dkv_columns_kernel<<<dim3(p.nk, p.B), kTile, 0, s>>>(p, cls, m.bwd_cnt, m.bwd_idx, m.part_bwd,
+                                                         m.part_cols, m.dkv_class, m.dkv_cnt,
+                                                         m.dkv_idx, m.dkv_slot);
+    const size_t sm_d = sizeof(int) * ((size_t)2 * p.nq + 1 + 1024);
+    if (sm_d > 48 * 1024) {
+        // long sequences: the histogram of the 64-row grid's counts needs more
+        // than the default dynamic shared memory (2^20 tokens: 69 KB)
+        const cudaError_t e = cudaFuncSetAttribute(order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)sm_d);
+        if (e != cudaSuccess) return e;
+    }
+    order_kernel<<<1, 1024, sm_d, s>>>(m.dkv_cnt, p.B * p.nk, 2 * p.nq, m.dkv_order);
     return cudaGetLastError();
 }
 

@@ -47,7 +47,7 @@ struct DevCache {
     int num_sms = 0;
     int *status = nullptr;
     bool attr_fwd64 = false, attr_fwd128 = false, attr_bwd64 = false, attr_bwd128 = false,
-         attr_simt64 = false, attr_simt128 = false, attr_fwd2 = false;
+         attr_simt64 = false, attr_simt128 = false, attr_fwd2 = false, attr_dkdv64 = false;
 };
 DevCache g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -122,6 +122,10 @@ int check_params(const ra_attn_params *p)
     if (p->local_mask && p->causal)
         return fail(RA_ERR_INVALID_ARG, "local_mask is only defined for causal == 0 (the causal ring "
                                         "replaces the mask)");
+    if (p->block_q_dkv != 0 && p->block_q_dkv != 64 && p->block_q_dkv != RA_TILE)
+        return fail(RA_ERR_INVALID_ARG, "block_q_dkv must be 0, 64 or 128 (got %d)", p->block_q_dkv);
+    if (p->block_q_dkv == 64 && p->D != 128)
+        return fail(RA_ERR_UNSUPPORTED, "block_q_dkv = 64 is implemented for D = 128");
     const void *ptrs[6] = {p->q_pos, p->kv_pos, p->q_seg, p->kv_seg, p->sinks, p->local_mask};
     for (const void *x : ptrs)
         if (x && !aligned16(x))
@@ -151,12 +155,14 @@ uint64_t mask_key(const ra_attn_params *p)
     h = mix(h, reinterpret_cast<uintptr_t>(p->q_seg));
     h = mix(h, reinterpret_cast<uintptr_t>(p->kv_seg));
     h = mix(h, reinterpret_cast<uintptr_t>(p->local_mask));
+    h = mix(h, (uint64_t)(p->block_q_dkv == 64 ? 64 : RA_TILE));
     return h;
 }
 
 struct MaskLayout {
     size_t cls, fwd_cnt, fwd_idx, bwd_cnt, bwd_idx, fwd_order, bwd_order, fwd_shard, part_fwd,
-        part_bwd, part_rows, part_cols, n_part, scratch, total;
+        part_bwd, part_rows, part_cols, n_part, dkv_class, dkv_cnt, dkv_idx, dkv_slot, dkv_order,
+        scratch, total;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -219,6 +225,11 @@ MaskLayout mask_layout(const ra_attn_params *p)
     m.part_rows = o; o += up256(cap * RA_TILE * 16);
     m.part_cols = o; o += up256(cap * RA_TILE * 16);
     m.n_part = o;    o += 256;
+    m.dkv_class = o; o += up256(B * 2 * nq * nk);
+    m.dkv_cnt = o;   o += up256(4 * B * nk);
+    m.dkv_idx = o;   o += up256(4 * B * nk * 2 * nq);
+    m.dkv_slot = o;  o += up256(4 * B * nk * 2 * nq);
+    m.dkv_order = o; o += up256(4 * B * nk);
     m.scratch = o;   o += up256(4 * mask_scratch_ints((int)B, (int)nq, (int)nk, p->n_virtual_shards));
     m.total = o;
     return m;
@@ -265,6 +276,11 @@ Problem make_problem(const ra_attn_params *p, const ra_block_mask *m, int *statu
         x.part_rows = m->part_rows;
         x.part_cols = m->part_cols;
         x.part_cap = m->part_cap;
+        x.dkv_class = m->dkv_class;
+        x.dkv_cnt = m->dkv_cnt;
+        x.dkv_idx = m->dkv_idx;
+        x.dkv_slot = m->dkv_slot;
+        x.dkv_order = m->dkv_order;
     }
     x.hsplit = 1;
     x.dkv_part = nullptr;
@@ -281,7 +297,8 @@ int check_mask(const ra_attn_params *p, const ra_block_mask *m)
     if (!m) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
     if (!m->tile_class || !m->fwd_cnt || !m->fwd_idx || !m->bwd_cnt || !m->bwd_idx ||
         !m->fwd_order || !m->bwd_order || !m->fwd_shard || !m->part_fwd || !m->part_bwd ||
-        !m->part_rows || !m->part_cols || !m->n_part)
+        !m->part_rows || !m->part_cols || !m->n_part || !m->dkv_class || !m->dkv_cnt ||
+        !m->dkv_idx || !m->dkv_slot || !m->dkv_order)
         return fail(RA_ERR_INVALID_ARG, "mask has NULL arrays (not built?)");
     if (m->B != p->B || m->nq != p->Lq / RA_TILE || m->nk != p->Lkv / RA_TILE ||
         m->n_shards != p->n_virtual_shards || m->key != mask_key(p) ||
@@ -291,14 +308,15 @@ int check_mask(const ra_attn_params *p, const ra_block_mask *m)
     return RA_OK;
 }
 
-// 4-D TMA descriptor over a (B, L, H, D) bf16 tensor, box (64, 1, 128, 1),
-// 128-byte swizzle: one box is 128 token rows x 64 head-dim elements.
-int encode_rows(CUtensorMap *map, const void *base, int B, int L, int H, int D)
+// 4-D TMA descriptor over a (B, L, H, D) bf16 tensor, box (64, 1, rows, 1),
+// 128-byte swizzle: one box is `rows` token rows (128, or 64 for the dK/dV
+// stage's query blocks) x 64 head-dim elements.
+int encode_rows(CUtensorMap *map, const void *base, int B, int L, int H, int D, int rows = RA_TILE)
 {
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
                                    (cuuint64_t)L * H * D * 2};
-    const cuuint32_t box[4] = {64, 1, (cuuint32_t)RA_TILE, 1};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -361,6 +379,11 @@ RA_API int ra_build_block_mask(const ra_attn_params *p, void *buf, size_t buf_by
     m.part_rows = reinterpret_cast<uint32_t *>(b + L.part_rows);
     m.part_cols = reinterpret_cast<uint32_t *>(b + L.part_cols);
     m.n_part = reinterpret_cast<int32_t *>(b + L.n_part);
+    m.dkv_class = b + L.dkv_class;
+    m.dkv_cnt = reinterpret_cast<int32_t *>(b + L.dkv_cnt);
+    m.dkv_idx = reinterpret_cast<int32_t *>(b + L.dkv_idx);
+    m.dkv_slot = reinterpret_cast<int32_t *>(b + L.dkv_slot);
+    m.dkv_order = reinterpret_cast<int32_t *>(b + L.dkv_order);
     m.B = p->B;
     m.nq = p->Lq / RA_TILE;
     m.nk = p->Lkv / RA_TILE;
@@ -368,10 +391,11 @@ RA_API int ra_build_block_mask(const ra_attn_params *p, void *buf, size_t buf_by
     m.part_cap = mask_part_cap(m.B, m.nq, m.nk);
     m.key = mask_key(p);
     const Problem pr = make_problem(p, nullptr, dc->status);
-    cudaError_t e = launch_mask_build(pr, m, reinterpret_cast<int32_t *>(b + L.scratch),
+    const bool dkv = p->block_q_dkv == 64;
+    cudaError_t e = launch_mask_build(pr, m, reinterpret_cast<int32_t *>(b + L.scratch), dkv,
                                       reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "mask build launch");
-    count(kMaskBuildKernels + (p->local_mask ? 1 : 0));
+    count(kMaskBuildKernels + (p->local_mask ? 1 : 0) + (dkv ? 2 : 0));
     *out = m;
     return RA_OK;
 }
@@ -627,7 +651,22 @@ int bwd_tc_kernels(const ra_attn_params *p, DevCache *dc, const Problem &pr, int
         Problem ps = pr;
         ps.hsplit = w.hsplit;
         ps.dkv_part = w.dkv_part;
-        e = launch_bwd_dkdv_tc(ps, &tq, &tk, &tv, &tdo, w.nlse2, w.delta, dk, dv, dc->num_sms, s);
+        if (p->block_q_dkv == 64) {
+            // the backward's own tile shape: 64 query rows per step
+            if (!dc->attr_dkdv64) {
+                if ((e = bwd_dkdv64_set_attributes()) != cudaSuccess)
+                    return cuda_fail(e, "backward dK/dV attributes");
+                dc->attr_dkdv64 = true;
+            }
+            alignas(64) CUtensorMap tq64, tdo64;
+            if ((rc = encode_rows(&tq64, q, p->B, p->Lq, p->Hq, p->D, 64))) return rc;
+            if ((rc = encode_rows(&tdo64, dout, p->B, p->Lq, p->Hq, p->D, 64))) return rc;
+            e = launch_bwd_dkdv64_tc(ps, &tq64, &tk, &tv, &tdo64, w.nlse2, w.delta, dk, dv,
+                                     dc->num_sms, s);
+            if (e == cudaSuccess && w.hsplit > 1) e = launch_dkv_reduce(ps, dk, dv, s);
+        } else {
+            e = launch_bwd_dkdv_tc(ps, &tq, &tk, &tv, &tdo, w.nlse2, w.delta, dk, dv, dc->num_sms, s);
+        }
         if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
         count(w.hsplit > 1 ? 2 : 1);
     }

@@ -37,6 +37,11 @@ struct Problem {
     const int32_t *part_fwd, *part_bwd;
     const uint32_t *part_rows, *part_cols; // (part_cap, 128, 4) words each
     int part_cap;
+    // the backward's grid of 64 query rows x 128 kv rows: classes, per-column
+    // lists of non-empty 64-row blocks with their parents' partial numbers,
+    // and the longest-first column order
+    const uint8_t *dkv_class;
+    const int32_t *dkv_cnt, *dkv_idx, *dkv_slot, *dkv_order;
     // dK/dV schedule: each kv head's G query heads are split into hsplit
     // chunks of units; with hsplit > 1 each chunk stores its scaled dK and
     // dV as fp32 partials (dkv_part: dK then dV, each (hsplit, B, Lkv, Hkv, D))
@@ -67,7 +72,8 @@ cudaError_t launch_permute(const void *in, void *out, int B, int L, size_t row_b
 // segments and local mask; `scratch` holds mask_scratch_ints() ints.
 // Launches kMaskBuildKernels kernels, one more with a local mask.
 cudaError_t launch_mask_build(const Problem &p, const ra_block_mask &m, int32_t *scratch,
-                              cudaStream_t s);
+                              bool dkv_grid, cudaStream_t s);
+// kernels of a build; two more with the backward's 64-row grid (dkv_grid)
 constexpr int kMaskBuildKernels = 9;
 size_t mask_scratch_ints(int B, int nq, int nk, int N);
 // slots of partial mask blocks in a map of B x nq x nk tiles
@@ -93,6 +99,14 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *tm_q, const void *t
                                const void *tm_v, const void *tm_do, const float *nlse2,
                                const float *delta, void *dk, void *dv, int num_sms,
                                cudaStream_t s);
+// dK/dV on the backward's own grid (64 query rows per step, D = 128), and
+// the sum of the head split's fp32 partials into dk, dv (hsplit > 1)
+cudaError_t bwd_dkdv64_set_attributes();
+cudaError_t launch_bwd_dkdv64_tc(const Problem &p, const void *tm_q64, const void *tm_k,
+                                 const void *tm_v, const void *tm_do64, const float *nlse2,
+                                 const float *delta, void *dk, void *dv, int num_sms,
+                                 cudaStream_t s);
+cudaError_t launch_dkv_reduce(const Problem &p, void *dk, void *dv, cudaStream_t s);
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
                              const void *tm_v, const void *tm_do, const float *nlse2,
                              const float *delta, void *dq, int num_sms, cudaStream_t s);

@@ -108,6 +108,12 @@ enum { RA_TILE_EMPTY = 0, RA_TILE_PARTIAL = 1, RA_TILE_FULL = 2 };
  *                    the mask; the combination is rejected here).  16-byte
  *                    aligned; owned by the caller, read by the block-map
  *                    build and by the attention kernels on partial tiles.
+ *   block_q_dkv      query rows per step of the backward's dK/dV stage: 0 or
+ *                    128 (the default: 128 x 128 tiles, the forward's grid)
+ *                    or 64 (the backward's own grid of 64 query rows x 128
+ *                    kv rows, _ring_splash make_ring_attention's
+ *                    block_q_dkv with has_backward_blocks; D = 128 only).
+ *                    The block map then also carries the dkv_* arrays.
  */
 typedef struct {
     int B, Lq, Lkv, Hq, Hkv, D;
@@ -124,6 +130,7 @@ typedef struct {
     const int32_t *kv_seg;
     const float *sinks;
     const uint8_t *local_mask;
+    int block_q_dkv;
 } ra_attn_params;
 
 /*
@@ -162,6 +169,17 @@ typedef struct {
  *               row j is set iff query row qt*128+32w+z sees kv row kt*128+j.
  *   n_part      (1) int32: PARTIAL tiles in the map (blocks stored:
  *               min(n_part, part_cap)).
+ * The backward's own grid (make_ring_attention's dkv MaskInfo with
+ * block_sizes.has_backward_blocks; Kvax create_attention_mask's backward
+ * mask): blocks of 64 query rows x 128 kv rows, which the dK/dV stage walks
+ * when params.block_q_dkv == 64 (filled only then):
+ *   dkv_class   (B, 2*nq, nk) uint8: EMPTY / PARTIAL / FULL of each block.
+ *   dkv_cnt     (B*nk) non-empty 64-row query blocks of each kv-tile column.
+ *   dkv_idx     (B*nk, 2*nq) their 64-row block index, ascending, -1 padded.
+ *   dkv_slot    (B*nk, 2*nq) for each listed block, the column-order number
+ *               of its 128 x 128 parent when that is PARTIAL (the parent's
+ *               stored bits give the block's visibility), -1 when FULL.
+ *   dkv_order   (B*nk) column ids by descending dkv_cnt, ties by id.
  *   part_cap    4 * B * (nq + nk).
  *   key         fingerprint of the ra_attn_params fields the map depends on;
  *               attention calls reject a map built for other params.
@@ -180,6 +198,11 @@ typedef struct {
     uint32_t *part_rows;
     uint32_t *part_cols;
     int32_t *n_part;
+    uint8_t *dkv_class;
+    int32_t *dkv_cnt;
+    int32_t *dkv_idx;
+    int32_t *dkv_slot;
+    int32_t *dkv_order;
     int B, nq, nk, n_shards, part_cap;
     uint64_t key;
 } ra_block_mask;

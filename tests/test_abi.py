@@ -51,6 +51,7 @@ def _params(**kw):
     dict(Hq=3, Hkv=2), dict(is_mqa=1, Hkv=2), dict(Lq=200), dict(Lq=384, n_virtual_shards=2),
     dict(n_virtual_shards=0), dict(B=0), dict(dtype=7), dict(scale=0.0),
     dict(local_mask=256),  # a local mask needs causal == 0
+    dict(block_q_dkv=32),  # the dK/dV stage's grids: 128 (default) or 64 query rows
 ])
 def test_invalid_params_rejected(L, bad):
     p = _params(**bad)
@@ -59,6 +60,13 @@ def test_invalid_params_rejected(L, bad):
     rc = L.ra_attn_fwd(ctypes.byref(p), 16, 16, 16, ctypes.byref(m), 16, 16, None, 0, None)
     assert rc == ra.RA_ERR_INVALID_ARG
     assert ra.ra_last_error()
+
+
+def test_backward_grid_of_64_rows_needs_d128(L):
+    p = _params(D=64, block_q_dkv=64)
+    assert L.ra_block_mask_bytes(ctypes.byref(p)) == 0
+    assert "block_q_dkv" in ra.ra_last_error()
+    assert L.ra_block_mask_bytes(ctypes.byref(_params(block_q_dkv=64))) > 0
 
 
 def test_segments_must_come_in_pairs(L):

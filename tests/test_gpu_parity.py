@@ -63,7 +63,7 @@ class Case:
     """One problem, with inputs on both sides in the (possibly permuted) order."""
 
     def __init__(self, w: Workload, *, structure=None, seed_struct=0, dout=False,
-                 overrides=None):
+                 overrides=None, block_q_dkv=0):
         self.w = w
         inp = make_inputs(w, with_dout=dout)
         if structure is not None:
@@ -87,7 +87,7 @@ class Case:
             dev["q"], dev["k"], scale=w.scale, causal=w.causal, soft_cap=w.soft_cap,
             n_virtual_shards=N, is_mqa=w.is_mqa, q_pos=dev["q_pos"], kv_pos=dev["kv_pos"],
             q_seg=dev["q_seg"], kv_seg=dev["kv_seg"], sinks=dev["sinks"],
-            local_mask=dev.get("local_mask"))
+            local_mask=dev.get("local_mask"), block_q_dkv=block_q_dkv)
         self.okw = dict(scale=w.scale, soft_cap=w.soft_cap or None, causal=w.causal,
                         q_pos=i32(host["q_pos"]), kv_pos=i32(host["kv_pos"]),
                         q_seg=i32(host["q_seg"]), kv_seg=i32(host["kv_seg"]),
@@ -231,6 +231,37 @@ def check_partial_blocks(m, cls, vis, n_shards):
     return len(part)
 
 
+def check_dkv_map(m, B, L, cls128, **okw):
+    """The backward's grid (64 query rows x 128 kv rows) against the oracle's
+    map on that grid: classes, column counts and lists, the column order, and
+    for each listed block its parent's column-order partial number."""
+    ref = oracle.block_mask(B, L, L, block_q=64, block_kv=128, **okw)
+    nq, nk = L // 128, L // 128
+    got = dict(tile_class=_dev_arr(m, m.dkv_class, B * 2 * nq * nk, torch.uint8),
+               bwd_cnt=_dev_arr(m, m.dkv_cnt, B * nk, torch.int32),
+               bwd_idx=_dev_arr(m, m.dkv_idx, B * nk * 2 * nq, torch.int32),
+               bwd_order=_dev_arr(m, m.dkv_order, B * nk, torch.int32))
+    for key, val in got.items():
+        assert np.array_equal(val.reshape(-1), np.asarray(ref[key]).reshape(-1)), key
+    # parents' numbers: PARTIAL 128 x 128 tiles numbered by column (b*nk+kt),
+    # then query tile, over the whole map
+    slot = _dev_arr(m, m.dkv_slot, B * nk * 2 * nq, torch.int32).reshape(B * nk, 2 * nq)
+    idx = np.asarray(ref["bwd_idx"]).reshape(B * nk, 2 * nq)
+    cols = cls128.transpose(0, 2, 1).reshape(B * nk, nq)
+    number, n = {}, 0
+    for c in range(B * nk):
+        for qt in range(nq):
+            if cols[c, qt] == 1:
+                number[(c, qt)] = n
+                n += 1
+    for c in range(B * nk):
+        for e, qb in enumerate(idx[c]):
+            if qb < 0:
+                assert slot[c, e] == -1
+                continue
+            assert slot[c, e] == number.get((c, qb // 2), -1), (c, e)
+
+
 @pytest.mark.parametrize("seed", range(5))
 def test_block_mask_bit_exact(seed):
     g = torch.Generator().manual_seed(seed)
@@ -239,10 +270,10 @@ def test_block_mask_bit_exact(seed):
                                 shuffle_positions=(seed == 4))
     causal = seed != 3
     n_shards = (4, 3, 5, 11, 6)[seed]  # divides nq = 8 + seed
-    q = torch.zeros(B, L, 1, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(B, L, 1, 128, dtype=torch.bfloat16, device="cuda")
     dseg, dpos = seg.cuda(), pos.cuda()
     p = ra.make_params(q, q, scale=1.0, causal=causal, q_pos=dpos, kv_pos=dpos, q_seg=dseg,
-                       kv_seg=dseg, n_virtual_shards=n_shards)
+                       kv_seg=dseg, n_virtual_shards=n_shards, block_q_dkv=64)
     m = ra.build_mask(p)
     torch.cuda.synchronize()
     ref = oracle.block_mask(B, L, L, causal=causal, q_pos=pos.numpy(), kv_pos=pos.numpy(),
@@ -276,6 +307,8 @@ def test_block_mask_bit_exact(seed):
     vis = visibility(B, L, L, causal=causal, q_pos=pos.numpy(), kv_pos=pos.numpy(),
                      q_seg=seg.numpy(), kv_seg=seg.numpy())
     check_partial_blocks(m, np.asarray(ref["tile_class"]).reshape(B, nq, nk), vis, n_shards)
+    check_dkv_map(m, B, L, np.asarray(ref["tile_class"]).reshape(B, nq, nk), causal=causal,
+                  q_pos=pos.numpy(), kv_pos=pos.numpy(), q_seg=seg.numpy(), kv_seg=seg.numpy())
 
 
 def test_block_mask_partial_blocks_past_capacity():
@@ -283,10 +316,10 @@ def test_block_mask_partial_blocks_past_capacity():
     g = torch.Generator().manual_seed(4)
     B, L, N = 1, 2048, 2
     seg, pos = random_structure(g, B, L, n_docs_max=2, shuffle_positions=True)
-    q = torch.zeros(B, L, 1, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(B, L, 1, 128, dtype=torch.bfloat16, device="cuda")
     dseg, dpos = seg.cuda(), pos.cuda()
     p = ra.make_params(q, q, scale=1.0, causal=True, q_pos=dpos, kv_pos=dpos, q_seg=dseg,
-                       kv_seg=dseg, n_virtual_shards=N)
+                       kv_seg=dseg, n_virtual_shards=N, block_q_dkv=64)
     m = ra.build_mask(p)
     torch.cuda.synchronize()
     ref = oracle.block_mask(B, L, L, causal=True, q_pos=pos.numpy(), kv_pos=pos.numpy(),
@@ -296,6 +329,10 @@ def test_block_mask_partial_blocks_past_capacity():
     nq = L // 128
     n_part = check_partial_blocks(m, np.asarray(ref["tile_class"]).reshape(B, nq, nq), vis, N)
     assert n_part > m.part_cap
+    # the backward grid's classes of parents past the capacity come from
+    # positions and segments: exact all the same
+    check_dkv_map(m, B, L, np.asarray(ref["tile_class"]).reshape(B, nq, nq), causal=True,
+                  q_pos=pos.numpy(), kv_pos=pos.numpy(), q_seg=seg.numpy(), kv_seg=seg.numpy())
 
 
 def test_block_mask_sequential_positions_bit_exact():
@@ -414,9 +451,14 @@ def _check_bwd(c, grads):
         assert err <= GRAD_TOL, ("dsinks", err)
 
 
+# block_q_dkv = 64: the dK/dV stage on the backward's own grid (64 query rows
+# x 128 kv rows; D = 128 only)
+@pytest.mark.parametrize("block_q_dkv", [0, 64], ids=["dkv128", "dkv64"])
 @pytest.mark.parametrize("name", list(BWD_CASES))
-def test_backward_matches_oracle(name):
-    c = Case(BWD_CASES[name], dout=True)
+def test_backward_matches_oracle(name, block_q_dkv):
+    if block_q_dkv == 64 and BWD_CASES[name].D != 128:
+        pytest.skip("the 64-row dK/dV grid serves D = 128")
+    c = Case(BWD_CASES[name], dout=True, block_q_dkv=block_q_dkv)
     out, lse, m = c.gpu_fwd()
     d = c.dev
     grads = ra.backward(c.params, d["q"], d["k"], d["v"], out, lse, d["dout"], m)
@@ -525,10 +567,10 @@ def test_local_mask_block_map_bit_exact():
     B, L, N = 2, 1024, 4
     seg, pos = random_structure(g, B, L, n_docs_max=3, pad_max=150)
     lm = _local_mask(3, L // N, window=180, density=0.97)
-    q = torch.zeros(B, L, 1, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(B, L, 1, 128, dtype=torch.bfloat16, device="cuda")
     dseg, dlm = seg.cuda(), lm.cuda()
     p = ra.make_params(q, q, scale=1.0, causal=False, q_seg=dseg, kv_seg=dseg,
-                       n_virtual_shards=N, local_mask=dlm)
+                       n_virtual_shards=N, local_mask=dlm, block_q_dkv=64)
     m = ra.build_mask(p)
     torch.cuda.synchronize()
     ref = oracle.block_mask(B, L, L, causal=False, q_seg=seg.numpy(), kv_seg=seg.numpy(),
@@ -542,3 +584,5 @@ def test_local_mask_block_map_bit_exact():
     vis = visibility(B, L, L, causal=False, q_seg=seg.numpy(), kv_seg=seg.numpy(),
                      local_mask=lm.numpy())
     check_partial_blocks(m, got.reshape(B, nq, nk), vis, N)
+    check_dkv_map(m, B, L, got.reshape(B, nq, nk), causal=False, q_seg=seg.numpy(),
+                  kv_seg=seg.numpy(), local_mask=lm.numpy())
