@@ -480,19 +480,21 @@ def run_e2e(pipe, K, ws_, rank=0):
     if ws_ > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    s.record(up)
-    for i in range(K):
-        one(i)
-    # the region ends when the last results are on the host
-    for st in (up, comp):
-        down.wait_stream(st)
-    e.record(down)
-    torch.cuda.synchronize()
+    with Clocks(torch.cuda.current_device()) as clk:
+        s.record(up)
+        for i in range(K):
+            one(i)
+        # the region ends when the last results are on the host
+        for st in (up, comp):
+            down.wait_stream(st)
+        e.record(down)
+        torch.cuda.synchronize()
     ms = max_over_ranks(s.elapsed_time(e) / K, ws_)
     v = job_tflops(pipe.f_fwd_bwd, ms, ws_)
     return {"value": round(v, 2), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K,
-            "overlap": "input copy of step i+1 and result copy of step i-1 overlap step i"}
+            "overlap": "input copy of step i+1 and result copy of step i-1 overlap step i",
+            "clocks": clk.summary()}
 
 
 # ---------------------------------------------------------------- oracle

@@ -697,7 +697,7 @@ RA_API int ra_attn_bwd_prep(const ra_attn_params *p, const void *out, const floa
     cudaError_t e = launch_bwd_pre(pr, out, dout, p->dtype, lse, w.delta, w.nlse2, w.part, dsinks,
                                    reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward preprocessing launch");
-    count(p->sinks ? 2 : 1);
+    count(p->sinks ? 3 : 1);
     return RA_OK;
 }
 
@@ -783,7 +783,7 @@ int bwd_all(const ra_attn_params *p, const void *q, const void *k, const void *v
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_bwd_pre(pr, out, dout, p->dtype, lse, w.delta, w.nlse2, w.part, dsinks, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward preprocessing launch");
-    count(p->sinks ? 2 : 1);
+    count(p->sinks ? 3 : 1);
     if (p->dtype == RA_BF16)
         return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, dout, w, dq, dk, dv, s);
     // fp32 inputs: Delta and dsinks above come from the fp32 out / dout; the

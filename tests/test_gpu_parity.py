@@ -366,7 +366,7 @@ def test_permute_bit_exact(dtype, inner, n):
 
 
 # ------------------------------------------------------------ merge
-@pytest.mark.parametrize("D", [128, 8, 200])
+@pytest.mark.parametrize("D", [128, 64, 8, 4, 200, 132])
 def test_merge_matches_oracle(D):
     g = torch.Generator().manual_seed(5)
     B, L, H = 2, 301, 3
