@@ -601,26 +601,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D>
 struct DqCfg {
     static constexpr int kTileBytes = kTile * D * 2;
-    static constexpr int kQOff = 0;
-    static constexpr int kDoOff = kTileBytes;
-    static constexpr int kKOff = 2 * kTileBytes;
-    // a K tile is held from S(g) to dQ(g), a V tile only until dP(g)
+    // only K and V pass through shared memory: Q and dO sit in TMEM as the A
+    // operands of S = Q K^T and dP = dO V^T for the whole unit.  A K tile is
+    // held from S(g) to dQ(g), a V tile only until dP(g).
+    static constexpr int kKOff = 0;
     static constexpr int kKStages = 3;
     static constexpr int kVStages = 2;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-    static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 8;
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 7;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmem = (kMiscOff + 16 + 1024) > 122880 ? (kMiscOff + 16 + 1024) : 122880;
     static_assert(kSmem <= 232448, "dQ shared memory exceeds the 227 KB per-block limit");
-    // dP / dS double buffer: tile g uses kColDP[g & 1]
-    static constexpr uint32_t kColDP0 = 128, kColDP1 = 384, kColDQ = 256;
+    // TMEM: S, dP (dS written over it), dQ, and the unit's Q and dO rows as
+    // packed bf16 pairs (D / 2 columns each)
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+    static constexpr uint32_t kColQA = 384, kColDOA = 384 + D / 2;
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);
-    static __device__ __forceinline__ uint32_t dp_col(uint32_t g) { return (g & 1) ? kColDP1 : kColDP0; }
 };
 
 struct DqBars {
-    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *dp_full, *s_free,
+    uint64_t *qa_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *dp_full, *s_free,
         *ds_ready, *acc_ready, *drain;
 };
 
@@ -630,17 +631,16 @@ __device__ __forceinline__ DqBars dq_bars(uint8_t *smem)
     using C = DqCfg<D>;
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     DqBars r;
-    r.q_full = b;
-    r.q_empty = b + 1;
-    r.k_full = b + 2;
+    r.qa_full = b;
+    r.k_full = b + 1;
     r.k_empty = r.k_full + C::kKStages;
     r.v_full = r.k_empty + C::kKStages;
     r.v_empty = r.v_full + C::kVStages;
     r.s_full = r.v_empty + C::kVStages;
-    r.dp_full = r.s_full + 1;    // [2], one per dP buffer
-    r.s_free = r.dp_full + 2;
-    r.ds_ready = r.s_free + 1;   // [2], one per dP buffer
-    r.acc_ready = r.ds_ready + 2;
+    r.dp_full = r.s_full + 1;
+    r.s_free = r.dp_full + 1;
+    r.ds_ready = r.s_free + 1;
+    r.acc_ready = r.ds_ready + 1;
     r.drain = r.acc_ready + 1;
     return r;
 }
@@ -664,8 +664,8 @@ __device__ __forceinline__ RowUnit row_unit(const Problem &p, int u)
 
 template <int D, bool CAP>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+    bwd_dq_kernel(const __nv_bfloat16 *__restrict__ q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16 *__restrict__ dout,
                   Problem p, const float *__restrict__ nlse2, const float *__restrict__ delta,
                   __nv_bfloat16 *__restrict__ dq)
 {
@@ -682,8 +682,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int Gd = gridDim.x;
 
     if (threadIdx.x == 0) {
-        mbar_init(bars.q_full, 1);
-        mbar_init(bars.q_empty, 1);
+        mbar_init(bars.qa_full, kSoftmaxThreads);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bars.k_full + s, 1);
             mbar_init(bars.k_empty + s, 1);
@@ -694,10 +693,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(bars.s_full, 1);
         mbar_init(bars.s_free, kSoftmaxThreads);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bars.dp_full + s, 1);
-            mbar_init(bars.ds_ready + s, kSoftmaxThreads);
-        }
+        mbar_init(bars.dp_full, 1);
+        mbar_init(bars.ds_ready, kSoftmaxThreads);
         mbar_init(bars.acc_ready, 1);
         mbar_init(bars.drain, 1);
         *abort_flag = 0;
@@ -708,10 +705,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
-        prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_do);
     }
     tc_fence_before();
     __syncthreads();
@@ -723,7 +718,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (warp == kProducerWarp) {
             // ---------------------------------------------------------- producer
             if (lane == 0) {
-                uint32_t g = 0, uq = 0;
+                uint32_t g = 0;
                 uint32_t k_issued[C::kKStages] = {}, v_issued[C::kVStages] = {};
                 bool ok = true;
                 for (int r = 0; ok && r * Gd < U; ++r) {
@@ -731,15 +726,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (u >= U) continue;
                     const RowUnit x = row_unit(p, u);
                     if (x.cnt == 0) continue;
-                    if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
-                    mbar_expect_tx(bars.q_full, 2 * C::kTileBytes);
-                    for (int hb = 0; hb < D / 64; ++hb) {
-                        tma_load_4d(smem + C::kQOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h,
-                                    x.qt * kTile, x.b);
-                        tma_load_4d(smem + C::kDoOff + hb * 16384, &tm_do, bars.q_full, hb * 64, x.h,
-                                    x.qt * kTile, x.b);
-                    }
-                    ++uq;
                     const int g_kv = x.h / p.G;
                     for (int e = 0; e < x.cnt; ++e) {
                         const int kt = x.list[e];
@@ -765,85 +751,75 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
                     for (int s = 0; s < C::kVStages; ++s)
                         if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
-                    if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
                 }
             }
         } else if (warp == kMmaWarp) {
             // ---------------------------------------------------------- MMA issuer
             if (lane == 0) {
-                const uint32_t q_base = smem_u32(smem + C::kQOff);
-                const uint32_t do_base = smem_u32(smem + C::kDoOff);
                 const uint32_t k_base = smem_u32(smem + C::kKOff);
                 const uint32_t v_base = smem_u32(smem + C::kVOff);
                 uint32_t g = 0, uq = 0;
                 bool ok = true;
-                auto wait_kv = [&](uint32_t t) -> bool {
-                    if (!mbar_wait(bars.k_full + t % C::kKStages, (t / C::kKStages) & 1, ctx)) return false;
-                    if (!mbar_wait(bars.v_full + t % C::kVStages, (t / C::kVStages) & 1, ctx)) return false;
-                    tc_fence_after();
-                    return true;
-                };
-                // S = Q K^T of tile t into columns [0,128)
+                // S = Q K^T of tile t into columns [0,128): A = the unit's Q rows
+                // from TMEM (16-column K chunk kk at column 8 kk), B = the K tile
                 // descriptors are built once per operand; an offset o adds o / 16
-                const uint64_t qd = sdesc_sw128(q_base, 16, 1024), dod = sdesc_sw128(do_base, 16, 1024);
-                auto issue_s = [&](uint32_t t) {
+                auto issue_s = [&](uint32_t t) -> bool {
+                    if (!mbar_wait(bars.k_full + t % C::kKStages, (t / C::kKStages) & 1, ctx)) return false;
+                    tc_fence_after();
                     const uint64_t kd = sdesc_sw128(k_base + (t % C::kKStages) * C::kTileBytes, 16, 1024);
     #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        mma_ss(tmem, qd + o, kd + o, kIdescT, kk > 0 ? 1u : 0u);
+                        mma_ts(tmem + C::kColS, tmem + C::kColQA + kk * 8, kd + o, kIdescT, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bars.s_full);
+                    return true;
                 };
-                // dP = dO V^T of tile t into its dP buffer; V's stage is free after it
-                auto issue_dp = [&](uint32_t t) {
+                // dP = dO V^T of tile t into [128,256); V's stage is free after it
+                auto issue_dp = [&](uint32_t t) -> bool {
+                    if (!mbar_wait(bars.v_full + t % C::kVStages, (t / C::kVStages) & 1, ctx)) return false;
+                    tc_fence_after();
                     const uint64_t vd = sdesc_sw128(v_base + (t % C::kVStages) * C::kTileBytes, 16, 1024);
     #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        mma_ss(tmem + C::dp_col(t), dod + o, vd + o, kIdescT, kk > 0 ? 1u : 0u);
+                        mma_ts(tmem + C::kColDP, tmem + C::kColDOA + kk * 8, vd + o, kIdescT, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bars.dp_full + (t & 1));
+                    tc_commit(bars.dp_full);
                     tc_commit(bars.v_empty + t % C::kVStages);
+                    return true;
                 };
-                // Issue order: S(g) and dP(g) together, as soon as phase A(g-1) has
-                // read S(g-1) (S is single-buffered); dQ(g) once phase B(g) has
-                // written dS(g) over dP(g).  dP is double-buffered, so dP(g+1)
-                // never waits for dQ(g): the softmax phases of tile g+1 overlap
-                // the products dQ(g), S(g+2), dP(g+2).  dP(g+1) overwrites the
-                // buffer of dS(g-1), whose reader dQ(g-1) is already issued.
+                // Issue order per tile g: S(g+1) as soon as phase A(g) has read S(g);
+                // dQ(g) once phase B(g) has written dS(g) over dP(g); then dP(g+1),
+                // which the in-order pipe runs after dQ(g) has read dS(g).  Every
+                // product takes its A operand from TMEM, so the shared-memory
+                // traffic per product is the one B tile.
                 for (int r = 0; ok && r * Gd < U; ++r) {
                     const int u = unit_index(r, blockIdx.x, Gd);
                     if (u >= U) continue;
                     const RowUnit x = row_unit(p, u);
                     if (x.cnt == 0) continue;
-                    if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                    // the softmax warps have put this unit's Q and dO rows in TMEM
+                    if (!(ok = mbar_wait(bars.qa_full, uq & 1, ctx))) break;
                     tc_fence_after();
                     ++uq;
-                    if (!(ok = wait_kv(g))) break;
-                    issue_s(g);
-                    issue_dp(g);
-                    if (x.cnt == 1) tc_commit(bars.q_empty);
+                    if (!(ok = issue_s(g))) break;
+                    if (!(ok = issue_dp(g))) break;
                     for (int e = 0; e < x.cnt; ++e, ++g) {
                         if (!(ok = mbar_wait(bars.s_free, g & 1, ctx))) break;
-                        if (e + 1 < x.cnt) {
-                            if (!(ok = wait_kv(g + 1))) break;
-                            issue_s(g + 1);
-                            issue_dp(g + 1);
-                            // Q and dO of the unit are read by nothing after this
-                            if (e + 2 == x.cnt) tc_commit(bars.q_empty);
-                        }
+                        if (e + 1 < x.cnt && !(ok = issue_s(g + 1))) break;
                         // dQ += dS K   (A = dS from TMEM, B = K as a K=kv x N=D MN-major tile)
-                        if (!(ok = mbar_wait(bars.ds_ready + (g & 1), (g >> 1) & 1, ctx))) break;
+                        if (!(ok = mbar_wait(bars.ds_ready, g & 1, ctx))) break;
                         tc_fence_after();
                         const int sk = g % C::kKStages;
                         const uint64_t kmn = sdesc_sw128(k_base + sk * C::kTileBytes, 16384, 1024);
     #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts(tmem + C::kColDQ, tmem + C::dp_col(g) + kk * 8 + (kk >= 4 ? 32 : 0),
+                            mma_ts(tmem + C::kColDQ, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
                                    kmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                    (e > 0 || kk > 0) ? 1u : 0u);
                         tc_commit(bars.k_empty + sk);
+                        if (e + 1 < x.cnt && !(ok = issue_dp(g + 1))) break;
                     }
                     if (!ok) break;
                     tc_commit(bars.acc_ready);
@@ -880,6 +856,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int qi = x.qt * kTile + row;
             __nv_bfloat16 *qrow = dq + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D + o_col;
             if (x.cnt > 0) {
+                {
+                    // the unit's A operands: group 0 puts this thread's Q row, group 1
+                    // its dO row, into TMEM as packed bf16 pairs (the row's memory
+                    // order: element 2c in the low half of column c).  The previous
+                    // unit's S and dP products have completed (its last phase B
+                    // waited for them).
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        (wg == 0 ? q : dout) + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D);
+                    uint32_t a[D / 2];
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) {
+                        const uint4 t = src[c];
+                        a[4 * c] = t.x;
+                        a[4 * c + 1] = t.y;
+                        a[4 * c + 2] = t.z;
+                        a[4 * c + 3] = t.w;
+                    }
+                    const uint32_t acol = wg == 0 ? C::kColQA : C::kColDOA;
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) tmem_st32(lane_base + acol + 32 * c, a + 32 * c);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bars.qa_full);
+                }
                 const size_t li = ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
                 // exponent offset -lse * log2 e (0 for a row with nothing visible:
                 // it only meets partial tiles, where the mask zeroes every P)
@@ -990,8 +990,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tc_fence_before();
                     mbar_arrive(bars.s_free);
                     // ---- phase B: dS = Pc (dP - Delta), written over this half's dP columns
-                    const uint32_t dpc = C::dp_col(g);
-                    if (!(ok = wait_all(bars.dp_full + (g & 1), (g >> 1) & 1))) break;
+                    const uint32_t dpc = C::kColDP;
+                    if (!(ok = wait_all(bars.dp_full, g & 1))) break;
                     tc_fence_after();
                     {
                         float dpv[64];
@@ -1010,7 +1010,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(bars.ds_ready + (g & 1));
+                    mbar_arrive(bars.ds_ready);
                 }
                 if (!ok) break;
                 if (!(ok = wait_all(bars.acc_ready, ua & 1))) break;
@@ -1123,8 +1123,8 @@ void launch_dkdv_d(const Problem &p, int grid, const CUtensorMap &q, const CUten
 }
 
 template <int D>
-void launch_dq_d(const Problem &p, int grid, const CUtensorMap &q, const CUtensorMap &k,
-                 const CUtensorMap &v, const CUtensorMap &d, const float *nlse2, const float *delta,
+void launch_dq_d(const Problem &p, int grid, const __nv_bfloat16 *q, const CUtensorMap &k,
+                 const CUtensorMap &v, const __nv_bfloat16 *d, const float *nlse2, const float *delta,
                  __nv_bfloat16 *gq, cudaStream_t s)
 {
     if (p.soft_cap > 0.f)
@@ -1166,16 +1166,16 @@ cudaError_t launch_dkv_reduce(const Problem &p, void *dk, void *dv, cudaStream_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
-                             const void *tm_v, const void *tm_do, const float *nlse2,
+cudaError_t launch_bwd_dq_tc(const Problem &p, const void *q_ptr, const void *tm_k,
+                             const void *tm_v, const void *do_ptr, const float *nlse2,
                              const float *delta, void *dq, int num_sms, cudaStream_t s)
 {
     const int U = p.B * p.nq * p.Hq;
     const int grid = U < num_sms ? U : num_sms;
-    const CUtensorMap &q = *static_cast<const CUtensorMap *>(tm_q);
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(q_ptr);
     const CUtensorMap &k = *static_cast<const CUtensorMap *>(tm_k);
     const CUtensorMap &v = *static_cast<const CUtensorMap *>(tm_v);
-    const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
+    const __nv_bfloat16 *d = static_cast<const __nv_bfloat16 *>(do_ptr);
     __nv_bfloat16 *gq = static_cast<__nv_bfloat16 *>(dq);
     if (p.D == 64)
         launch_dq_d<64>(p, grid, q, k, v, d, nlse2, delta, gq, s);
