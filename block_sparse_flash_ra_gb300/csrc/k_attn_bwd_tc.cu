@@ -601,15 +601,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D>
 struct DqCfg {
     static constexpr int kTileBytes = kTile * D * 2;
-    // only K and V pass through shared memory: Q and dO sit in TMEM as the A
-    // operands of S = Q K^T and dP = dO V^T for the whole unit.  A K tile is
-    // held from S(g) to dQ(g), a V tile only until dP(g).
-    static constexpr int kKOff = 0;
+    // Q and dO of a unit land in shared memory by TMA and are copied into
+    // TMEM once (tcgen05.cp), where they are the A operands of S = Q K^T and
+    // dP = dO V^T for the whole unit; their shared-memory tiles are then free
+    // for the next unit's.  A K tile is held from S(g) to dQ(g), a V tile
+    // only until dP(g).
+    static constexpr int kQOff = 0;
+    static constexpr int kDoOff = kTileBytes;
+    static constexpr int kKOff = 2 * kTileBytes;
     static constexpr int kKStages = 3;
     static constexpr int kVStages = 2;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 7;
+    static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 7;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmem = (kMiscOff + 16 + 1024) > 122880 ? (kMiscOff + 16 + 1024) : 122880;
     static_assert(kSmem <= 232448, "dQ shared memory exceeds the 227 KB per-block limit");
@@ -621,7 +625,7 @@ struct DqCfg {
 };
 
 struct DqBars {
-    uint64_t *qa_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *dp_full, *s_free,
+    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *dp_full, *s_free,
         *ds_ready, *acc_ready, *drain;
 };
 
@@ -631,8 +635,9 @@ __device__ __forceinline__ DqBars dq_bars(uint8_t *smem)
     using C = DqCfg<D>;
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     DqBars r;
-    r.qa_full = b;
-    r.k_full = b + 1;
+    r.q_full = b;
+    r.q_empty = b + 1;
+    r.k_full = b + 2;
     r.k_empty = r.k_full + C::kKStages;
     r.v_full = r.k_empty + C::kKStages;
     r.v_empty = r.v_full + C::kVStages;
@@ -664,8 +669,8 @@ __device__ __forceinline__ RowUnit row_unit(const Problem &p, int u)
 
 template <int D, bool CAP>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dq_kernel(const __nv_bfloat16 *__restrict__ q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16 *__restrict__ dout,
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   Problem p, const float *__restrict__ nlse2, const float *__restrict__ delta,
                   __nv_bfloat16 *__restrict__ dq)
 {
@@ -682,7 +687,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int Gd = gridDim.x;
 
     if (threadIdx.x == 0) {
-        mbar_init(bars.qa_full, kSoftmaxThreads);
+        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bars.k_full + s, 1);
             mbar_init(bars.k_empty + s, 1);
@@ -705,8 +711,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
     }
     tc_fence_before();
     __syncthreads();
@@ -718,7 +726,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (warp == kProducerWarp) {
             // ---------------------------------------------------------- producer
             if (lane == 0) {
-                uint32_t g = 0;
+                uint32_t g = 0, uq = 0;
                 uint32_t k_issued[C::kKStages] = {}, v_issued[C::kVStages] = {};
                 bool ok = true;
                 for (int r = 0; ok && r * Gd < U; ++r) {
@@ -726,6 +734,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (u >= U) continue;
                     const RowUnit x = row_unit(p, u);
                     if (x.cnt == 0) continue;
+                    if (!(ok = mbar_wait(bars.q_empty, (uq & 1) ^ 1, ctx))) break;
+                    mbar_expect_tx(bars.q_full, 2 * C::kTileBytes);
+                    for (int hb = 0; hb < D / 64; ++hb) {
+                        tma_load_4d(smem + C::kQOff + hb * 16384, &tm_q, bars.q_full, hb * 64, x.h,
+                                    x.qt * kTile, x.b);
+                        tma_load_4d(smem + C::kDoOff + hb * 16384, &tm_do, bars.q_full, hb * 64, x.h,
+                                    x.qt * kTile, x.b);
+                    }
+                    ++uq;
                     const int g_kv = x.h / p.G;
                     for (int e = 0; e < x.cnt; ++e) {
                         const int kt = x.list[e];
@@ -751,6 +768,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (k_issued[s]) wait_drain(bars.k_full + s, (k_issued[s] - 1) & 1, kDrainNs);
                     for (int s = 0; s < C::kVStages; ++s)
                         if (v_issued[s]) wait_drain(bars.v_full + s, (v_issued[s] - 1) & 1, kDrainNs);
+                    if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
                 }
             }
         } else if (warp == kMmaWarp) {
@@ -758,6 +776,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) {
                 const uint32_t k_base = smem_u32(smem + C::kKOff);
                 const uint32_t v_base = smem_u32(smem + C::kVOff);
+                const uint64_t qd = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
+                const uint64_t dod = sdesc_sw128(smem_u32(smem + C::kDoOff), 16, 1024);
                 uint32_t g = 0, uq = 0;
                 bool ok = true;
                 // S = Q K^T of tile t into columns [0,128): A = the unit's Q rows
@@ -799,10 +819,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (u >= U) continue;
                     const RowUnit x = row_unit(p, u);
                     if (x.cnt == 0) continue;
-                    // the softmax warps have put this unit's Q and dO rows in TMEM
-                    if (!(ok = mbar_wait(bars.qa_full, uq & 1, ctx))) break;
+                    // this unit's Q and dO tiles into TMEM, 16 columns of the head
+                    // dimension per copy, at the K-chunk offsets the products use.
+                    // No product still reads the previous unit's: its last dP had
+                    // completed before its last phase B began.
+                    if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
                     tc_fence_after();
                     ++uq;
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        tmem_cp_128x256b(tmem + C::kColQA + kk * 8, qd + o);
+                        tmem_cp_128x256b(tmem + C::kColDOA + kk * 8, dod + o);
+                    }
+                    tc_commit(bars.q_empty); // the tiles' shared memory is free once the copies are done
                     if (!(ok = issue_s(g))) break;
                     if (!(ok = issue_dp(g))) break;
                     for (int e = 0; e < x.cnt; ++e, ++g) {
@@ -856,30 +886,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int qi = x.qt * kTile + row;
             __nv_bfloat16 *qrow = dq + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D + o_col;
             if (x.cnt > 0) {
-                {
-                    // the unit's A operands: group 0 puts this thread's Q row, group 1
-                    // its dO row, into TMEM as packed bf16 pairs (the row's memory
-                    // order: element 2c in the low half of column c).  The previous
-                    // unit's S and dP products have completed (its last phase B
-                    // waited for them).
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        (wg == 0 ? q : dout) + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h) * D);
-                    uint32_t a[D / 2];
-#pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
-                        const uint4 t = src[c];
-                        a[4 * c] = t.x;
-                        a[4 * c + 1] = t.y;
-                        a[4 * c + 2] = t.z;
-                        a[4 * c + 3] = t.w;
-                    }
-                    const uint32_t acol = wg == 0 ? C::kColQA : C::kColDOA;
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c) tmem_st32(lane_base + acol + 32 * c, a + 32 * c);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    mbar_arrive(bars.qa_full);
-                }
                 const size_t li = ((size_t)x.b * p.Hq + x.h) * p.Lq + qi;
                 // exponent offset -lse * log2 e (0 for a row with nothing visible:
                 // it only meets partial tiles, where the mask zeroes every P)
@@ -1123,8 +1129,8 @@ void launch_dkdv_d(const Problem &p, int grid, const CUtensorMap &q, const CUten
 }
 
 template <int D>
-void launch_dq_d(const Problem &p, int grid, const __nv_bfloat16 *q, const CUtensorMap &k,
-                 const CUtensorMap &v, const __nv_bfloat16 *d, const float *nlse2, const float *delta,
+void launch_dq_d(const Problem &p, int grid, const CUtensorMap &q, const CUtensorMap &k,
+                 const CUtensorMap &v, const CUtensorMap &d, const float *nlse2, const float *delta,
                  __nv_bfloat16 *gq, cudaStream_t s)
 {
     if (p.soft_cap > 0.f)
@@ -1166,16 +1172,16 @@ cudaError_t launch_dkv_reduce(const Problem &p, void *dk, void *dv, cudaStream_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq_tc(const Problem &p, const void *q_ptr, const void *tm_k,
-                             const void *tm_v, const void *do_ptr, const float *nlse2,
+cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
+                             const void *tm_v, const void *tm_do, const float *nlse2,
                              const float *delta, void *dq, int num_sms, cudaStream_t s)
 {
     const int U = p.B * p.nq * p.Hq;
     const int grid = U < num_sms ? U : num_sms;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(q_ptr);
+    const CUtensorMap &q = *static_cast<const CUtensorMap *>(tm_q);
     const CUtensorMap &k = *static_cast<const CUtensorMap *>(tm_k);
     const CUtensorMap &v = *static_cast<const CUtensorMap *>(tm_v);
-    const __nv_bfloat16 *d = static_cast<const __nv_bfloat16 *>(do_ptr);
+    const CUtensorMap &d = *static_cast<const CUtensorMap *>(tm_do);
     __nv_bfloat16 *gq = static_cast<__nv_bfloat16 *>(dq);
     if (p.D == 64)
         launch_dq_d<64>(p, grid, q, k, v, d, nlse2, delta, gq, s);

@@ -671,7 +671,7 @@ int bwd_tc_kernels(const ra_attn_params *p, DevCache *dc, const Problem &pr, int
         count(w.hsplit > 1 ? 2 : 1);
     }
     if (stages & kDq) {
-        e = launch_bwd_dq_tc(pr, q, &tk, &tv, dout, w.nlse2, w.delta, dq, dc->num_sms, s);
+        e = launch_bwd_dq_tc(pr, &tq, &tk, &tv, &tdo, w.nlse2, w.delta, dq, dc->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
         count(1);
     }

@@ -156,6 +156,15 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
 }
 
 // D(tmem) (+)= A(smem desc) x B(smem desc)^T, kind::f16 (bf16 in, fp32 acc).
+// tcgen05.cp: 128 rows x 256 bits (16 bf16) of a shared-memory matrix, named
+// by a matrix descriptor as an MMA operand is, into 128 lanes x 8 columns of
+// TMEM (row r -> lane r, the 16 elements packed two per column).  Issued by
+// the MMA thread; it runs ahead of the products issued after it.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)
 {

@@ -107,10 +107,8 @@ cudaError_t launch_bwd_dkdv64_tc(const Problem &p, const void *tm_q64, const voi
                                  const float *delta, void *dk, void *dv, int num_sms,
                                  cudaStream_t s);
 cudaError_t launch_dkv_reduce(const Problem &p, void *dk, void *dv, cudaStream_t s);
-// q_ptr, do_ptr: the bf16 q and dO tensors themselves (the dQ kernel reads
-// a unit's rows straight into TMEM); tm_k, tm_v: their TMA maps
-cudaError_t launch_bwd_dq_tc(const Problem &p, const void *q_ptr, const void *tm_k,
-                             const void *tm_v, const void *do_ptr, const float *nlse2,
+cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
+                             const void *tm_v, const void *tm_do, const float *nlse2,
                              const float *delta, void *dq, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,
                                 const float *dout, const float *lse, const float *delta,
