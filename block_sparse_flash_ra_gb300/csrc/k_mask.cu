@@ -52,9 +52,10 @@ __device__ __forceinline__ int pos_at(const int32_t *pos, int b, int L, int i)
     return pos ? pos[(size_t)b * L + i] : i;
 }
 
-// grid (ntiles, B), 128 threads: thread i looks at row tile*128 + i.
-__global__ void __launch_bounds__(128) tile_summary_kernel(const int32_t *seg, const int32_t *pos,
-                                                           int L, int pad_id, TileSum *out)
+// One side (query or key rows) of the summaries: blockIdx.x = tile, thread i
+// looks at row tile*128 + i.
+__device__ __forceinline__ void tile_summary(const int32_t *seg, const int32_t *pos, int L, int pad_id,
+                                             TileSum *out)
 {
     const int b = blockIdx.y, t = blockIdx.x, i = t * kTile + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -113,6 +114,20 @@ __global__ void __launch_bounds__(128) tile_summary_kernel(const int32_t *seg, c
         __syncthreads();
     }
     if (threadIdx.x == 0) out[(size_t)b * gridDim.x + t] = ts;
+}
+
+// grid (max(nq, nk), B, 2), 128 threads: z = 0 summarises the query-row
+// tiles, z = 1 the key-row tiles (blocks past a side's tile count return).
+__global__ void __launch_bounds__(128) tile_summary_kernel(const int32_t *q_seg, const int32_t *q_pos,
+                                                           int Lq, const int32_t *kv_seg,
+                                                           const int32_t *kv_pos, int Lkv, int pad_id,
+                                                           TileSum *qsum, TileSum *ksum)
+{
+    const bool q_side = blockIdx.z == 0;
+    const int L = q_side ? Lq : Lkv;
+    if ((int)blockIdx.x >= L / kTile) return;
+    if (q_side) tile_summary(q_seg, q_pos, Lq, pad_id, qsum);
+    else tile_summary(kv_seg, kv_pos, Lkv, pad_id, ksum);
 }
 
 // Class from the summaries when it is exact, else -1 (count pairs).  With
@@ -412,8 +427,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *wsum, int &total
 
 // Stable counting sort of ids 0..R-1 by descending cnt[id] (ties by id).
 // One block of 1024 threads; hist needs (maxc + 1) ints of dynamic smem.
-__global__ void __launch_bounds__(1024) order_kernel(const int32_t *cnt, int R, int maxc,
-                                                     int32_t *order)
+__device__ __forceinline__ void order_block(const int32_t *cnt, int R, int maxc, int32_t *order)
 {
     extern __shared__ int hist[]; // [maxc + 1], then [1024] partials
     int *part = hist + maxc + 1;
@@ -456,15 +470,19 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t *cnt, int R, 
     }
 }
 
-// Block 0: exclusive prefix over rows of their partial counts, added to
+__global__ void __launch_bounds__(1024) order_kernel(const int32_t *cnt, int R, int maxc,
+                                                     int32_t *order)
+{
+    order_block(cnt, R, maxc, order);
+}
+
+// by_rows: exclusive prefix over rows of their partial counts, added to
 // every per-shard entry of the row (entry N held the row's own total), and
-// the grand total into n_part.  Block 1: exclusive prefix over columns.
-__global__ void __launch_bounds__(1024) part_scan_kernel(int32_t *part_fwd, int rows, int n1,
-                                                         int32_t *part_bwd, int cols,
-                                                         int32_t *n_part)
+// the grand total into n_part; else: exclusive prefix over columns.
+__device__ __forceinline__ void part_scan_block(bool by_rows, int32_t *part_fwd, int rows, int n1,
+                                                int32_t *part_bwd, int cols, int32_t *n_part)
 {
     __shared__ int wsum[32];
-    const bool by_rows = blockIdx.x == 0;
     const int R = by_rows ? rows : cols;
     const int per = (R + 1023) / 1024;
     const int lo = min(R, (int)threadIdx.x * per), hi = min(R, lo + per);
@@ -485,6 +503,21 @@ __global__ void __launch_bounds__(1024) part_scan_kernel(int32_t *part_fwd, int 
             part_bwd[r] = run;
             run += v;
         }
+    }
+}
+
+// The row and column orders and the partial-tile numbering, which all read
+// only the classified map: 4 blocks of 1024 threads, block 0 the row order
+// (fwd_order), 1 the column order (bwd_order), 2 and 3 the row and column
+// scans of the partial counts.  Dynamic smem: the larger histogram.
+__global__ void __launch_bounds__(1024) orders_scans_kernel(const ra_block_mask m, int B, int nq, int nk,
+                                                            int n1)
+{
+    switch (blockIdx.x) {
+    case 0: order_block(m.fwd_cnt, B * nq, nk, m.fwd_order); break;
+    case 1: order_block(m.bwd_cnt, B * nk, nq, m.bwd_order); break;
+    case 2: part_scan_block(true, m.part_fwd, B * nq, n1, m.part_bwd, B * nk, m.n_part); break;
+    default: part_scan_block(false, m.part_fwd, B * nq, n1, m.part_bwd, B * nk, m.n_part); break;
     }
 }
 
@@ -730,20 +763,18 @@ cudaError_t launch_mask_build(const Problem &pin, const ra_block_mask &m, int32_
     TileSum *qsum = reinterpret_cast<TileSum *>(cols_list + m.part_cap);
     TileSum *ksum = qsum + (size_t)p.B * p.nq;
     uint8_t *lcls = reinterpret_cast<uint8_t *>(ksum + (size_t)p.B * p.nk);
-    tile_summary_kernel<<<dim3(p.nq, p.B), 128, 0, s>>>(p.q_seg, p.q_pos, p.Lq, p.pad_id, qsum);
-    tile_summary_kernel<<<dim3(p.nk, p.B), 128, 0, s>>>(p.kv_seg, p.kv_pos, p.Lkv, p.pad_id, ksum);
+    tile_summary_kernel<<<dim3(max(p.nq, p.nk), p.B, 2), 128, 0, s>>>(
+        p.q_seg, p.q_pos, p.Lq, p.kv_seg, p.kv_pos, p.Lkv, p.pad_id, qsum, ksum);
     if (p.local_mask)
         local_tile_kernel<<<dim3(p.tq, p.tk), kCls, 0, s>>>(p.local_mask, p.lk_s, p.tk, lcls);
     classify_rows_kernel<<<dim3(p.nq, p.B), kCls, 0, s>>>(p, qsum, ksum, lcls, cls, m.fwd_cnt,
                                                           m.fwd_idx, m.fwd_shard, m.part_fwd);
     columns_kernel<<<dim3(p.nk, p.B), kCls, 0, s>>>(cls, p.nq, p.nk, m.bwd_cnt, m.bwd_idx,
                                                     m.part_bwd);
-    const size_t sm_f = sizeof(int) * ((size_t)p.nk + 1 + 1024);
-    const size_t sm_b = sizeof(int) * ((size_t)p.nq + 1 + 1024);
-    order_kernel<<<1, 1024, sm_f, s>>>(m.fwd_cnt, p.B * p.nq, p.nk, m.fwd_order);
-    order_kernel<<<1, 1024, sm_b, s>>>(m.bwd_cnt, p.B * p.nk, p.nq, m.bwd_order);
-    part_scan_kernel<<<2, 1024, 0, s>>>(m.part_fwd, p.B * p.nq, p.N + 1, m.part_bwd, p.B * p.nk,
-                                        m.n_part);
+    // histograms of nk + 1 (rows) or nq + 1 (columns) counts: at most 8193
+    // ints for 2^20 tokens, 37 KB with the partials, under the default limit
+    const size_t sm_o = sizeof(int) * ((size_t)max(p.nq, p.nk) + 1 + 1024);
+    orders_scans_kernel<<<4, 1024, sm_o, s>>>(m, p.B, p.nq, p.nk, p.N + 1);
     part_list_kernel<<<dim3(max(p.nq, p.nk), p.B, 2), kTile, 0, s>>>(
         p, cls, m.fwd_cnt, m.fwd_idx, m.part_fwd, m.bwd_cnt, m.bwd_idx, m.part_bwd, rows_list,
         cols_list);

@@ -74,7 +74,7 @@ cudaError_t launch_permute(const void *in, void *out, int B, int L, size_t row_b
 cudaError_t launch_mask_build(const Problem &p, const ra_block_mask &m, int32_t *scratch,
                               bool dkv_grid, cudaStream_t s);
 // kernels of a build; two more with the backward's 64-row grid (dkv_grid)
-constexpr int kMaskBuildKernels = 9;
+constexpr int kMaskBuildKernels = 6;
 size_t mask_scratch_ints(int B, int nq, int nk, int N);
 // slots of partial mask blocks in a map of B x nq x nk tiles
 int mask_part_cap(int B, int nq, int nk);
