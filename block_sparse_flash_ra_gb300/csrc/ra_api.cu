@@ -47,7 +47,7 @@ struct DevCache {
     int num_sms = 0;
     int *status = nullptr;
     bool attr_fwd64 = false, attr_fwd128 = false, attr_bwd64 = false, attr_bwd128 = false,
-         attr_simt64 = false, attr_simt128 = false, attr_fwd2 = false, attr_dkdv64 = false;
+         attr_f32tc64 = false, attr_f32tc128 = false, attr_fwd2 = false, attr_dkdv64 = false;
 };
 DevCache g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -426,13 +426,13 @@ RA_API int ra_attn_fwd(const ra_attn_params *p, const void *q, const void *k, co
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (p->dtype == RA_FP32) {
-        bool &done = p->D == 64 ? dc->attr_simt64 : dc->attr_simt128;
+        bool &done = p->D == 64 ? dc->attr_f32tc64 : dc->attr_f32tc128;
         if (!done) {
-            if ((e = simt_set_attributes(p->D)) != cudaSuccess) return cuda_fail(e, "simt attributes");
+            if ((e = f32tc_set_attributes(p->D)) != cudaSuccess) return cuda_fail(e, "fp32 forward attributes");
             done = true;
         }
-        e = launch_fwd_simt_f32(pr, static_cast<const float *>(q), static_cast<const float *>(k),
-                                static_cast<const float *>(v), static_cast<float *>(out), lse, s);
+        e = launch_fwd_f32_tc(pr, static_cast<const float *>(q), static_cast<const float *>(k),
+                              static_cast<const float *>(v), static_cast<float *>(out), lse, s);
         if (e != cudaSuccess) return cuda_fail(e, "forward (fp32) launch");
         count(1);
         return RA_OK;

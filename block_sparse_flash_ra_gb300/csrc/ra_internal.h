@@ -80,8 +80,10 @@ size_t mask_scratch_ints(int B, int nq, int nk, int N);
 int mask_part_cap(int B, int nq, int nk);
 cudaError_t launch_merge(float *out, float *lse, const float *bout, const float *blse, int B,
                          int L, int H, int D, cudaStream_t s);
-cudaError_t launch_fwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,
-                                float *out, float *lse, cudaStream_t s);
+// fp32 inputs: the forward on the tensor cores (kind::tf32, the logits from
+// three hi / lo products)
+cudaError_t launch_fwd_f32_tc(const Problem &p, const float *q, const float *k, const float *v,
+                              float *out, float *lse, cudaStream_t s);
 cudaError_t launch_fwd_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,
                           void *out, float *lse, int num_sms, cudaStream_t s);
 // The two-heads-per-CTA forward (D = 128, an even number of query heads per
@@ -110,9 +112,6 @@ cudaError_t launch_dkv_reduce(const Problem &p, void *dk, void *dv, cudaStream_t
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *tm_q, const void *tm_k,
                              const void *tm_v, const void *tm_do, const float *nlse2,
                              const float *delta, void *dq, int num_sms, cudaStream_t s);
-cudaError_t launch_bwd_simt_f32(const Problem &p, const float *q, const float *k, const float *v,
-                                const float *dout, const float *lse, const float *delta,
-                                float *dq, float *dk, float *dv, cudaStream_t s);
 
 // fp32 -> bf16 (or a copy for fp32) of n elements; acc += x over n floats
 cudaError_t launch_cast_from_f32(const float *in, void *out, size_t n, int dtype, cudaStream_t s);
@@ -126,7 +125,7 @@ int bwd_dkdv_smem_bytes(int D);
 int bwd_dq_smem_bytes(int D);
 cudaError_t fwd_tc_set_attributes(int D);
 cudaError_t bwd_tc_set_attributes(int D);
-cudaError_t simt_set_attributes(int D);
+cudaError_t f32tc_set_attributes(int D);
 
 // ra_attn_bwd with the dK/dV head split allowed or not (without it the
 // workspace needs only bwd_ws_min_bytes).

@@ -130,6 +130,10 @@ FWD_CASES = {
     "d64": W(D=64, seed=17),
     "d64_cap50_sinks": W(D=64, soft_cap=50.0, sinks=True, seed=22),
     "d64_fp32": W(D=64, dtype="fp32", seed=18, L=512),
+    "d128_fp32_gqa_sinks_cap20_zigzag": W(dtype="fp32", Hq=4, Hkv=2, sinks=True, soft_cap=20.0,
+                                          zigzag=True, n_shards=4, L=512, seed=61),
+    "d128_fp32_noncausal_b2_n3": W(dtype="fp32", causal=False, B=2, Hq=2, Hkv=1, L=384,
+                                   n_shards=3, seed=62),
     "zigzag_n4": W(zigzag=True, n_shards=4, seed=19),
     "b2_gqa": W(B=2, Hq=6, Hkv=3, seed=20, L=768, n_shards=3),
 }
@@ -156,7 +160,27 @@ STRUCT_CASES = {
     "shuffled_positions_past_block_capacity": (W(seed=26, L=2048, Hq=2, Hkv=1, n_shards=2),
                                                dict(n_docs_max=2, shuffle_positions=True)),
     "noncausal_segments": (W(causal=False, seed=24), dict(n_docs_max=6, pad_max=50)),
+    "fp32_packed_docs_pad": (W(B=2, seed=63, dtype="fp32", L=512, sinks=True),
+                             dict(n_docs_max=4, pad_max=100)),
 }
+
+
+# fp32 inputs run on the tensor cores with the logits from three tf32 products
+# (q and k split into hi and lo parts), so lse stays near fp32 accuracy; P and
+# V enter the output product in tf32 (relative 2^-11 per term)
+F32_LSE_TOL, F32_O_TOL = 1e-4, 4e-3
+
+
+@pytest.mark.parametrize("name", [n for n in FWD_CASES if "fp32" in n])
+def test_fp32_forward_keeps_fp32_logits(name):
+    c = Case(FWD_CASES[name])
+    out, lse, _ = c.gpu_fwd()
+    torch.cuda.synchronize()
+    o_ref, l_ref = c.oracle_fwd()
+    l, fin = f64(lse), np.isfinite(l_ref)
+    assert np.array_equal(np.isfinite(l), fin)
+    assert np.max(np.abs(l[fin] - l_ref[fin])) <= F32_LSE_TOL
+    assert np.max(np.abs(f64(out) - o_ref)) <= F32_O_TOL
 
 
 @pytest.mark.parametrize("workspace", [True, False], ids=["ws", "no_ws"])
