@@ -45,9 +45,9 @@ UNIT = "TFLOP/s"
 # (_src_hash); a changed source, or another workload, reports null.
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch, ncu on the gqa32k bench step
-    ("gqa32k", "fwd2_tc_kernel"): (3.367e9 + 1.714e9, "9daef49e2794ba1a"),
-    ("gqa32k", "bwd_dkdv_kernel"): (4.069e9 + 0.121e9, "cdba98e9dd7eaf21"),
-    ("gqa32k", "bwd_dq_kernel"): (3.542e9 + 0.241e9, "cdba98e9dd7eaf21"),
+    ("gqa32k", "fwd2_tc_kernel"): (3.594e9 + 1.847e9, "fc7cd6632ae7adb7"),
+    ("gqa32k", "bwd_dkdv_kernel"): (4.065e9 + 0.118e9, "416d2e3a9d077e1c"),
+    ("gqa32k", "bwd_dq_kernel"): (3.510e9 + 0.240e9, "416d2e3a9d077e1c"),
 }
 
 
