@@ -490,6 +490,50 @@ def test_backward_matches_oracle(name, block_q_dkv):
     _check_bwd(c, grads)
 
 
+# Query and key lengths that differ: each virtual device holds Lq/N query rows
+# and Lkv/N key rows.  "suffix": the queries are the last Lq positions of the
+# key sequence (explicit positions), so causal rows see a prefix of keys.
+UNEQUAL = {
+    "lkv2x_noncausal_n2": dict(Lq=512, Lkv=1024, causal=False, N=2, seed=71),
+    "lkv2x_causal_suffix_n4_sinks": dict(Lq=512, Lkv=1024, causal=True, N=4, seed=72, suffix=True,
+                                         sinks=True),
+    "lq2x_causal_n2_cap20": dict(Lq=1024, Lkv=512, causal=True, N=2, seed=73, cap=20.0),
+    "lkv3x_gqa_d64_n1": dict(Lq=256, Lkv=768, causal=False, N=1, seed=74, D=64, Hq=6),
+}
+
+
+@pytest.mark.parametrize("name", list(UNEQUAL))
+def test_unequal_lengths_match_oracle(name):
+    cfg = UNEQUAL[name]
+    g = torch.Generator().manual_seed(cfg["seed"])
+    B, Hq, Hkv, D = 1, cfg.get("Hq", 4), 2, cfg.get("D", 128)
+    Lq, Lkv, N = cfg["Lq"], cfg["Lkv"], cfg["N"]
+    q, do = (torch.randn(B, Lq, Hq, D, generator=g).to(torch.bfloat16) for _ in range(2))
+    k, v = (torch.randn(B, Lkv, Hkv, D, generator=g).to(torch.bfloat16) for _ in range(2))
+    q_pos = kv_pos = None
+    if cfg.get("suffix"):
+        q_pos = (torch.arange(Lq, dtype=torch.int32) + (Lkv - Lq)).expand(B, Lq).contiguous()
+        kv_pos = torch.arange(Lkv, dtype=torch.int32).expand(B, Lkv).contiguous()
+    sinks = torch.randn(Hq, generator=g) if cfg.get("sinks") else None
+    cu = lambda t: None if t is None else t.cuda()  # noqa: E731
+    dq_, dk_, dv_, ddo = cu(q), cu(k), cu(v), cu(do)
+    p = ra.make_params(dq_, dk_, scale=D ** -0.5, causal=cfg["causal"], soft_cap=cfg.get("cap", 0.0),
+                       n_virtual_shards=N, q_pos=cu(q_pos), kv_pos=cu(kv_pos), sinks=cu(sinks))
+    m = ra.build_mask(p)
+    out, lse = ra.forward(p, dq_, dk_, dv_, m)
+    grads = ra.backward(p, dq_, dk_, dv_, out, lse, ddo, m)
+    torch.cuda.synchronize()
+    okw = dict(scale=D ** -0.5, soft_cap=cfg.get("cap"), causal=cfg["causal"], q_pos=i32(q_pos),
+               kv_pos=i32(kv_pos), sinks=f64(sinks))
+    o_ref, l_ref = oracle.attn_fwd_ring(f64(q), f64(k), f64(v), n_shards=N, **okw)
+    check_fwd(out, lse, o_ref, l_ref)
+    dq, dk, dv, ds, _, _ = oracle.attn_bwd(f64(q), f64(k), f64(v), f64(do), **okw)
+    for nm, got, ref in (("dq", grads[0], dq), ("dk", grads[1], dk), ("dv", grads[2], dv)):
+        assert rel_l2(f64(got), ref) <= GRAD_TOL, nm
+    if ds is not None:
+        assert rel_l2(f64(grads[3]), ds) <= GRAD_TOL
+
+
 def test_backward_packed_docs_with_padding():
     c = Case(W(B=2, L=768, Hq=2, Hkv=2, seed=35, n_shards=3, sinks=True), dout=True,
              structure=dict(n_docs_max=4, pad_max=200), seed_struct=9)
