@@ -365,9 +365,13 @@ __global__ void __launch_bounds__(kThreads64, 1)
                         const float4 *l4 = reinterpret_cast<const float4 *>(lse_s);
                         uint32_t pk[32];
                         if (CAP) {
-                            float xa = 0.f;
+                            // max |s| in four independent chains (one serial chain of max3 would
+                            // put 32 dependent instructions on the softmax's path)
+                            float xa4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                            for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
+                            for (int j = 0; j < 64; j += 8)
+                                for (int k = 0; k < 4; ++k) xa4[k] = max3(xa4[k], fabsf(s[j + 2 * k]), fabsf(s[j + 2 * k + 1]));
+                            const float xa = fmaxf(fmaxf(xa4[0], xa4[1]), fmaxf(xa4[2], xa4[3]));
                             const bool tiny = __all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny) != 0;
                             if (tiny || __all_sync(0xffffffffu, xa * scale_over_cap < kTanhSmall)) {
                                 // tanh by its odd Taylor series on the FMA pipe, two lanes

@@ -598,9 +598,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, s + 32 * c);
                     tmem_ld_wait();
                     if (cap > 0.f) {
-                        float xa = 0.f;
+                        // max |s| in four independent chains (one serial chain of max3 would
+                        // put 64 dependent instructions on the softmax's path)
+                        float xa4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int j = 0; j < 128; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
+                        for (int j = 0; j < 128; j += 8)
+                            for (int k = 0; k < 4; ++k) xa4[k] = max3(xa4[k], fabsf(s[j + 2 * k]), fabsf(s[j + 2 * k + 1]));
+                        const float xa = fmaxf(fmaxf(xa4[0], xa4[1]), fmaxf(xa4[2], xa4[3]));
                         if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny)) {
                             const float kk = scale_over_cap;
                             const float2 A = make_float2(cap2 * kk, cap2 * kk);

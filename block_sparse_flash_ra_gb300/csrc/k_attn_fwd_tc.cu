@@ -689,9 +689,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     // with a soft cap the logits are formed here in log2 units;
                     // without one s stays raw and the scale rides in the exponent
                     if (cap > 0.f) {
-                        float xa = 0.f;
+                        // max |s| in four independent chains (one serial chain of max3 would
+                        // put 32 dependent instructions on the softmax's path)
+                        float xa4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int j = 0; j < 64; j += 2) xa = max3(xa, fabsf(s[j]), fabsf(s[j + 1]));
+                        for (int j = 0; j < 64; j += 8)
+                            for (int k = 0; k < 4; ++k) xa4[k] = max3(xa4[k], fabsf(s[j + 2 * k]), fabsf(s[j + 2 * k + 1]));
+                        const float xa = fmaxf(fmaxf(xa4[0], xa4[1]), fmaxf(xa4[2], xa4[3]));
                         if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny)) {
                             // cap * log2 e * (x - x^3/3), x = s * scale / cap, as
                             // s * (A + B s^2): three instructions per pair of logits
