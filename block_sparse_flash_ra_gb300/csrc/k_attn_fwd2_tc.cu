@@ -564,6 +564,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const float cap2 = cap * kLog2e;
         const float scale_over_cap = cap > 0.f ? p.scale / cap : 0.f;
         const float a_mul = cap > 0.f ? 1.f : scale2;
+        // the cubic soft-cap tier as cA s + cB s^3 (base-2 logits): tanh x ~ x - x^3 / 3
+        const float cA = cap2 * scale_over_cap;
+        const float cB = cap2 * kTanhC3 * scale_over_cap * scale_over_cap * scale_over_cap;
         uint32_t g = 0, nshard = 0;
         bool ok = true;
         auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -597,6 +600,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, s + 32 * c);
                     tmem_ld_wait();
+                    // fused: the cubic soft cap evaluated inside the exponent argument
+                    // (FULL tiles whose |s scale / cap| are all below 1/8); the
+                    // reference max is then the cap of max |s|, an upper bound of the
+                    // row's capped logits that the normalisation cancels
+                    bool fused = false;
+                    float tmax;
                     if (cap > 0.f) {
                         // max |s| in four independent chains (one serial chain of max3 would
                         // put 64 dependent instructions on the softmax's path)
@@ -605,11 +614,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         for (int j = 0; j < 128; j += 8)
                             for (int k = 0; k < 4; ++k) xa4[k] = max3(xa4[k], fabsf(s[j + 2 * k]), fabsf(s[j + 2 * k + 1]));
                         const float xa = fmaxf(fmaxf(xa4[0], xa4[1]), fmaxf(xa4[2], xa4[3]));
-                        if (__all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny)) {
-                            const float kk = scale_over_cap;
-                            const float2 A = make_float2(cap2 * kk, cap2 * kk);
-                            const float2 B = make_float2(cap2 * kTanhC3 * kk * kk * kk,
-                                                         cap2 * kTanhC3 * kk * kk * kk);
+                        const bool tiny = __all_sync(0xffffffffu, xa * scale_over_cap < kTanhTiny) != 0;
+                        if (tiny && !partial) {
+                            fused = true;
+                            tmax = xa * fmaf(xa * xa, cB, cA);
+                        } else if (tiny) {
+                            const float2 A = make_float2(cA, cA);
+                            const float2 B = make_float2(cB, cB);
 #pragma unroll
                             for (int j = 0; j < 128; j += 2) {
                                 const float2 v = make_float2(s[j], s[j + 1]);
@@ -645,15 +656,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         for (int j = 0; j < 128; ++j)
                             if (!((vw[j >> 5] >> (j & 31)) & 1u)) s[j] = -INFINITY;
                     }
-                    float mx[8];
+                    if (!fused) {
+                        float mx[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        mx[k] = max3(s[k], s[k + 8], s[k + 16]);
+                        for (int k = 0; k < 8; ++k) {
+                            mx[k] = max3(s[k], s[k + 8], s[k + 16]);
 #pragma unroll
-                        for (int j = 24; j < 128; j += 16) mx[k] = max3(mx[k], s[k + j], s[k + j + 8]);
+                            for (int j = 24; j < 128; j += 16) mx[k] = max3(mx[k], s[k + j], s[k + j + 8]);
+                        }
+                        tmax = a_mul * max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]),
+                                            fmaxf(mx[6], mx[7]));
                     }
-                    const float tmax = a_mul * max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]),
-                                                    fmaxf(mx[6], mx[7]));
                     const float m_new = fmaxf(m_ref, tmax);
                     const bool need = (m_ref != -INFINITY) && (m_new > m_ref + 8.f);
                     if (m_ref == -INFINITY) m_ref = m_new;
@@ -681,19 +694,37 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     const float2 nm2 = make_float2(-m_use, -m_use);
                     float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                     make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    if (fused) {
+                        const float2 A = make_float2(cA, cA), B = make_float2(cB, cB);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t pk[32];
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t pk[32];
 #pragma unroll
-                        for (int j = 0; j < 64; j += 2) {
-                            const int jj = hh * 64 + j;
-                            const float2 x2 = ffma2(make_float2(s[jj], s[jj + 1]), am2, nm2);
-                            const float2 e2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
-                            ls[(j >> 1) & 3] = fadd2(ls[(j >> 1) & 3], e2);
-                            pk[j >> 1] = pack_bf16x2(e2.x, e2.y);
+                            for (int j = 0; j < 64; j += 2) {
+                                const int jj = hh * 64 + j;
+                                const float2 v = make_float2(s[jj], s[jj + 1]);
+                                const float2 x2 = ffma2(v, ffma2(fmul2(v, v), B, A), nm2);
+                                const float2 e2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
+                                ls[(j >> 1) & 3] = fadd2(ls[(j >> 1) & 3], e2);
+                                pk[j >> 1] = pack_bf16x2(e2.x, e2.y);
+                            }
+                            tmem_st32(lane_base + s_col + hh * 32, pk);
                         }
-                        // P elements 64hh..64hh+63 -> columns [32hh, 32hh+32), already read
-                        tmem_st32(lane_base + s_col + hh * 32, pk);
+                    } else {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t pk[32];
+#pragma unroll
+                            for (int j = 0; j < 64; j += 2) {
+                                const int jj = hh * 64 + j;
+                                const float2 x2 = ffma2(make_float2(s[jj], s[jj + 1]), am2, nm2);
+                                const float2 e2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
+                                ls[(j >> 1) & 3] = fadd2(ls[(j >> 1) & 3], e2);
+                                pk[j >> 1] = pack_bf16x2(e2.x, e2.y);
+                            }
+                            // P elements 64hh..64hh+63 -> columns [32hh, 32hh+32), already read
+                            tmem_st32(lane_base + s_col + hh * 32, pk);
+                        }
                     }
                     const float2 l01 = fadd2(ls[0], ls[1]), l23 = fadd2(ls[2], ls[3]);
                     const float2 l03 = fadd2(l01, l23);
