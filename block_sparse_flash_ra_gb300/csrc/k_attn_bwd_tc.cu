@@ -230,7 +230,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
         } else if (warp == kMmaWarp) {
             // ---------------------------------------------------------- MMA issuer
-            if (lane == 0) {
+            // The whole warp runs the issue loop, converged: every lane waits on
+            // the barriers, and one lane, chosen by elect.sync, issues each
+            // product, copy and commit.
+            {
+                auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
+                    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+                };
                 const uint32_t k_base = smem_u32(smem + C::kKOff);
                 const uint32_t v_base = smem_u32(smem + C::kVOff);
                 uint32_t n = 0, uk = 0;
@@ -239,7 +245,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     return smem_u32(smem + C::kStageOff + (step % C::kStages) * C::kStageBytes);
                 };
                 auto wait_stage = [&](uint32_t step) -> bool {
-                    if (!mbar_wait(bars.st_full + step % C::kStages, (step / C::kStages) & 1, ctx)) return false;
+                    if (!wait_w(bars.st_full + step % C::kStages, (step / C::kStages) & 1)) return false;
                     tc_fence_after();
                     return true;
                 };
@@ -251,9 +257,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        mma_ss(tmem, kd + o, qd + o, kIdescT, kk > 0 ? 1u : 0u);
+                        mma_ss_w(tmem, kd + o, qd + o, kIdescT, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bars.s_full);
+                    tc_commit_w(bars.s_full);
                 };
                 // dP^T = V dO^T into columns [128,256)
                 auto issue_dp = [&](uint32_t do_base) {
@@ -261,9 +267,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        mma_ss(tmem + C::kColDP, vd + o, dd + o, kIdescT, kk > 0 ? 1u : 0u);
+                        mma_ss_w(tmem + C::kColDP, vd + o, dd + o, kIdescT, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bars.dp_full);
+                    tc_commit_w(bars.dp_full);
                 };
                 // Issue order per step n (each product overlaps a softmax phase):
                 //   dP(n) | phase A(n);  dV(n), S(n+1) | phase B(n);
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (u >= U) continue;
                     const ColUnit x = col_unit(p, u);
                     if (x.cnt == 0) continue;
-                    if (!(ok = mbar_wait(bars.kv_full, uk & 1, ctx))) break;
+                    if (!(ok = wait_w(bars.kv_full, uk & 1))) break;
                     tc_fence_after();
                     ++uk;
                     const int steps = x.gc * x.cnt;
@@ -286,12 +292,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const uint32_t do_base = q_base + C::kTileBytes;
                         issue_dp(do_base);
                         // dV += P^T dO   (A = P^T from TMEM, B = dO as a K=q x N=D MN-major tile)
-                        if (!(ok = mbar_wait(bars.p_ready, n & 1, ctx))) break;
+                        if (!(ok = wait_w(bars.p_ready, n & 1))) break;
                         tc_fence_after();
                         const uint64_t dmn = sdesc_sw128(do_base, 16384, 1024);
     #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts(tmem + C::kColDV, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
+                            mma_ts_w(tmem + C::kColDV, tmem + kk * 8 + (kk >= 4 ? 32 : 0),
                                    dmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                    (i > 0 || kk > 0) ? 1u : 0u);
                         if (i + 1 < steps) {
@@ -299,21 +305,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             issue_s(stage_base(n + 1));
                         }
                         // dK += dS^T Q
-                        if (!(ok = mbar_wait(bars.ds_ready, n & 1, ctx))) break;
+                        if (!(ok = wait_w(bars.ds_ready, n & 1))) break;
                         tc_fence_after();
                         const uint64_t qmn = sdesc_sw128(q_base, 16384, 1024);
     #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
+                            mma_ts_w(tmem + C::kColDK, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
                                    qmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                    (i > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(bars.st_empty + n % C::kStages);
+                        tc_commit_w(bars.st_empty + n % C::kStages);
                     }
                     if (!ok) break;
-                    tc_commit(bars.kv_empty);
-                    tc_commit(bars.acc_ready);
+                    tc_commit_w(bars.kv_empty);
+                    tc_commit_w(bars.acc_ready);
                 }
-                tc_commit(bars.drain);
+                tc_commit_w(bars.drain);
                 wait_drain(bars.drain, 0, kDrainNs);
             }
         }
@@ -777,7 +783,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
         } else if (warp == kMmaWarp) {
             // ---------------------------------------------------------- MMA issuer
-            if (lane == 0) {
+            // The whole warp runs the issue loop, converged: every lane waits on
+            // the barriers, and one lane, chosen by elect.sync, issues each
+            // product, copy and commit.
+            {
+                auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
+                    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+                };
                 const uint32_t k_base = smem_u32(smem + C::kKOff);
                 const uint32_t v_base = smem_u32(smem + C::kVOff);
                 const uint64_t qd = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
@@ -788,29 +800,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // from TMEM (16-column K chunk kk at column 8 kk), B = the K tile
                 // descriptors are built once per operand; an offset o adds o / 16
                 auto issue_s = [&](uint32_t t) -> bool {
-                    if (!mbar_wait(bars.k_full + t % C::kKStages, (t / C::kKStages) & 1, ctx)) return false;
+                    if (!wait_w(bars.k_full + t % C::kKStages, (t / C::kKStages) & 1)) return false;
                     tc_fence_after();
                     const uint64_t kd = sdesc_sw128(k_base + (t % C::kKStages) * C::kTileBytes, 16, 1024);
     #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        mma_ts(tmem + C::kColS, tmem + C::kColQA + kk * 8, kd + o, kIdescT, kk > 0 ? 1u : 0u);
+                        mma_ts_w(tmem + C::kColS, tmem + C::kColQA + kk * 8, kd + o, kIdescT, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bars.s_full);
+                    tc_commit_w(bars.s_full);
                     return true;
                 };
                 // dP = dO V^T of tile t into [128,256); V's stage is free after it
                 auto issue_dp = [&](uint32_t t) -> bool {
-                    if (!mbar_wait(bars.v_full + t % C::kVStages, (t / C::kVStages) & 1, ctx)) return false;
+                    if (!wait_w(bars.v_full + t % C::kVStages, (t / C::kVStages) & 1)) return false;
                     tc_fence_after();
                     const uint64_t vd = sdesc_sw128(v_base + (t % C::kVStages) * C::kTileBytes, 16, 1024);
     #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        mma_ts(tmem + C::kColDP, tmem + C::kColDOA + kk * 8, vd + o, kIdescT, kk > 0 ? 1u : 0u);
+                        mma_ts_w(tmem + C::kColDP, tmem + C::kColDOA + kk * 8, vd + o, kIdescT, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bars.dp_full);
-                    tc_commit(bars.v_empty + t % C::kVStages);
+                    tc_commit_w(bars.dp_full);
+                    tc_commit_w(bars.v_empty + t % C::kVStages);
                     return true;
                 };
                 // Issue order per tile g: S(g+1) as soon as phase A(g) has read S(g);
@@ -827,38 +839,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // dimension per copy, at the K-chunk offsets the products use.
                     // No product still reads the previous unit's: its last dP had
                     // completed before its last phase B began.
-                    if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                    if (!(ok = wait_w(bars.q_full, uq & 1))) break;
                     tc_fence_after();
                     ++uq;
     #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        tmem_cp_128x256b(tmem + C::kColQA + kk * 8, qd + o);
-                        tmem_cp_128x256b(tmem + C::kColDOA + kk * 8, dod + o);
+                        tmem_cp_128x256b_w(tmem + C::kColQA + kk * 8, qd + o);
+                        tmem_cp_128x256b_w(tmem + C::kColDOA + kk * 8, dod + o);
                     }
-                    tc_commit(bars.q_empty); // the tiles' shared memory is free once the copies are done
+                    tc_commit_w(bars.q_empty); // the tiles' shared memory is free once the copies are done
                     if (!(ok = issue_s(g))) break;
                     if (!(ok = issue_dp(g))) break;
                     for (int e = 0; e < x.cnt; ++e, ++g) {
-                        if (!(ok = mbar_wait(bars.s_free, g & 1, ctx))) break;
+                        if (!(ok = wait_w(bars.s_free, g & 1))) break;
                         if (e + 1 < x.cnt && !(ok = issue_s(g + 1))) break;
                         // dQ += dS K   (A = dS from TMEM, B = K as a K=kv x N=D MN-major tile)
-                        if (!(ok = mbar_wait(bars.ds_ready, g & 1, ctx))) break;
+                        if (!(ok = wait_w(bars.ds_ready, g & 1))) break;
                         tc_fence_after();
                         const int sk = g % C::kKStages;
                         const uint64_t kmn = sdesc_sw128(k_base + sk * C::kTileBytes, 16384, 1024);
     #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts(tmem + C::kColDQ, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
+                            mma_ts_w(tmem + C::kColDQ, tmem + C::kColDP + kk * 8 + (kk >= 4 ? 32 : 0),
                                    kmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                    (e > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(bars.k_empty + sk);
+                        tc_commit_w(bars.k_empty + sk);
                         if (e + 1 < x.cnt && !(ok = issue_dp(g + 1))) break;
                     }
                     if (!ok) break;
-                    tc_commit(bars.acc_ready);
+                    tc_commit_w(bars.acc_ready);
                 }
-                tc_commit(bars.drain);
+                tc_commit_w(bars.drain);
                 wait_drain(bars.drain, 0, kDrainNs);
             }
         }

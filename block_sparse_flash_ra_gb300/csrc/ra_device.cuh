@@ -155,7 +155,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
         : "memory");
 }
 
-// D(tmem) (+)= A(smem desc) x B(smem desc)^T, kind::f16 (bf16 in, fp32 acc).
 // tcgen05.cp: 128 rows x 256 bits (16 bf16) of a shared-memory matrix, named
 // by a matrix descriptor as an MMA operand is, into 128 lanes x 8 columns of
 // TMEM (row r -> lane r, the 16 elements packed two per column).  Issued by
@@ -165,6 +164,7 @@ __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
     asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// D(tmem) (+)= A(smem desc) x B(smem desc)^T, kind::f16 (bf16 in, fp32 acc).
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)
 {
@@ -182,6 +182,45 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same four issued by a whole, converged warp: every lane executes the
+// instruction and elect.sync lets one lane issue it.  An issue loop that the
+// whole warp runs, barrier waits included, stays converged; one thread
+// looping on barrier waits inside a lane-0 branch does not, and a clock
+// probe on this GPU issued 128x128x16 products at 83-101 cycles each that way
+// against 64-67 from a converged warp with the same waits.
+__device__ __forceinline__ void tc_commit_w(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_cp_128x256b_w(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
