@@ -216,8 +216,14 @@ __global__ void __launch_bounds__(kThreads64, 1)
                     if (st_issued[s]) wait_drain(bars.st_full + s, (st_issued[s] - 1) & 1, kDrainNs);
                 if (uk) wait_drain(bars.kv_full, (uk - 1) & 1, kDrainNs);
             }
-        } else if (warp == kMma64 && lane == 0) {
+        } else if (warp == kMma64) {
             // ---------------------------------------------------------- MMA issuer
+            // The whole warp runs the issue loop, converged: every lane waits on
+            // the barriers, and one lane, chosen by elect.sync, issues each
+            // product and commit.
+            auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+            };
             // descriptors built once per operand; an offset o adds o / 16
             const uint64_t kd = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
             const uint64_t vd = sdesc_sw128(smem_u32(smem + C::kVOff), 16, 1024);
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(kThreads64, 1)
             uint32_t n = 0, uk = 0;
             bool ok = true;
             auto wait_stage = [&](uint32_t step) -> bool {
-                if (!mbar_wait(bars.st_full + step % kStages64, (step / kStages64) & 1, ctx)) return false;
+                if (!wait_w(bars.st_full + step % kStages64, (step / kStages64) & 1)) return false;
                 tc_fence_after();
                 return true;
             };
@@ -238,23 +244,23 @@ __global__ void __launch_bounds__(kThreads64, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
                     const uint32_t ob = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + buf * 64, kd + oa, qd + ob, C::kIdescT, kk > 0 ? 1u : 0u);
+                    mma_ss_w(tmem + buf * 64, kd + oa, qd + ob, C::kIdescT, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bars.s_full + buf);
+                tc_commit_w(bars.s_full + buf);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
                     const uint32_t ob = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + C::kColDP + buf * 64, vd + oa, dd + ob, C::kIdescT, kk > 0 ? 1u : 0u);
+                    mma_ss_w(tmem + C::kColDP + buf * 64, vd + oa, dd + ob, C::kIdescT, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bars.dp_full + buf);
+                tc_commit_w(bars.dp_full + buf);
             };
             for (int r = 0; ok && r * Gd < U; ++r) {
                 const int u = unit_index(r, blockIdx.x, Gd);
                 if (u >= U) continue;
                 const Col64 x = col64_of(p, u);
                 if (x.cnt == 0) continue;
-                if (!(ok = mbar_wait(bars.kv_full, uk & 1, ctx))) break;
+                if (!(ok = wait_w(bars.kv_full, uk & 1))) break;
                 tc_fence_after();
                 ++uk;
                 const int steps = x.gc * x.cnt;
@@ -266,24 +272,24 @@ __global__ void __launch_bounds__(kThreads64, 1)
                     const uint32_t buf = n & 1, ph = (n >> 1) & 1;
                     const uint32_t sb = stage0 + (n % kStages64) * C::kStageBytes;
                     // dV += P^T dO   (A = P^T from TMEM, B = dO as a K=q x N=D MN-major block)
-                    if (!(ok = mbar_wait(bars.p_ready + buf, ph, ctx))) break;
+                    if (!(ok = wait_w(bars.p_ready + buf, ph))) break;
                     tc_fence_after();
                     const uint64_t dmn = sdesc_sw128(sb + kBlk, 8192, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kQB / 16; ++kk)
-                        mma_ts(tmem + C::kColDV, tmem + buf * 64 + kk * 8,
+                        mma_ts_w(tmem + C::kColDV, tmem + buf * 64 + kk * 8,
                                dmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                (i > 0 || kk > 0) ? 1u : 0u);
                     // dK += dS^T Q
-                    if (!(ok = mbar_wait(bars.ds_ready + buf, ph, ctx))) break;
+                    if (!(ok = wait_w(bars.ds_ready + buf, ph))) break;
                     tc_fence_after();
                     const uint64_t qmn = sdesc_sw128(sb, 8192, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kQB / 16; ++kk)
-                        mma_ts(tmem + C::kColDK, tmem + C::kColDP + buf * 64 + kk * 8,
+                        mma_ts_w(tmem + C::kColDK, tmem + C::kColDP + buf * 64 + kk * 8,
                                qmn + (uint32_t)((kk * 2048) >> 4), C::kIdescAcc,
                                (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bars.st_empty + n % kStages64);
+                    tc_commit_w(bars.st_empty + n % kStages64);
                     // the next products of this buffer pair: step n + 2
                     if (i + 2 < steps) {
                         if (!(ok = wait_stage(n + 2))) break;
@@ -291,10 +297,10 @@ __global__ void __launch_bounds__(kThreads64, 1)
                     }
                 }
                 if (!ok) break;
-                tc_commit(bars.kv_empty);
-                tc_commit(bars.acc_ready);
+                tc_commit_w(bars.kv_empty);
+                tc_commit_w(bars.acc_ready);
             }
-            tc_commit(bars.drain);
+            tc_commit_w(bars.drain);
             wait_drain(bars.drain, 0, kDrainNs);
         }
     } else {

@@ -288,8 +288,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 }
                 if (uq) wait_drain(bars.q_full, (uq - 1) & 1, kDrainNs);
             }
-        } else if (warp == kMmaWarp2 && lane == 0) {
+        } else if (warp == kMmaWarp2) {
             // ------------------------------------------------------------ MMA issuer
+            // The whole warp runs the issue loop, converged: every lane waits on
+            // the barriers, and one lane, chosen by elect.sync, issues each
+            // product and commit.
+            auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+            };
             // Shared-memory descriptors are built once; an operand at byte
             // offset o from a base has the base's descriptor plus o / 16 (the
             // start-address field cannot carry: shared memory is < 256 KB).
@@ -305,14 +311,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint64_t kd_ = dk + (uint64_t)(KS) * kStageStep;                                     \
         _Pragma("unroll") for (int kk = 0; kk < kD2 / 16; ++kk) {                                  \
             const uint64_t o_ = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);              \
-            mma_ss(tmem + (TCOL), (QD) + o_, kd_ + o_, C::kIdescQK, kk > 0 ? 1u : 0u);             \
+            mma_ss_w(tmem + (TCOL), (QD) + o_, kd_ + o_, C::kIdescQK, kk > 0 ? 1u : 0u);             \
         }                                                                                          \
     } while (0)
 #define RA_ISSUE_PV(H, VS, FIRST)                                                                  \
     do {                                                                                           \
         const uint64_t vd_ = dv + (uint64_t)(VS) * kStageStep;                                     \
         _Pragma("unroll") for (int kk = 0; kk < kTile / 16; ++kk)                                  \
-            mma_ts(tmem + C::kColO + (H) * 128, tmem + (H) * 128 + kk * 8,                         \
+            mma_ts_w(tmem + C::kColO + (H) * 128, tmem + (H) * 128 + kk * 8,                         \
                    vd_ + (uint64_t)((kk * 2048) >> 4), C::kIdescPV, (kk > 0 || !(FIRST)) ? 1u : 0u); \
     } while (0)
             for (int r = 0; ok && r * G < U; ++r) {
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 if (u >= U) continue;
                 const Unit2 x = unit2_of(p, u);
                 if (x.cnt == 0) continue;
-                if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                if (!(ok = wait_w(bars.q_full, uq & 1))) break;
                 ++uq;
                 RingWalk it;
                 it.start(p, x);
@@ -329,16 +335,16 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 bool cf, cl;
                 it.get(x, kt, cf, cl, lo);
                 uint32_t ks = gk % kStages2;
-                if (!(ok = mbar_wait(bars.k_full + ks, (gk / kStages2) & 1, ctx))) break;
+                if (!(ok = wait_w(bars.k_full + ks, (gk / kStages2) & 1))) break;
                 tc_fence_after();
                 RA_ISSUE_S(dq0, 0, ks);
-                tc_commit(bars.s_full + 0);
+                tc_commit_w(bars.s_full + 0);
                 RA_ISSUE_S(dq1, 128, ks);
-                tc_commit(bars.s_full + 1);
-                tc_commit(bars.k_empty + ks);
+                tc_commit_w(bars.s_full + 1);
+                tc_commit_w(bars.k_empty + ks);
                 ++gk;
                 int done = 1;
-                if (done == x.cnt) tc_commit(bars.q_empty);
+                if (done == x.cnt) tc_commit_w(bars.q_empty);
                 while (true) {
                     // the next tile in ring order, if any
                     const int cur_t = it.t;
@@ -354,41 +360,41 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     const uint32_t vs = gv % kStages2;
                     ks = gk % kStages2;
                     // head A: PV of this tile, then S of the next (its S buffer held P)
-                    if (!(ok = mbar_wait(bars.p_full + 0, gp & 1, ctx))) break;
-                    if (!(ok = mbar_wait(bars.v_full + vs, (gv / kStages2) & 1, ctx))) break;
-                    if (cf && !(ok = mbar_wait(bars.o_empty + 0, (n_oe & 1) ^ 1, ctx))) break;
+                    if (!(ok = wait_w(bars.p_full + 0, gp & 1))) break;
+                    if (!(ok = wait_w(bars.v_full + vs, (gv / kStages2) & 1))) break;
+                    if (cf && !(ok = wait_w(bars.o_empty + 0, (n_oe & 1) ^ 1))) break;
                     tc_fence_after();
                     if (cf) RA_ISSUE_PV(0, vs, true); else RA_ISSUE_PV(0, vs, false);
-                    if (cl) tc_commit(bars.o_full + 0);
+                    if (cl) tc_commit_w(bars.o_full + 0);
                     if (has_next) {
-                        if (!(ok = mbar_wait(bars.k_full + ks, (gk / kStages2) & 1, ctx))) break;
+                        if (!(ok = wait_w(bars.k_full + ks, (gk / kStages2) & 1))) break;
                         tc_fence_after();
                         RA_ISSUE_S(dq0, 0, ks);
-                        tc_commit(bars.s_full + 0);
+                        tc_commit_w(bars.s_full + 0);
                     }
                     // head B, the same
-                    if (!(ok = mbar_wait(bars.p_full + 1, gp & 1, ctx))) break;
-                    if (cf && !(ok = mbar_wait(bars.o_empty + 1, (n_oe & 1) ^ 1, ctx))) break;
+                    if (!(ok = wait_w(bars.p_full + 1, gp & 1))) break;
+                    if (cf && !(ok = wait_w(bars.o_empty + 1, (n_oe & 1) ^ 1))) break;
                     tc_fence_after();
                     if (cf) RA_ISSUE_PV(1, vs, true); else RA_ISSUE_PV(1, vs, false);
-                    tc_commit(bars.v_empty + vs);
-                    if (cl) tc_commit(bars.o_full + 1);
+                    tc_commit_w(bars.v_empty + vs);
+                    if (cl) tc_commit_w(bars.o_full + 1);
                     if (cf) ++n_oe;
                     ++gv;
                     ++gp;
                     if (!has_next) break;
                     RA_ISSUE_S(dq1, 128, ks);
-                    tc_commit(bars.s_full + 1);
-                    tc_commit(bars.k_empty + ks);
+                    tc_commit_w(bars.s_full + 1);
+                    tc_commit_w(bars.k_empty + ks);
                     ++gk;
-                    if (++done == x.cnt) tc_commit(bars.q_empty);
+                    if (++done == x.cnt) tc_commit_w(bars.q_empty);
                     cf = nf;
                     cl = nl;
                 }
             }
 #undef RA_ISSUE_S
 #undef RA_ISSUE_PV
-            tc_commit(bars.drain);
+            tc_commit_w(bars.drain);
             wait_drain(bars.drain, 0, kDrainNs);
         }
     } else if (warp >= kCorrWarp0_2) {

@@ -375,7 +375,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------------ MMA issuer
-            if (lane == 0) {
+            // The whole warp runs the issue loop, converged: every lane waits on
+            // the barriers, and one lane, chosen by elect.sync, issues each
+            // product and commit.
+            {
+                auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
+                    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx)) != 0;
+                };
                 // descriptors are built once per operand; an offset o adds o / 16
                 const uint64_t qd = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
                 const uint64_t kd0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
@@ -388,12 +394,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 // PV product of tile pg; `first` / `last`: the tile opens / closes its shard
                 auto issue_pv = [&](uint32_t pg, bool first, bool last) -> bool {
                     const int sb = pg & 1;
-                    if (!mbar_wait(bars.p_full + sb, (pg >> 1) & 1, ctx)) return false;
+                    if (!wait_w(bars.p_full + sb, (pg >> 1) & 1)) return false;
                     const int st = pg % C::kVStages;
-                    if (!mbar_wait(bars.v_full + st, (pg / C::kVStages) & 1, ctx)) return false;
+                    if (!wait_w(bars.v_full + st, (pg / C::kVStages) & 1)) return false;
                     // the shard's first product overwrites O_acc: the correction
                     // warps must have read the previous shard's
-                    if (first && !mbar_wait(bars.o_empty, (n_oe++ & 1) ^ 1, ctx)) return false;
+                    if (first && !wait_w(bars.o_empty, (n_oe++ & 1) ^ 1)) return false;
                     tc_fence_after();
                     const uint64_t vd = vd0 + (uint64_t)(st * kStageStep);
 #pragma unroll
@@ -402,12 +408,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         // P of kv rows 16kk..16kk+15: the half of warps 0-3 (kk < 4) sits
                         // in columns [0,32) of the S buffer, the other half in [64,96)
                         const uint32_t acol = sb * 128 + kk * 8 + (kk >= 4 ? 32 : 0);
-                        mma_ts(tmem + C::kColO, tmem + acol, bdesc, C::kIdescPV,
+                        mma_ts_w(tmem + C::kColO, tmem + acol, bdesc, C::kIdescPV,
                                (kk > 0 || !first) ? 1u : 0u);
                     }
-                    tc_commit(bars.v_empty + st);
-                    tc_commit(bars.pv_done);
-                    if (last) tc_commit(bars.o_full);
+                    tc_commit_w(bars.v_empty + st);
+                    tc_commit_w(bars.pv_done);
+                    if (last) tc_commit_w(bars.o_full);
                     return true;
                 };
                 for (int r = 0; ok && r * G < U; ++r) {
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     if (u >= U) continue;
                     const Unit x = unit_of(p, u);
                     if (x.cnt == 0) continue;
-                    if (!(ok = mbar_wait(bars.q_full, uq & 1, ctx))) break;
+                    if (!(ok = wait_w(bars.q_full, uq & 1))) break;
                     tc_fence_after();
                     ++uq;
                     int done = 0;
@@ -424,18 +430,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         shard_range(p, x, (x.dev - t + p.N) % p.N, lo, hi);
                         for (int e = lo; e < hi; ++e) {
                             const int st = g % C::kKStages;
-                            if (!(ok = mbar_wait(bars.k_full + st, (g / C::kKStages) & 1, ctx))) break;
+                            if (!(ok = wait_w(bars.k_full + st, (g / C::kKStages) & 1))) break;
                             tc_fence_after();
                             const int sb = g & 1;
                             const uint64_t kd = kd0 + (uint64_t)(st * kStageStep);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
                                 const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                                mma_ss(tmem + sb * 128, qd + o, kd + o, C::kIdescQK, kk > 0 ? 1u : 0u);
+                                mma_ss_w(tmem + sb * 128, qd + o, kd + o, C::kIdescQK, kk > 0 ? 1u : 0u);
                             }
-                            tc_commit(bars.k_empty + st);
-                            tc_commit(bars.s_full + sb);
-                            if (++done == x.cnt) tc_commit(bars.q_empty);
+                            tc_commit_w(bars.k_empty + st);
+                            tc_commit_w(bars.s_full + sb);
+                            if (++done == x.cnt) tc_commit_w(bars.q_empty);
                             if (have_prev && !(ok = issue_pv(prev_g, prev_first, prev_last))) break;
                             have_prev = true;
                             prev_g = g;
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 if (ok && have_prev) ok = issue_pv(prev_g, prev_first, prev_last);
                 // all issued MMAs must finish before TMEM is released
-                tc_commit(bars.drain);
+                tc_commit_w(bars.drain);
                 wait_drain(bars.drain, 0, kDrainNs);
             }
         }
