@@ -21,7 +21,8 @@
 //               heads and the unit's bf16 output and lse
 //   warp 12     TMA producer: Q of both heads once per unit, K and V tiles
 //               into 2-stage rings
-//   warp 13     TMEM allocator and single-thread MMA issuer
+//   warp 13     TMEM allocator and MMA issuer (the whole warp runs the issue
+//               loop; one elected lane issues each product)
 //   warps 14-15 no role (setmaxnreg donors)
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384),
 // O_B [384,512); P (bf16) overwrites the first 64 columns of its S buffer.
@@ -29,7 +30,7 @@
 // head's softmax runs, the tensor pipe computes the other head's products,
 // and the two softmax warpgroups interleave their exponent phases on the
 // MUFU units instead of running them at the same time.  S_X(g+1) completing
-// implies PV_X(g) has completed (one issuing thread, in order), so a softmax
+// implies PV_X(g) has completed (one issuing lane, in order), so a softmax
 // warp never waits for a PV product separately.
 // The running output O_run of both heads lives in the caller's workspace
 // (fp32, one slot per CTA): at a shard end the correction warps first copy

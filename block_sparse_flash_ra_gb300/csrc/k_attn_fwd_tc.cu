@@ -26,7 +26,8 @@
 //               overlapped with the softmax of the next shard's tiles
 //   warp 12     TMA producer: Q once per work unit, K and V tiles into rings
 //               of shared-memory stages (2 for K, 3 for V at D = 128)
-//   warp 13     TMEM allocator and single-thread MMA issuer
+//   warp 13     TMEM allocator and MMA issuer (the whole warp runs the issue
+//               loop; one elected lane issues each product)
 //   warps 14-15 no role (with warps 12-13 they form the warpgroup that hands
 //               registers to the softmax warpgroups through setmaxnreg)
 // TMEM (512 columns x 128 lanes, fp32):
