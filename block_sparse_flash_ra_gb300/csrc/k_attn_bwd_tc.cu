@@ -112,11 +112,20 @@ struct ColUnit {
 __device__ __forceinline__ ColUnit col_unit(const Problem &p, int u)
 {
     ColUnit x;
-    const int per = p.Hkv * p.hsplit;
-    x.col = p.bwd_order[u / per];
-    const int r = u - (u / per) * per;
-    x.hkv = r / p.hsplit;
-    x.chunk = r - x.hkv * p.hsplit;
+    // waves of two kv heads: all columns (longest first) of kv heads 2w and
+    // 2w + 1 before the next pair, so that the Q / dO rows read at a time
+    // belong to 2 G query heads (when a wave holds at least three units per
+    // CTA; smaller waves would leave CTAs on the same few tiles at once)
+    int hpw = (p.Hkv % 2 == 0) ? 2 : 1;
+    if (p.B * p.nk * hpw * p.hsplit < 3 * (int)gridDim.x) hpw = p.Hkv;
+    const int per = hpw * p.hsplit;
+    const int wave_units = p.B * p.nk * per;
+    const int w = u / wave_units;
+    const int rr = u - w * wave_units;
+    x.col = p.bwd_order[rr / per];
+    const int r = rr - (rr / per) * per;
+    x.hkv = w * hpw + r / p.hsplit;
+    x.chunk = r - (r / p.hsplit) * p.hsplit;
     x.gc = p.G / p.hsplit;
     x.h0 = x.hkv * p.G + x.chunk * x.gc;
     x.b = x.col / p.nk;
@@ -668,8 +677,17 @@ struct RowUnit {
 __device__ __forceinline__ RowUnit row_unit(const Problem &p, int u)
 {
     RowUnit x;
-    x.row = p.fwd_order[u / p.Hq];
-    x.h = u % p.Hq;
+    // waves of the query heads of two kv heads: all rows (longest first) of
+    // those 2 G heads before the next, so that the K / V rows read at a time
+    // belong to two kv heads (when a wave holds at least three units per CTA;
+    // smaller waves would leave CTAs on the same few tiles at once)
+    int hpw = (p.Hkv % 2 == 0) ? 2 * p.G : p.G;
+    if (p.B * p.nq * hpw < 3 * (int)gridDim.x) hpw = p.Hq;
+    const int wave_units = p.B * p.nq * hpw;
+    const int w = u / wave_units;
+    const int rr = u - w * wave_units;
+    x.row = p.fwd_order[rr / hpw];
+    x.h = w * hpw + (rr - (rr / hpw) * hpw);
     x.b = x.row / p.nq;
     x.qt = x.row - x.b * p.nq;
     x.cnt = p.fwd_cnt[x.row];

@@ -104,10 +104,18 @@ struct Unit2 {
 
 __device__ __forceinline__ Unit2 unit2_of(const Problem &p, int u)
 {
-    const int pairs = p.Hq >> 1;
+    // waves of the head pairs of two kv heads: all rows (longest first) of
+    // those pairs before the next, so that the K / V rows read at a time
+    // belong to two kv heads (when a wave holds at least three units per CTA;
+    // smaller waves would leave CTAs on the same few tiles at once)
+    int ppw = (p.Hkv % 2 == 0) ? p.G : p.G / 2;
+    if (p.B * p.nq * ppw < 3 * (int)gridDim.x) ppw = p.Hq >> 1;
+    const int wave_units = p.B * p.nq * ppw;
+    const int w = u / wave_units;
+    const int rr = u - w * wave_units;
     Unit2 x;
-    x.row = p.fwd_order[u / pairs];
-    x.h0 = 2 * (u % pairs);
+    x.row = p.fwd_order[rr / ppw];
+    x.h0 = 2 * (w * ppw + (rr - (rr / ppw) * ppw));
     x.b = x.row / p.nq;
     x.qt = x.row - x.b * p.nq;
     x.cnt = p.fwd_cnt[x.row];
