@@ -24,6 +24,12 @@
 //   B: K_hi | K_lo of the same pass, then V^T (D rows x 128 keys)
 // TMEM: S [0,128), the tile's P V [128,128+D), the running output
 // O_run [256,256+D).
+//
+// Ring step (p.run_out set, one key/value chunk): the running pair starts
+// from run_out / run_lse (unless step_first, then (0, -inf)), the sinks count
+// only with step_sink, and the merged pair goes back to run_out / run_lse --
+// and to `out` as well when it is given (the last step's result in the query
+// dtype, which here is fp32).
 #include <math.h>
 
 #include "ra_sched.cuh"
@@ -131,8 +137,22 @@ __global__ void __launch_bounds__(128, 1) fwd_f32tc_kernel(Problem p, const floa
         return r;
     };
 
+    const bool stepm = p.run_out != nullptr;
+    const size_t row_off = (((size_t)b * p.Lq + i) * p.Hq + h) * D;
     float lse_run = -INFINITY;
     bool orun_set = false; // O_run holds real data (else logically zero)
+    if (stepm && !p.step_first) {
+        // the running pair of the ring so far
+        lse_run = p.run_lse[((size_t)b * p.Hq + h) * p.Lq + i];
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t run[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) run[c] = __float_as_uint(p.run_out[row_off + c0 + c]);
+            tmem_st32(lane_base + kColRun + c0, run);
+        }
+        tmem_st_wait();
+        orun_set = true;
+    }
     for (int step = 0; ok && step < p.N; ++step) {
         const int src = (dev - step + p.N) % p.N;
         const int lo_kt = src * p.tk, hi_kt = lo_kt + p.tk;
@@ -237,7 +257,7 @@ __global__ void __launch_bounds__(128, 1) fwd_f32tc_kernel(Problem p, const floa
             tc_fence_after();
         }
         if (!ok) break;
-        const bool sink_here = (step == 0) && p.sinks;
+        const bool sink_here = (step == 0) && p.sinks && (!stepm || p.step_sink);
         if (!any_tile && !sink_here) continue; // partial (0, -inf): merge is a no-op
         if (sink_here) {
             const float s2 = p.sinks[h] * kLog2e;
@@ -283,13 +303,18 @@ __global__ void __launch_bounds__(128, 1) fwd_f32tc_kernel(Problem p, const floa
     // before the TMEM it writes is freed
     if (!ok && t == 0) wait_drain(bar, phase ^ 1, kDrainNs);
     if (ok) {
-        float *dst = out + (((size_t)b * p.Lq + i) * p.Hq + h) * D;
+        float *dst = out ? out + row_off : nullptr;
+        float *dst_run = stepm ? p.run_out + row_off : nullptr;
         for (int c0 = 0; c0 < D; c0 += 32) {
             float run[32];
             tmem_ld32(lane_base + kColRun + c0, run);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) dst[c0 + c] = orun_set ? run[c] : 0.f;
+            for (int c = 0; c < 32; ++c) {
+                const float val = orun_set ? run[c] : 0.f;
+                if (dst) dst[c0 + c] = val;
+                if (dst_run) dst_run[c0 + c] = val;
+            }
         }
         lse[((size_t)b * p.Hq + h) * p.Lq + i] = lse_run;
     }

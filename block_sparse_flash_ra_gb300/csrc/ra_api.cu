@@ -481,8 +481,12 @@ RA_API int ra_attn_fwd_step(const ra_attn_params *p, const void *q, const void *
         return fail(RA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
     if ((rc = check_mask(p, mask))) return rc;
     if (p->D != 64 && p->D != 128) return fail(RA_ERR_UNSUPPORTED, "D must be 64 or 128 (got %d)", p->D);
-    if (p->dtype != RA_BF16)
-        return fail(RA_ERR_UNSUPPORTED, "ring steps are implemented for bf16 inputs");
+    if (out) {
+        const size_t nrun = (size_t)p->B * p->Lq * p->Hq * p->D * 4;
+        const size_t nout = nrun / (p->dtype == RA_BF16 ? 2 : 1);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(out), r = reinterpret_cast<uintptr_t>(out_run);
+        if (a < r + nrun && r < a + nout) return fail(RA_ERR_INVALID_ARG, "out overlaps out_run");
+    }
     DevCache *dc = nullptr;
     if ((rc = device_cache(&dc))) return rc;
     Problem pr = make_problem(p, mask, dc->status);
@@ -491,6 +495,19 @@ RA_API int ra_attn_fwd_step(const ra_attn_params *p, const void *q, const void *
     pr.step_sink = (flags & RA_STEP_SINKS) ? 1 : 0;
     pr.step_first = (flags & RA_STEP_FIRST) ? 1 : 0;
     cudaError_t e;
+    if (p->dtype == RA_FP32) {
+        bool &done = p->D == 64 ? dc->attr_f32tc64 : dc->attr_f32tc128;
+        if (!done) {
+            if ((e = f32tc_set_attributes(p->D)) != cudaSuccess) return cuda_fail(e, "fp32 forward attributes");
+            done = true;
+        }
+        e = launch_fwd_f32_tc(pr, static_cast<const float *>(q), static_cast<const float *>(k),
+                              static_cast<const float *>(v), static_cast<float *>(out), lse_run,
+                              reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "forward step (fp32) launch");
+        count(1);
+        return RA_OK;
+    }
     bool &done = p->D == 64 ? dc->attr_fwd64 : dc->attr_fwd128;
     if (!done) {
         if ((e = fwd_tc_set_attributes(p->D)) != cudaSuccess) return cuda_fail(e, "forward attributes");
@@ -631,6 +648,27 @@ int bwd_common(const ra_attn_params *p, const void *const *ptrs, int nptrs,
     return RA_OK;
 }
 
+// fp32 inputs of the backward: bf16 copies of q, k, v, dout in the front of
+// ws (bwd_f32_copy_bytes of it), each rounded to nearest once; out16 gets
+// the copies' addresses in that order
+int bwd_f32_copies(const ra_attn_params *p, const void *q, const void *k, const void *v,
+                   const void *dout, void *ws, const void **out16, cudaStream_t s)
+{
+    const size_t nq = (size_t)p->B * p->Lq * p->Hq * p->D, nk = (size_t)p->B * p->Lkv * p->Hkv * p->D;
+    uint8_t *cb = static_cast<uint8_t *>(ws);
+    void *q16 = cb, *do16 = cb + up256(nq * 2), *k16 = cb + 2 * up256(nq * 2),
+         *v16 = cb + 2 * up256(nq * 2) + up256(nk * 2);
+    const struct { const void *src; void *dst; size_t n; } casts[4] = {
+        {q, q16, nq}, {dout, do16, nq}, {k, k16, nk}, {v, v16, nk}};
+    for (const auto &c : casts) {
+        cudaError_t e = launch_cast_from_f32(static_cast<const float *>(c.src), c.dst, c.n, RA_BF16, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 -> bf16 cast launch");
+        count(1);
+    }
+    out16[0] = q16, out16[1] = k16, out16[2] = v16, out16[3] = do16;
+    return RA_OK;
+}
+
 int bwd_tc_kernels(const ra_attn_params *p, DevCache *dc, const Problem &pr, int stages,
                    const void *q, const void *k, const void *v, const void *dout,
                    const BwdWs &w, void *dq, void *dk, void *dv, cudaStream_t s)
@@ -690,7 +728,8 @@ RA_API int ra_attn_bwd_prep(const ra_attn_params *p, const void *out, const floa
     const void *ptrs[3] = {out, lse, dout};
     DevCache *dc = nullptr;
     BwdWs w{};
-    int rc = bwd_common(p, ptrs, 3, nullptr, ws, ws_bytes, &dc, &w);
+    // fp32 out / dout too: the ring's prep (Delta and dsinks in fp32)
+    int rc = bwd_common(p, ptrs, 3, nullptr, ws, ws_bytes, &dc, &w, true, true);
     if (rc) return rc;
     if (p->sinks && !dsinks) return fail(RA_ERR_INVALID_ARG, "dsinks is NULL but sinks are given");
     const Problem pr = make_problem(p, nullptr, dc->status);
@@ -733,7 +772,7 @@ RA_API int ra_attn_bwd_dq(const ra_attn_params *p, const void *q, const void *k,
 
 RA_API int ra_attn_bwd_step(const ra_attn_params *p, const void *q, const void *k, const void *v,
                             const void *dout, const ra_block_mask *mask, float *dq_acc,
-                            float *dk_acc, float *dv_acc, const void *ws, size_t ws_bytes,
+                            float *dk_acc, float *dv_acc, void *ws, size_t ws_bytes,
                             ra_stream_t stream)
 {
     if (!mask) return fail(RA_ERR_INVALID_ARG, "mask is NULL");
@@ -743,15 +782,22 @@ RA_API int ra_attn_bwd_step(const ra_attn_params *p, const void *q, const void *
     const void *ptrs[7] = {q, k, v, dout, dq_acc, dk_acc, dv_acc};
     DevCache *dc = nullptr;
     BwdWs w{};
-    int rc = bwd_common(p, ptrs, 7, mask, const_cast<void *>(ws), ws_bytes, &dc, &w, false);
+    int rc = bwd_common(p, ptrs, 7, mask, ws, ws_bytes, &dc, &w, false, true);
     if (rc) return rc;
     Problem pr = make_problem(p, mask, dc->status);
     pr.acc_dq = dq_acc;
     pr.acc_dk = dk_acc;
     pr.acc_dv = dv_acc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (p->dtype == RA_FP32) {
+        // the products read bf16 copies of this step's q, k, v, dout, made in
+        // the front of ws (the part ra_attn_bwd_prep leaves alone)
+        const void *c16[4];
+        if ((rc = bwd_f32_copies(p, q, k, v, dout, ws, c16, s))) return rc;
+        q = c16[0], k = c16[1], v = c16[2], dout = c16[3];
+    }
     // the gradient kernels never write their bf16 outputs in this mode
-    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, dout, w, dq_acc, dk_acc, dv_acc,
-                          reinterpret_cast<cudaStream_t>(stream));
+    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q, k, v, dout, w, dq_acc, dk_acc, dv_acc, s);
 }
 
 RA_API int ra_attn_bwd(const ra_attn_params *p, const void *q, const void *k, const void *v,
@@ -789,25 +835,16 @@ int bwd_all(const ra_attn_params *p, const void *q, const void *k, const void *v
     // fp32 inputs: Delta and dsinks above come from the fp32 out / dout; the
     // tensor-core kernels read bf16 copies of q, k, v, dout made here and add
     // their fp32 gradients into dq, dk, dv, zeroed first
+    const void *c16[4];
+    if ((rc = bwd_f32_copies(p, q, k, v, dout, ws, c16, s))) return rc;
     const size_t nq = (size_t)p->B * p->Lq * p->Hq * p->D, nk = (size_t)p->B * p->Lkv * p->Hkv * p->D;
-    uint8_t *cb = static_cast<uint8_t *>(ws);
-    void *q16 = cb, *do16 = cb + up256(nq * 2), *k16 = cb + 2 * up256(nq * 2),
-         *v16 = cb + 2 * up256(nq * 2) + up256(nk * 2);
-    const struct { const void *src; void *dst; size_t n; } casts[4] = {
-        {q, q16, nq}, {dout, do16, nq}, {k, k16, nk}, {v, v16, nk}};
-    for (const auto &c : casts) {
-        if ((e = launch_cast_from_f32(static_cast<const float *>(c.src), c.dst, c.n, RA_BF16, s)) !=
-            cudaSuccess)
-            return cuda_fail(e, "fp32 -> bf16 cast launch");
-        count(1);
-    }
     const struct { void *dst; size_t n; } zero[3] = {{dq, nq}, {dk, nk}, {dv, nk}};
     for (const auto &z : zero)
         if ((e = cudaMemsetAsync(z.dst, 0, z.n * 4, s)) != cudaSuccess) return cuda_fail(e, "gradient zeroing");
     pr.acc_dq = static_cast<float *>(dq);
     pr.acc_dk = static_cast<float *>(dk);
     pr.acc_dv = static_cast<float *>(dv);
-    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, q16, k16, v16, do16, w, dq, dk, dv, s);
+    return bwd_tc_kernels(p, dc, pr, kDkdv | kDq, c16[0], c16[1], c16[2], c16[3], w, dq, dk, dv, s);
 }
 
 size_t bwd_ws_min_bytes(const ra_attn_params *p) { return bwd_ws_bytes(p, false); }

@@ -95,8 +95,8 @@ def forward_device(q, k, v, *, device_idx, n_devices, scale, causal=False, soft_
                    pad_segment_id=-1, ops=None):
     """Device ``device_idx``'s forward as a generator (see the module notes).
 
-    q (B, Lq, Hq, D), k / v (B, Lkv, Hkv, D): this device's shards (bf16,
-    contiguous).  Yields its chunk dict after each step but the last and is
+    q (B, Lq, Hq, D), k / v (B, Lkv, Hkv, D): this device's shards (bf16 or
+    fp32, contiguous).  Yields its chunk dict after each step but the last and is
     sent the left neighbour's; returns (out in q's dtype, lse fp32)."""
     ops = ops or KernelOps()
     B, Lq, Hq, D = q.shape

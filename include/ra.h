@@ -316,8 +316,10 @@ RA_API int ra_attn_bwd(const ra_attn_params *p, const void *q, const void *k, co
  *                     and dsinks (if sinks);
  *   ra_attn_bwd_dkdv  dk, dv (one work unit per kv head and 128-row kv tile);
  *   ra_attn_bwd_dq    dq     (one work unit per query head and query tile).
- * dkdv and dq read lse and Delta only through ws.  These stages take bf16
- * inputs only (RA_ERR_UNSUPPORTED for fp32); ra_attn_bwd takes both.
+ * dkdv and dq read lse and Delta only through ws.  These two stages take
+ * bf16 inputs only (RA_ERR_UNSUPPORTED for fp32); ra_attn_bwd and
+ * ra_attn_bwd_prep take both (fp32: Delta and dsinks from the fp32 out and
+ * dout, as ra_attn_bwd forms them).
  */
 RA_API int ra_attn_bwd_prep(const ra_attn_params *p, const void *out, const float *lse,
                             const void *dout, float *dsinks, void *ws, size_t ws_bytes,
@@ -377,16 +379,19 @@ enum { RA_STEP_SINKS = 1, RA_STEP_FIRST = 2 };
  * Forward step: the chunk's partial (out, lse) -- with the sinks in the
  * denominator when flags has RA_STEP_SINKS (the pages: step 0 only) -- merged
  * by _update_out_and_lse into the running pair.
- *   q (B,Lq,Hq,D), k, v (B,Lkv,Hkv,D) bf16: the local queries and the chunk.
+ *   q (B,Lq,Hq,D), k, v (B,Lkv,Hkv,D) in p->dtype (bf16, or fp32: then the
+ *   products are those of ra_attn_fwd for fp32): the local queries and the
+ *   chunk.
  *   out_run (B,Lq,Hq,D) fp32 and lse_run (B,Hq,Lq) fp32: the running pair,
  *   read and written in place; with RA_STEP_FIRST they are not read and the
  *   running pair is taken as (0, -inf) (the pages' initial state).
- *   out: NULL, or (B,Lq,Hq,D) bf16 that also receives the merged output (the
- *   final cast to the query dtype after the last step).
+ *   out: NULL, or (B,Lq,Hq,D) in p->dtype, not overlapping out_run, that also
+ *   receives the merged output (the final cast to the query dtype after the
+ *   last step).
  * lse_run ends as the natural-log lse of the rows over every chunk merged so
  * far (-inf for rows with nothing visible).
- * Errors: RA_ERR_INVALID_ARG (n_virtual_shards != 1, flags, pointers, mask),
- * RA_ERR_UNSUPPORTED (D, fp32 inputs), RA_ERR_CUDA.
+ * Errors: RA_ERR_INVALID_ARG (n_virtual_shards != 1, flags, pointers, mask,
+ * out overlapping out_run), RA_ERR_UNSUPPORTED (D), RA_ERR_CUDA.
  */
 RA_API int ra_attn_fwd_step(const ra_attn_params *p, const void *q, const void *k, const void *v,
                             const ra_block_mask *mask, int flags, float *out_run, float *lse_run,
@@ -401,12 +406,15 @@ RA_API int ra_attn_fwd_step(const ra_attn_params *p, const void *q, const void *
  * ws: the workspace ra_attn_bwd_prep filled for the same local rows (Delta,
  * -lse * log2 e); run ra_attn_bwd_prep once per backward, before the steps
  * (it also gives this device's dsinks, whose sum over the devices is the
- * pages' psum).  The query heads of a kv head are never split here.
+ * pages' psum).  The query heads of a kv head are never split here.  With
+ * fp32 inputs the step also writes bf16 copies of q, k, v, dout into the
+ * front of ws, a part ra_attn_bwd_prep does not use (so steps sharing one ws
+ * must be ordered, as the ring orders them anyway).
  * Errors: as ra_attn_bwd.
  */
 RA_API int ra_attn_bwd_step(const ra_attn_params *p, const void *q, const void *k, const void *v,
                             const void *dout, const ra_block_mask *mask, float *dq_acc,
-                            float *dk_acc, float *dv_acc, const void *ws, size_t ws_bytes,
+                            float *dk_acc, float *dv_acc, void *ws, size_t ws_bytes,
                             ra_stream_t stream);
 
 /*

@@ -60,7 +60,20 @@ CASES = {
                                            backward=True, seed=64)),
     "causal_n8_one_tile_each": dict(w=Workload("r5", 1, 1024, 2, 1, 128, n_shards=8,
                                                backward=True, seed=65)),
+    # fp32 inputs: the tiny workload's shapes (B1 Hq=Hkv=2 L256 D64, 2 shards)
+    # and a GQA one with sinks, soft cap and zigzag; the forward keeps fp32
+    # logits (tf32 hi / lo products), so it is held to the fp32 bars
+    "tiny_fp32_n2": dict(w=Workload("r6", 1, 256, 2, 2, 64, dtype="fp32", n_shards=2,
+                                    backward=True, seed=0), f32=True),
+    "fp32_gqa_sinks_cap20_zigzag_n4": dict(w=Workload("r7", 1, 1024, 4, 2, 128, dtype="fp32",
+                                                      n_shards=4, zigzag=True, soft_cap=20.0,
+                                                      sinks=True, backward=True, seed=67),
+                                           f32=True),
 }
+
+# fp32 forward bars (as for ra_attn_fwd on fp32 inputs): lse and O well inside
+# what a bf16 rounding of q and k would allow
+F32_LSE_TOL, F32_O_TOL = 1e-4, 4e-3
 
 
 def _prepare(case):
@@ -88,14 +101,14 @@ def _prepare(case):
     return w, inp, d, kw, geo, okw
 
 
-def _compare(w, inp, okw, out, lse, grads):
+def _compare(w, inp, okw, out, lse, grads, f32=False):
     q, k, v, do = (f64(inp[key]) for key in ("q", "k", "v", "dout"))
     o_ref, l_ref = oracle.attn_fwd(q, k, v, **okw)
     fin = np.isfinite(l_ref)
     assert np.array_equal(np.isfinite(lse), fin)
     if fin.any():
-        assert np.max(np.abs(lse[fin] - l_ref[fin])) <= LSE_TOL
-    assert np.max(np.abs(out - o_ref)) <= O_TOL
+        assert np.max(np.abs(lse[fin] - l_ref[fin])) <= (F32_LSE_TOL if f32 else LSE_TOL)
+    assert np.max(np.abs(out - o_ref)) <= (F32_O_TOL if f32 else O_TOL)
     dq, dk, dv, ds, _, _ = oracle.attn_bwd(q, k, v, do, **okw)
     for name, got, ref in (("dq", grads[0], dq), ("dk", grads[1], dk), ("dv", grads[2], dv)):
         assert rel_l2(got, ref) <= GRAD_TOL, name
@@ -112,29 +125,33 @@ def test_ring_steps_on_virtual_devices_match_oracle(name):
                                                      N, **geo, **kw)
     torch.cuda.synchronize()
     assert ra.ra_get_device_status() == ra.RA_OK
+    for t in list(outs) + list(dqs) + list(dks) + list(dvs):
+        assert t.dtype == w.torch_dtype  # results in the input dtype
     out = np.concatenate([f64(o) for o in outs], 1)
     lse = np.concatenate([f64(x) for x in lses], 2)
     grads = (np.concatenate([f64(x) for x in dqs], 1), np.concatenate([f64(x) for x in dks], 1),
              np.concatenate([f64(x) for x in dvs], 1), f64(dsinks))
-    _compare(w, inp, okw, out, lse, grads)
+    _compare(w, inp, okw, out, lse, grads, CASES[name].get("f32", False))
 
 
-def test_ring_step_forward_equals_the_fused_ring():
+@pytest.mark.parametrize("name", ["mqa_sinks_cap20_zigzag_n2", "fp32_gqa_sinks_cap20_zigzag_n4"])
+def test_ring_step_forward_equals_the_fused_ring(name):
     # the same ring, once step by step and once in the single-launch forward
     # (ra_attn_fwd over N virtual shards): both are the pages' ring; they
     # differ only in rounding
-    w, inp, d, kw, geo, okw = _prepare(CASES["mqa_sinks_cap20_zigzag_n2"])
+    w, inp, d, kw, geo, okw = _prepare(CASES[name])
     N = w.n_shards
     outs, lses = ring.ring_forward_local(d["q"], d["k"], d["v"], N, **geo, **kw)
     p = ra.make_params(d["q"], d["k"], scale=w.scale, causal=True, soft_cap=w.soft_cap,
-                       n_virtual_shards=N, is_mqa=True, q_pos=geo["q_pos"], kv_pos=geo["kv_pos"],
-                       sinks=d["sinks"])
+                       n_virtual_shards=N, is_mqa=w.is_mqa, q_pos=geo["q_pos"],
+                       kv_pos=geo["kv_pos"], sinks=d["sinks"])
     out_f, lse_f = ra.forward(p, d["q"], d["k"], d["v"], ra.build_mask(p))
     torch.cuda.synchronize()
     out = np.concatenate([f64(o) for o in outs], 1)
     lse = np.concatenate([f64(x) for x in lses], 2)
-    assert np.max(np.abs(out - f64(out_f))) <= O_TOL
-    assert np.max(np.abs(lse - f64(lse_f))) <= LSE_TOL
+    f32 = CASES[name].get("f32", False)
+    assert np.max(np.abs(out - f64(out_f))) <= (F32_O_TOL if f32 else O_TOL)
+    assert np.max(np.abs(lse - f64(lse_f))) <= (F32_LSE_TOL if f32 else LSE_TOL)
 
 
 def test_step_with_an_empty_chunk_and_sinks_keeps_the_running_pair():
@@ -178,6 +195,15 @@ def test_step_arguments_are_checked():
         ra.ra_attn_fwd_step(p1, q, q, q, m1, 8, o, lse)  # unknown flag
     with pytest.raises(ra.RaError):
         ra.ra_attn_fwd_step(p1, q, q, q, m1, 0, None, lse)
+    # fp32: the optional output may not share memory with the running output
+    q32 = torch.zeros(1, 256, 2, 128, device="cuda")
+    p32 = ra.make_params(q32, q32, scale=0.1, causal=True)
+    m32 = ra.build_mask(p32)
+    with pytest.raises(ra.RaError) as e:
+        ra.ra_attn_fwd_step(p32, q32, q32, q32, m32, ra.RA_STEP_FIRST, o, lse, o)
+    assert e.value.code == ra.RA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert ra.ra_get_device_status() == ra.RA_OK
 
 
 def _free_port():
