@@ -412,8 +412,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        // this CTA's workspace: O_run[2 heads] then staging[2 heads], (128, D) fp32 each
+        // this CTA's workspace: O_run[2 heads] then staging[2 heads], 128 x D
+        // fp32 each, stored by groups of four columns: group j of row r is the
+        // float4 at j * 128 + r, so that one warp's 32 rows of a group are 512
+        // contiguous bytes (a row-major slot would scatter every warp store
+        // over 32 lines).  Each thread only ever touches its own row.
         float *orun_base = ws + (size_t)blockIdx.x * 4 * kTile * kD2;
+        auto slot4 = [&](int sl) -> float4 * {
+            return reinterpret_cast<float4 *>(orun_base + (size_t)sl * kTile * kD2) + row;
+        };
         uint32_t nshard = 0, n_of = 0;
         bool ok = true;
         auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     w[h] = first[h] ? 1.f : sigmoid_fast(lse_s[h] - lse_run[h]);
                     // the first merge of the unit takes the block: O_s goes
                     // straight to O_run (or, if also the last, to the output)
-                    float *dst = orun_base + ((first[h] ? 0 : 2) + h) * kTile * kD2 + (size_t)row * kD2;
+                    float4 *dst4 = slot4((first[h] ? 0 : 2) + h);
                     __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h0 + h) * kD2;
 #pragma unroll
                     for (int c = 0; c < kD2 / 16; ++c) {
@@ -486,10 +493,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         if (first[h] && last) {
                             store_bf16_16(orow + c * 16, a);
                         } else {
-                            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 16);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                d4[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+                                dst4[(c * 4 + k) * kTile] =
+                                    make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
                         }
                     }
                 }
@@ -499,8 +506,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 // phase 2, per head: O_run -= w (O_run - O_s) from the staging slot
                 for (int h = 0; h < 2; ++h) {
                     if (!first[h]) {
-                        float *orun = orun_base + h * kTile * kD2 + (size_t)row * kD2;
-                        const float *stg = orun_base + (2 + h) * kTile * kD2 + (size_t)row * kD2;
+                        float4 *orun4 = slot4(h);
+                        const float4 *stg4 = slot4(2 + h);
                         __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h0 + h) * kD2;
                         const float wh = w[h];
 #pragma unroll 2
@@ -509,9 +516,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 // O_run is still (0, lse_run) after a sink-only step
-                                cv[k] = orun_set[h] ? reinterpret_cast<const float4 *>(orun + c * 16)[k]
+                                cv[k] = orun_set[h] ? orun4[(c * 4 + k) * kTile]
                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-                                sv[k] = reinterpret_cast<const float4 *>(stg + c * 16)[k];
+                                sv[k] = stg4[(c * 4 + k) * kTile];
                             }
                             float nv[16];
 #pragma unroll
@@ -526,7 +533,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                             } else {
 #pragma unroll
                                 for (int k = 0; k < 4; ++k)
-                                    reinterpret_cast<float4 *>(orun + c * 16)[k] =
+                                    orun4[(c * 4 + k) * kTile] =
                                         make_float4(nv[4 * k], nv[4 * k + 1], nv[4 * k + 2], nv[4 * k + 3]);
                             }
                         }
@@ -544,12 +551,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 __nv_bfloat16 *orow = out + (((size_t)x.b * p.Lq + qi) * p.Hq + x.h0 + h) * kD2;
                 if (!out_written[h]) {
                     if (orun_set[h]) {
-                        const float *orun = orun_base + h * kTile * kD2 + (size_t)row * kD2;
+                        const float4 *orun4 = slot4(h);
                         for (int c = 0; c < kD2 / 16; ++c) {
                             float a[16];
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                const float4 v4 = reinterpret_cast<const float4 *>(orun + c * 16)[k];
+                                const float4 v4 = orun4[(c * 4 + k) * kTile];
                                 a[4 * k] = v4.x;
                                 a[4 * k + 1] = v4.y;
                                 a[4 * k + 2] = v4.z;
