@@ -123,3 +123,22 @@ def test_bwd_needs_workspace_and_dsinks(L):
 
 def test_version(L):
     assert "sm_103a" in ra.ra_version()
+
+
+def test_ring_step_validation(L):
+    # checks that come before any device work, for both dtypes
+    for dt in (ra.RA_BF16, ra.RA_FP32):
+        m = ra.RaBlockMask()
+        p2 = _params(dtype=dt)  # two virtual shards: a ring step takes one chunk
+        assert L.ra_attn_fwd_step(ctypes.byref(p2), 16, 16, 16, ctypes.byref(m), 0, 16, 16, None,
+                                  None) == ra.RA_ERR_INVALID_ARG
+        assert "n_virtual_shards" in ra.ra_last_error()
+        p1 = _params(dtype=dt, n_virtual_shards=1)
+        assert L.ra_attn_fwd_step(ctypes.byref(p1), 16, 16, 16, ctypes.byref(m), 8, 16, 16, None,
+                                  None) == ra.RA_ERR_INVALID_ARG  # unknown flag
+        assert L.ra_attn_fwd_step(ctypes.byref(p1), 16, 16, 16, ctypes.byref(m), 0, None, 16, None,
+                                  None) == ra.RA_ERR_INVALID_ARG  # no running output
+        assert L.ra_attn_bwd_step(ctypes.byref(p2), 16, 16, 16, 16, ctypes.byref(m), 16, 16, 16,
+                                  4096, 1 << 20, None) == ra.RA_ERR_INVALID_ARG
+        assert L.ra_attn_bwd_step(ctypes.byref(p1), 16, 16, 16, 16, None, 16, 16, 16, 4096,
+                                  1 << 20, None) == ra.RA_ERR_INVALID_ARG  # no mask
