@@ -53,8 +53,9 @@ struct Problem {
     // global memory instead of being written as the final outputs.
     //   forward: run_out (B, Lq, Hq, D) and run_lse (B, Hq, Lq) are the
     //   running pair (read unless step_first, then written); step_sink counts
-    //   the sinks in this step; the bf16 `out` of the launch, if not NULL,
-    //   receives the merged result (the last step's cast).
+    //   the sinks in this step; the `out` of the launch (bf16, or fp32 for
+    //   fp32 inputs), if not NULL, receives the merged result (the last
+    //   step's cast).
     //   backward: acc_dq (B, Lq, Hq, D), acc_dk / acc_dv (B, Lkv, Hkv, D)
     //   receive += of the step's scaled gradients (hsplit == 1).
     float *run_out, *run_lse;
@@ -81,7 +82,8 @@ int mask_part_cap(int B, int nq, int nk);
 cudaError_t launch_merge(float *out, float *lse, const float *bout, const float *blse, int B,
                          int L, int H, int D, cudaStream_t s);
 // fp32 inputs: the forward on the tensor cores (kind::tf32, the logits from
-// three hi / lo products)
+// three hi / lo products); a ring step when p.run_out is set (out may then be
+// NULL)
 cudaError_t launch_fwd_f32_tc(const Problem &p, const float *q, const float *k, const float *v,
                               float *out, float *lse, cudaStream_t s);
 cudaError_t launch_fwd_tc(const Problem &p, const void *tm_q, const void *tm_k, const void *tm_v,
