@@ -29,7 +29,10 @@
 // MMA order per tile g: PV_A(g), S_A(g+1), PV_B(g), S_B(g+1): while one
 // head's softmax runs, the tensor pipe computes the other head's products,
 // and the two softmax warpgroups interleave their exponent phases on the
-// MUFU units instead of running them at the same time.  S_X(g+1) completing
+// MUFU units instead of running them at the same time.  Each PV product is
+// issued in two halves of 64 keys: the softmax publishes P of keys 0..63
+// (p_half) before it computes the exponents of keys 64..127 (p_full), so
+// the first half runs on the tensor pipe meanwhile.  S_X(g+1) completing
 // implies PV_X(g) has completed (one issuing lane, in order), so a softmax
 // warp never waits for a PV product separately.
 // The running output O_run of both heads lives in the caller's workspace
@@ -59,8 +62,8 @@ struct Fwd2Cfg {
     static constexpr int kBarOff = kVOff + kStages2 * kTileBytes2;
     // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2],
     // s_full[2 heads], p_full[2], stat_full[2 heads][2 slots], o_full[2],
-    // o_empty[2], drain
-    static constexpr int kNumBars = 2 + 4 * kStages2 + 2 + 2 + 4 + 2 + 2 + 1;
+    // o_empty[2], drain, p_half[2]
+    static constexpr int kNumBars = 2 + 4 * kStages2 + 2 + 2 + 4 + 2 + 2 + 1 + 2;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kStatOff = kMiscOff + 16; // l then m: [2 heads][2 slots][128] each
     static constexpr int kSmemUsed = kStatOff + 2 * 2 * 2 * 128 * 4;
@@ -73,7 +76,7 @@ struct Fwd2Cfg {
 
 struct Bars2 {
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
-        *stat_full, *o_full, *o_empty, *drain;
+        *stat_full, *o_full, *o_empty, *drain, *p_half;
 };
 
 __device__ __forceinline__ Bars2 carve_bars2(uint8_t *smem)
@@ -93,6 +96,7 @@ __device__ __forceinline__ Bars2 carve_bars2(uint8_t *smem)
     r.o_full = r.stat_full + 4;       // [head]
     r.o_empty = r.o_full + 2;         // [head]
     r.drain = r.o_empty + 2;
+    r.p_half = r.drain + 1;           // [head]: P of keys 0..63 is in TMEM
     return r;
 }
 
@@ -225,6 +229,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         for (int h = 0; h < 2; ++h) {
             mbar_init(bars.s_full + h, 1);
             mbar_init(bars.p_full + h, 128);
+            mbar_init(bars.p_half + h, 128);
             mbar_init(bars.stat_full + 2 * h, 128);
             mbar_init(bars.stat_full + 2 * h + 1, 128);
             mbar_init(bars.o_full + h, 1);
@@ -323,12 +328,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
             mma_ss_w(tmem + (TCOL), (QD) + o_, kd_ + o_, C::kIdescQK, kk > 0 ? 1u : 0u);             \
         }                                                                                          \
     } while (0)
-#define RA_ISSUE_PV(H, VS, FIRST)                                                                  \
+// half HF of the PV product: keys 64 HF .. 64 HF + 63 (P columns [32 HF, 32 HF + 32))
+#define RA_ISSUE_PV(H, VS, FIRST, HF)                                                              \
     do {                                                                                           \
         const uint64_t vd_ = dv + (uint64_t)(VS) * kStageStep;                                     \
-        _Pragma("unroll") for (int kk = 0; kk < kTile / 16; ++kk)                                  \
+        _Pragma("unroll") for (int k4 = 0; k4 < kTile / 32; ++k4) {                                \
+            const int kk = (HF) * (kTile / 32) + k4;                                               \
             mma_ts_w(tmem + C::kColO + (H) * 128, tmem + (H) * 128 + kk * 8,                         \
                    vd_ + (uint64_t)((kk * 2048) >> 4), C::kIdescPV, (kk > 0 || !(FIRST)) ? 1u : 0u); \
+        }                                                                                          \
     } while (0)
             for (int r = 0; ok && r * G < U; ++r) {
                 const int u = unit_index(r, blockIdx.x, G);
@@ -368,12 +376,16 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     }
                     const uint32_t vs = gv % kStages2;
                     ks = gk % kStages2;
-                    // head A: PV of this tile, then S of the next (its S buffer held P)
-                    if (!(ok = wait_w(bars.p_full + 0, gp & 1))) break;
+                    // head A: PV of this tile -- its first half as soon as the softmax
+                    // has stored P of keys 0..63 -- then S of the next (its S buffer held P)
+                    if (!(ok = wait_w(bars.p_half + 0, gp & 1))) break;
                     if (!(ok = wait_w(bars.v_full + vs, (gv / kStages2) & 1))) break;
                     if (cf && !(ok = wait_w(bars.o_empty + 0, (n_oe & 1) ^ 1))) break;
                     tc_fence_after();
-                    if (cf) RA_ISSUE_PV(0, vs, true); else RA_ISSUE_PV(0, vs, false);
+                    RA_ISSUE_PV(0, vs, cf, 0);
+                    if (!(ok = wait_w(bars.p_full + 0, gp & 1))) break;
+                    tc_fence_after();
+                    RA_ISSUE_PV(0, vs, false, 1);
                     if (cl) tc_commit_w(bars.o_full + 0);
                     if (has_next) {
                         if (!(ok = wait_w(bars.k_full + ks, (gk / kStages2) & 1))) break;
@@ -382,10 +394,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         tc_commit_w(bars.s_full + 0);
                     }
                     // head B, the same
-                    if (!(ok = wait_w(bars.p_full + 1, gp & 1))) break;
+                    if (!(ok = wait_w(bars.p_half + 1, gp & 1))) break;
                     if (cf && !(ok = wait_w(bars.o_empty + 1, (n_oe & 1) ^ 1))) break;
                     tc_fence_after();
-                    if (cf) RA_ISSUE_PV(1, vs, true); else RA_ISSUE_PV(1, vs, false);
+                    RA_ISSUE_PV(1, vs, cf, 0);
+                    if (!(ok = wait_w(bars.p_full + 1, gp & 1))) break;
+                    tc_fence_after();
+                    RA_ISSUE_PV(1, vs, false, 1);
                     tc_commit_w(bars.v_empty + vs);
                     if (cl) tc_commit_w(bars.o_full + 1);
                     if (cf) ++n_oe;
@@ -731,6 +746,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
                                 pk[j >> 1] = pack_bf16x2(e2.x, e2.y);
                             }
                             tmem_st32(lane_base + s_col + hh * 32, pk);
+                            if (hh == 0) {
+                                // keys 0..63 are in TMEM: the first half of PV may start
+                                tmem_st_wait();
+                                tc_fence_before();
+                                mbar_arrive(bars.p_half + hx);
+                            }
                         }
                     } else {
 #pragma unroll
@@ -746,6 +767,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
                             }
                             // P elements 64hh..64hh+63 -> columns [32hh, 32hh+32), already read
                             tmem_st32(lane_base + s_col + hh * 32, pk);
+                            if (hh == 0) {
+                                // keys 0..63 are in TMEM: the first half of PV may start
+                                tmem_st_wait();
+                                tc_fence_before();
+                                mbar_arrive(bars.p_half + hx);
+                            }
                         }
                     }
                     const float2 l01 = fadd2(ls[0], ls[1]), l23 = fadd2(ls[2], ls[3]);
